@@ -1,0 +1,470 @@
+"""Benchmark of the NF4 quantize + fused NF4-dequant matmul path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+for the default workload (a Qwen2.5-7B-shaped decoder layer, seven linear
+weights) it quantizes every fp32 weight (NF4, blocksize 64, double quant),
+runs the fused forward of every projection at M = 1, 64 and 2048 tokens and
+the fused input gradient at M = 2048. The printed `value` is the step's
+matmul FLOP divided by the device time of the step (quantization included in
+the time); per-kernel-class numbers, their roofline fractions and the
+quantize bandwidth are in `parts`.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+`--impl reference` times the CPU oracle (the plain fp64 reference the kernels
+are checked against) on a bounded sample of the same workload on this host's
+cores. Under torchrun each rank runs its own replica (weak scaling) and rank 0
+prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dequant_gemm_gb300 import workloads as wl  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------- work accounting --
+def packed_bytes(rows, cols):
+    n = rows * cols
+    nb = n // 64
+    return n // 2 + nb + 4 * ((nb + 255) // 256)
+
+
+def fwd_work(p, M):
+    """(flop, algorithmic bytes) of Y = X W^T: packed W + X in + Y out."""
+    return 2 * M * p.rows * p.cols, packed_bytes(p.rows, p.cols) + 2 * M * p.cols + 4 * M * p.rows
+
+
+def dx_work(p, M):
+    return 2 * M * p.rows * p.cols, packed_bytes(p.rows, p.cols) + 2 * M * p.rows + 4 * M * p.cols
+
+
+def quant_bytes(p):
+    return 4 * p.rows * p.cols + packed_bytes(p.rows, p.cols)
+
+
+# --------------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nf4_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax = max(smax, float(f[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+            os.unlink(self.path)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our workload --
+class Step:
+    """Device buffers and the call list of one step of a workload."""
+
+    def __init__(self, name, device, rotate=1):
+        import dequant_gemm_gb300 as nf4
+        self.nf4 = nf4
+        self.w = wl.WORKLOADS[name]
+        self.dev = device
+        self.rotate = rotate
+        self.weights = []       # fp32 weights (inputs of quantize)
+        self.q = []             # quantized weights, one set per rotation copy
+        self.x = {}             # (K, M) -> bf16 activations
+        self.dy = {}            # (N, M) -> bf16 output gradients
+        self.y = {}             # (proj index, M) -> fp32 outputs
+        self.dx = {}
+        for i, p in enumerate(self.w.projections):
+            W = p.make_weight().to(device)
+            self.weights.append(W)
+        for r in range(rotate):
+            self.q.append([nf4.nf4_quantize(W) for W in self.weights])
+        for i, p in enumerate(self.w.projections):
+            for M in self.w.fwd_m:
+                if (p.cols, M) not in self.x:
+                    self.x[(p.cols, M)] = wl.activations(M, p.cols, std=self.w.x_std,
+                                                         seed=wl.SEED_X + M).to(device)
+                self.y[(i, M)] = torch.empty(M, p.rows, dtype=torch.float32, device=device)
+            for M in self.w.dx_m:
+                if (p.rows, M) not in self.dy:
+                    self.dy[(p.rows, M)] = wl.activations(M, p.rows, std=self.w.dy_std,
+                                                          seed=wl.SEED_X + 7 + M).to(device)
+                self.dx[(i, M)] = torch.empty(M, p.cols, dtype=torch.float32, device=device)
+        self.quantize_in_step = rotate == 1
+        self.calls = self._calls()
+
+    def _calls(self):
+        """List of (category, flop, bytes, launches, fn(rot)) in step order."""
+        nf4 = self.nf4
+        calls = []
+        P = self.w.projections
+        if self.quantize_in_step:
+            for i, p in enumerate(P):
+                calls.append(("quantize", 0, quant_bytes(p), 1,
+                              lambda r, i=i: nf4.nf4_quantize(self.weights[i], out=self.q[r][i])))
+        for M in sorted(self.w.fwd_m, reverse=True):
+            for i, p in enumerate(P):
+                f, b = fwd_work(p, M)
+                calls.append((f"fwd_M{M}", f, b, 1,
+                              lambda r, i=i, M=M, p=p: nf4.nf4_matmul_fwd(
+                                  self.x[(p.cols, M)], self.q[r][i], out=self.y[(i, M)])))
+        for M in self.w.dx_m:
+            for i, p in enumerate(P):
+                f, b = dx_work(p, M)
+                calls.append((f"dx_M{M}", f, b, 1,
+                              lambda r, i=i, M=M, p=p: nf4.nf4_matmul_bwd_dx(
+                                  self.dy[(p.rows, M)], self.q[r][i], out=self.dx[(i, M)])))
+        return calls
+
+    def flop(self):
+        return sum(c[1] for c in self.calls)
+
+    def launches(self):
+        return sum(c[3] for c in self.calls)
+
+    def run(self, r, events=None):
+        for k, (cat, _, _, _, fn) in enumerate(self.calls):
+            if events is not None:
+                events[k][0].record()
+            fn(r)
+            if events is not None:
+                events[k][1].record()
+
+    # end to end: host inputs -> device, step, outputs -> host
+    def host_buffers(self):
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        self.h_w = [pin(W) for W in self.weights] if self.quantize_in_step else []
+        self.h_x = {k: pin(v) for k, v in self.x.items()}
+        self.h_dy = {k: pin(v) for k, v in self.dy.items()}
+        self.h_y = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.y.items()}
+        self.h_dx = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.dx.items()}
+        h2d = sum(t.numel() * t.element_size() for t in
+                  self.h_w + list(self.h_x.values()) + list(self.h_dy.values()))
+        d2h = sum(t.numel() * t.element_size() for t in
+                  list(self.h_y.values()) + list(self.h_dx.values()))
+        return h2d, d2h
+
+    def run_e2e(self, r):
+        for W, hW in zip(self.weights, self.h_w):
+            W.copy_(hW, non_blocking=True)
+        for k, v in self.x.items():
+            v.copy_(self.h_x[k], non_blocking=True)
+        for k, v in self.dy.items():
+            v.copy_(self.h_dy[k], non_blocking=True)
+        self.run(r)
+        for k, v in self.y.items():
+            self.h_y[k].copy_(v, non_blocking=True)
+        for k, v in self.dx.items():
+            self.h_dx[k].copy_(v, non_blocking=True)
+
+
+# ------------------------------------------------------------ oracle sample --
+def oracle_sample(name, budget_s=15.0):
+    """Time the CPU oracle on a bounded sample of the workload: for each
+    projection, quantize + dequantize a few rows (whole groups) and multiply
+    them in fp64 against the activations of every forward and dX shape.
+    Returns (matmul flop/s, description, cores)."""
+    from oracle import nf4_oracle as o
+    w = wl.WORKLOADS[name]
+    t_total, flop_total, rows_total = 0.0, 0, 0
+    g = np.random.default_rng(0)
+    per_proj = max(4, int(64 / len(w.projections)))
+    for p in w.projections:
+        W = p.make_weight().numpy()
+        K = p.cols
+        # whole groups covering `per_proj` consecutive rows from a random start
+        r0 = int(g.integers(0, max(1, p.rows - per_proj)))
+        lo = (r0 * K) // 16384 * 16384
+        hi = min(((r0 + per_proj) * K + 16383) // 16384 * 16384, p.rows * K)
+        xs = [wl.activations(M, K, std=w.x_std, seed=wl.SEED_X + M).float().numpy()
+              for M in w.fwd_m]
+        dys = [wl.activations(M, p.rows, std=w.dy_std).float().numpy()[:, :per_proj]
+               for M in w.dx_m]
+        t0 = time.perf_counter()
+        packed, a8, s2 = o.quantize_flat(W.reshape(-1)[lo:hi])
+        what = o.dequantize_flat(packed, a8, s2)
+        rows = what[(r0 * K - lo):(r0 * K - lo) + per_proj * K].reshape(per_proj, K)
+        for X in xs:
+            o.matmul_fwd(X, rows)
+            flop_total += 2 * X.shape[0] * per_proj * K
+        for dY in dys:
+            o.matmul_bwd_dx(dY, rows)
+            flop_total += 2 * dY.shape[0] * per_proj * K
+        t_total += time.perf_counter() - t0
+        rows_total += per_proj
+        if t_total > budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = (f"{rows_total} weight rows ({per_proj} per projection, whole 16384-weight groups "
+            f"quantized + dequantized) x every forward and dX token count of {name}; "
+            "numpy fp64, BLAS threads = host cores")
+    return flop_total / t_total, desc, cores, t_total
+
+
+# ------------------------------------------------------------------- helpers --
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.workload]
+    vals, descs, cores = [], None, None
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, budget_s=2.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, descs, cores, _ = oracle_sample(args.workload, budget_s=10.0)
+        vals.append(v)
+    dt = time.perf_counter() - t0
+    value = statistics.median(vals) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": descs},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = ("fused NF4 matmul TFLOP/s and HBM GB/s vs roofline; nf4_quantize GB/s "
+          "(value: matmul FLOP of one layer step / device time of the step, quantization included)")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen2.5_7b_layer", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the NF4 kernels have no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import dequant_gemm_gb300 as nf4
+    nf4.lib()
+
+    work = wl.WORKLOADS[args.workload]
+    ws_bytes = sum(4 * p.rows * p.cols for p in work.projections)
+    rotate = 1 if ws_bytes > L2_BYTES else max(2, int(np.ceil(3 * L2_BYTES / sum(
+        packed_bytes(p.rows, p.cols) for p in work.projections))))
+    step = Step(args.workload, dev, rotate=rotate)
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        step.run(i % rotate)
+    status = nf4.nf4_poll_device_status(dev)
+    if status != 0:
+        raise SystemExit(f"device status {status} after warm-up")
+
+    ncalls = len(step.calls)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ncalls * args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step.run(s % rotate, events[s * ncalls:(s + 1) * ncalls])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    status = nf4.nf4_poll_device_status(dev)
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed steps")
+
+    # per-category device time from the per-call events
+    cat_ms, cat_flop, cat_bytes, cat_n = {}, {}, {}, {}
+    for s in range(args.steps):
+        for k, (cat, f, b, n, _) in enumerate(step.calls):
+            e0, e1 = events[s * ncalls + k]
+            cat_ms[cat] = cat_ms.get(cat, 0.0) + e0.elapsed_time(e1)
+            cat_flop[cat] = cat_flop.get(cat, 0) + f
+            cat_bytes[cat] = cat_bytes.get(cat, 0) + b
+            cat_n[cat] = cat_n.get(cat, 0) + n
+
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    flop_step = step.flop()
+    value = world * flop_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    pk, pk_kind = peaks()
+    parts = {}
+    for cat in cat_ms:
+        t = cat_ms[cat] * 1e-3
+        gbs = cat_bytes[cat] / t / 1e9
+        tf = cat_flop[cat] / t / 1e12
+        parts[cat] = {"ms_per_step": cat_ms[cat] / args.steps, "launches_per_step": cat_n[cat] // args.steps,
+                      "TFLOP/s": tf, "GB/s": gbs,
+                      "hbm_frac": gbs / pk["hbm_gbs"],
+                      "tensor_frac": tf / pk["bf16_tflops_sustained"]}
+    dom = max(cat_ms, key=cat_ms.get)
+    d = parts[dom]
+    tensor_bound = cat_flop[dom] / max(1, cat_bytes[dom]) > (1e3 * pk["bf16_tflops_sustained"] / pk["hbm_gbs"])
+    if cat_flop[dom] == 0 or not tensor_bound:
+        roof = {"bound": "hbm", "achieved": d["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": d["GB/s"] / pk["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": d["TFLOP/s"] / pk["bf16_tflops_sustained"]}
+    roof.update({"kernel": dom, "traffic": None, "peak_kind": f"{pk_kind} ("
+                 + ("sustained bf16" if roof["bound"] == "tensor" else "copy") + ")"})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": work.name,
+                   "projections": [f"{p.name} {p.rows}x{p.cols}" for p in work.projections],
+                   "fwd_m": list(work.fwd_m), "dx_m": list(work.dx_m),
+                   "quantize_in_step": step.quantize_in_step,
+                   "l2": ("inputs larger than L2: %.2f GB of fp32 weights read per step" % (ws_bytes / 1e9))
+                   if rotate == 1 else f"rotating over {rotate} quantized copies (> 3x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": step.launches() * args.steps,
+        "roofline": roof,
+        "parts": parts,
+    }
+    if clk:
+        line["clocks"] = clk
+
+    if not args.no_e2e:
+        h2d, d2h = step.host_buffers()
+        for i in range(2):
+            step.run_e2e(i % rotate)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for s in range(args.steps):
+            step.run_e2e(s % rotate)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        line["e2e"] = {"value": world * flop_step * args.steps / (e2e_ms * 1e-3) / 1e12,
+                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms / args.steps}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, cores, secs = oracle_sample(args.workload, budget_s=20.0)
+        line["cpu_baseline"] = {"value": v / 1e12, "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle", "sample": desc, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,205 @@
+"""GB300-native NF4 quantization and fused NF4-dequant matmul.
 
+A thin Python binding over the C ABI of ``libnf4gemm.so`` (declared in
+``include/nf4gemm.h``): the functions below only allocate outputs with
+PyTorch, marshal pointers and the current CUDA stream, and raise on a
+non-OK status. Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback, and a missing library is an
+error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+BLOCKSIZE = 64
+DQ_GROUP = 256
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnf4gemm.so")
+
+STATUS = {
+    0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_ALIGN",
+    4: "NF4_ERR_BLOCKSIZE", 5: "NF4_ERR_DEVICE", 6: "NF4_ERR_LAUNCH",
+    7: "NF4_ERR_DEVICE_TIMEOUT",
+}
+
+# Every symbol the header declares, for load checks.
+EXPORTS = ("nf4_quantize", "nf4_dequantize", "nf4_matmul_fwd", "nf4_matmul_bwd_dx",
+           "nf4_poll_device_status", "nf4_codebook", "nf4_status_string")
+
+
+class NF4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+class nf4_weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("absmax_q", ctypes.c_void_p),
+                ("absmax_scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("blocksize", ctypes.c_int32),
+                ("dq_group", ctypes.c_int32)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m dequant_gemm_gb300.build` "
+                    "(the NF4 kernels have no fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+            W = ctypes.POINTER(nf4_weight)
+            sig = {
+                "nf4_quantize": [vp, i64, i64, i32, vp, vp, vp, vp],
+                "nf4_dequantize": [W, vp, vp],
+                "nf4_matmul_fwd": [vp, i64, W, vp, vp],
+                "nf4_matmul_bwd_dx": [vp, i64, W, vp, vp],
+                "nf4_poll_device_status": [vp],
+                "nf4_codebook": [vp],
+            }
+            for name, args in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int32
+            L.nf4_status_string.argtypes = [ctypes.c_int32]
+            L.nf4_status_string.restype = ctypes.c_char_p
+            _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().nf4_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise NF4Error(fn, status)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+@dataclass
+class NF4Weight:
+    """A quantized weight: codes, absmax codes, second-level scales, shape
+    (the QuantState of the bitsandbytes page). Plain tensors; save them with
+    torch.save."""
+    codes: torch.Tensor          # uint8 [rows*cols/2]
+    absmax_q: torch.Tensor       # uint8 [rows*cols/64]
+    absmax_scale: torch.Tensor   # float32 [ceil(rows*cols/16384)]
+    rows: int
+    cols: int
+
+    def c_struct(self) -> nf4_weight:
+        return nf4_weight(self.codes.data_ptr(), self.absmax_q.data_ptr(),
+                          self.absmax_scale.data_ptr(), self.rows, self.cols, BLOCKSIZE, DQ_GROUP)
+
+    @property
+    def device(self) -> torch.device:
+        return self.codes.device
+
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.absmax_q.numel() + 4 * self.absmax_scale.numel()
+
+
+def _require_cuda(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def alloc_weight(rows: int, cols: int, device) -> NF4Weight:
+    n = rows * cols
+    nb = n // BLOCKSIZE
+    ng = (nb + DQ_GROUP - 1) // DQ_GROUP
+    return NF4Weight(torch.empty(n // 2, dtype=torch.uint8, device=device),
+                     torch.empty(nb, dtype=torch.uint8, device=device),
+                     torch.empty(ng, dtype=torch.float32, device=device), rows, cols)
+
+
+def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None) -> NF4Weight:
+    """NF4-quantize an fp32 [rows, cols] CUDA tensor (blocksize 64, double quant)."""
+    _require_cuda(W, "W", torch.float32)
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [rows, cols]")
+    rows, cols = W.shape
+    q = out if out is not None else alloc_weight(rows, cols, W.device)
+    with torch.cuda.device(W.device):
+        _check("nf4_quantize", lib().nf4_quantize(
+            _ptr(W), rows, cols, BLOCKSIZE, _ptr(q.codes), _ptr(q.absmax_q),
+            _ptr(q.absmax_scale), _stream(W.device)))
+    return q
+
+
+def nf4_dequantize(w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 [rows, cols] dequantized weight (for checks and export only)."""
+    y = out if out is not None else torch.empty(w.rows, w.cols, dtype=torch.float32,
+                                                device=w.device)
+    s = w.c_struct()
+    with torch.cuda.device(w.device):
+        _check("nf4_dequantize", lib().nf4_dequantize(ctypes.byref(s), _ptr(y), _stream(w.device)))
+    return y
+
+
+def nf4_matmul_fwd(X: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y = X * dequant(W)^T; X bf16 [M, cols] -> Y fp32 [M, rows]."""
+    _require_cuda(X, "X", torch.bfloat16)
+    if X.dim() != 2 or X.shape[1] != w.cols:
+        raise ValueError(f"X must be [M, {w.cols}]")
+    M = X.shape[0]
+    y = out if out is not None else torch.empty(M, w.rows, dtype=torch.float32, device=X.device)
+    s = w.c_struct()
+    with torch.cuda.device(X.device):
+        _check("nf4_matmul_fwd", lib().nf4_matmul_fwd(_ptr(X), M, ctypes.byref(s), _ptr(y),
+                                                      _stream(X.device)))
+    return y
+
+
+def nf4_matmul_bwd_dx(dY: torch.Tensor, w: NF4Weight,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    """dX = dY * dequant(W); dY bf16 [M, rows] -> dX fp32 [M, cols]. No dW."""
+    _require_cuda(dY, "dY", torch.bfloat16)
+    if dY.dim() != 2 or dY.shape[1] != w.rows:
+        raise ValueError(f"dY must be [M, {w.rows}]")
+    M = dY.shape[0]
+    y = out if out is not None else torch.empty(M, w.cols, dtype=torch.float32, device=dY.device)
+    s = w.c_struct()
+    with torch.cuda.device(dY.device):
+        _check("nf4_matmul_bwd_dx", lib().nf4_matmul_bwd_dx(_ptr(dY), M, ctypes.byref(s), _ptr(y),
+                                                            _stream(dY.device)))
+    return y
+
+
+def nf4_poll_device_status(device=None) -> int:
+    """Synchronize the current stream and return (and clear) the device status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().nf4_poll_device_status(_stream(dev)))
+
+
+def nf4_codebook() -> torch.Tensor:
+    """The 16 fp32 NF4 levels compiled into the library (host only)."""
+    buf = (ctypes.c_float * 16)()
+    _check("nf4_codebook", lib().nf4_codebook(ctypes.cast(buf, ctypes.c_void_p)))
+    return torch.tensor(list(buf), dtype=torch.float32)

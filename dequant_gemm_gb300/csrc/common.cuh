@@ -1,0 +1,82 @@
+// Shared definitions of the NF4 CUDA library (device side and host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "nf4gemm.h"
+
+namespace nf4 {
+
+constexpr int kBlock = 64;                    // weights per absmax block
+constexpr int kGroup = 256;                   // blocks per second-level scale
+constexpr int kGroupElems = kBlock * kGroup;  // 16384 weights per group
+
+// The 16 NF4 levels: standard-normal quantiles at evenly spaced probabilities
+// (8 on the positive side from delta = (1 - 1/30 + 1 - 1/32) / 2 to 1/2,
+// 7 on the negative side), an exact 0, all divided by Phi^-1(delta) and
+// rounded once to fp32 ("bitsandbytes", NF4 paragraph: levels derived from
+// the inverse normal CDF). Stored as bit patterns.
+constexpr uint32_t kLevelBits[16] = {
+    0xbf800000u, 0xbf3239b1u, 0xbf066b2eu, 0xbeca329eu, 0xbe91a24bu, 0xbe3d353du,
+    0xbdba7869u, 0x00000000u, 0x3da2fb01u, 0x3e24cadfu, 0x3e7c04dau, 0x3ead0336u,
+    0x3ee1a4b5u, 0x3f1007a9u, 0x3f3913b0u, 0x3f800000u};
+
+// Device copy of the levels for run-time indexing (one per translation unit).
+static __constant__ uint32_t kLevelBitsDev[16] = {
+    0xbf800000u, 0xbf3239b1u, 0xbf066b2eu, 0xbeca329eu, 0xbe91a24bu, 0xbe3d353du,
+    0xbdba7869u, 0x00000000u, 0x3da2fb01u, 0x3e24cadfu, 0x3e7c04dau, 0x3ead0336u,
+    0x3ee1a4b5u, 0x3f1007a9u, 0x3f3913b0u, 0x3f800000u};
+
+// Decision thresholds between neighbouring levels: t[i] is the largest fp32
+// value not above the exact midpoint (c[i] + c[i+1]) / 2. For an fp32 x the
+// nearest level, ties to the lower index, is #{i : x > t[i]}. A constexpr
+// function so that unrolled device loops see immediates.
+__host__ __device__ constexpr uint32_t threshold_bits(int i) {
+  return i == 0 ? 0xbf591cd9u : i == 1 ? 0xbf1c5270u : i == 2 ? 0xbeeb847du
+       : i == 3 ? 0xbeadea75u : i == 4 ? 0xbe703ceau : i == 5 ? 0xbe0d38b9u
+       : i == 6 ? 0xbd3a7869u : i == 7 ? 0x3d22fb01u : i == 8 ? 0x3df6485fu
+       : i == 9 ? 0x3e5067dcu : i == 10 ? 0x3e9582d1u : i == 11 ? 0x3ec753f5u
+       : i == 12 ? 0x3f006d01u : i == 13 ? 0x3f248dacu : 0x3f5c89d8u;
+}
+
+__host__ __device__ inline float bits_to_float(uint32_t b) {
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(b);
+#else
+  union { uint32_t u; float f; } v;
+  v.u = b;
+  return v.f;
+#endif
+}
+
+// Device status word values (the library's nf4_status codes).
+constexpr int kStatusTimeout = NF4_ERR_DEVICE_TIMEOUT;
+
+// Record a device-side failure without trapping.
+__device__ inline void report_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Second-level dequant: ahat = fl32(fl32(a8 * s2) / 255), both IEEE RN.
+__device__ __forceinline__ float dequant_absmax(uint32_t a8, float s2) {
+  return __fdiv_rn(__fmul_rn(static_cast<float>(a8), s2), 255.0f);
+}
+
+}  // namespace nf4
+
+// Kernel launchers (each returns cudaGetLastError() of its launch).
+namespace nf4 {
+cudaError_t launch_quantize(const float* W, int64_t n_elems, uint8_t* codes, uint8_t* a8,
+                            float* s2, cudaStream_t st);
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const float* s2,
+                              int64_t n_elems, float* out, cudaStream_t st);
+cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
+                            const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
+                            int num_sms, cudaStream_t st);
+cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,
+                           const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* dX,
+                           int num_sms, cudaStream_t st);
+}  // namespace nf4

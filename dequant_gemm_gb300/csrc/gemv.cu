@@ -1,0 +1,394 @@
+// Small-M fused NF4-dequant matmul: Y = X * dequant(W)^T for M <= 16 tokens
+// (decode shapes), and a plain fp32 input-gradient kernel for small M
+// ("Zenbit", zenbit.pallas_nf4 bullet: the compressed weight is streamed and
+// dequantized on chip; the full-precision weight never reaches HBM).
+//
+// Forward design (HBM-bound: 0.516 B of weight per 2*M flops):
+//  * CTA = 8 warps = 128 weight rows (16 per warp) x one K-slice of `bs`
+//    absmax blocks; K-slices of the same rows are summed with vector atomics
+//    into a zeroed Y when there is more than one.
+//  * The weight is the A operand of mma.sync.m16n8k16 (16 rows per warp), the
+//    tokens are the N operand (8 per n-tile): the "swap AB" shape for skinny
+//    products.
+//  * Dequantization is factored as  sum_b ahat_b * (sum_{k in b} x_k c[q_k]):
+//    the MMA consumes the raw levels c[q] and each 64-weight block's partial
+//    sum is scaled by its dequantized absmax in fp32 afterwards. The levels
+//    enter the tensor core as fp16 (relative error <= 2^-12), which needs the
+//    activations in fp16 too: each token's slice of X is scaled by a power of
+//    two that puts its max |x| in [2^14, 2^15) before conversion (exact for
+//    bf16 values), and the scale is removed from the fp32 result.
+//  * One packed byte (two adjacent weights) becomes one f16x2 fragment
+//    register through a 256-entry table held in 32 copies, one per lane, so
+//    that every lookup of a warp hits 32 distinct banks.
+//  * Within a block the 4 threads of an MMA quad each own 16 contiguous k
+//    (8 code bytes); the reduction order over k is permuted consistently in A
+//    and B, which leaves the sum unchanged.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace nf4 {
+namespace {
+
+constexpr int kGemvThreads = 256;
+constexpr int kGemvRows = 128;
+constexpr int kTabBytes = 256 * 32 * 4;
+constexpr int kMaxSliceBlocks = 32;
+constexpr int kOutStride = kGemvRows + 4;   // floats, keeps rows 16-byte aligned
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 ldg_codes(const uint8_t* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+struct GemvArgs {
+  const uint16_t* X;     // bf16 [M, K]
+  const uint8_t* codes;  // [N*K/2]
+  const uint8_t* a8;     // [N*K/64]
+  const float* s2;       // [groups]
+  float* Y;              // fp32 [M, N]
+  int64_t M, N, K;
+  int nblk;              // K / 64
+  int bs;                // blocks per K-slice
+  int slices;            // number of K-slices
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kGemvThreads)
+gemv_fwd_kernel(const GemvArgs p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
+  float* ahat_s = reinterpret_cast<float*>(smem + kTabBytes);
+  float* xinv = ahat_s + kGemvRows * p.bs;
+  const int xstride_b = p.bs * 128 + 8;  // bytes per token row of the fp16 slice
+  uint8_t* xs = reinterpret_cast<uint8_t*>(xinv + 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kGemvRows;
+  const int kb0 = blockIdx.y * p.bs;
+  const int nb = min(p.bs, p.nblk - kb0);
+  const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
+  const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
+  const int64_t rowg = row0 + warp * 16 + g, rowg8 = rowg + 8;
+  const int64_t rowbytes = p.K / 2;
+
+  // Codes of this thread: rows g and g+8 of the warp, 8 bytes per block.
+  const uint8_t* cg_ptr = p.codes + rowg * rowbytes + static_cast<int64_t>(kb0) * 32 + t * 8;
+  const uint8_t* cg8_ptr = cg_ptr + 8 * rowbytes;
+  const bool vg = rowg < p.N, vg8 = rowg8 < p.N;
+  uint2 cur[4][2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    cur[j][0] = (vg && j < nb) ? ldg_codes(cg_ptr + j * 32) : make_uint2(0u, 0u);
+    cur[j][1] = (vg8 && j < nb) ? ldg_codes(cg8_ptr + j * 32) : make_uint2(0u, 0u);
+  }
+
+  // Level table: entry b of copy l at word 32 b + l; low half = level of the
+  // high nibble (the even, lower-k element), high half = level of the low one.
+  for (int i = tid; i < 256 * 32; i += kGemvThreads) {
+    const int b = i >> 5;
+    const __half lo = __float2half_rn(__uint_as_float(kLevelBitsDev[b >> 4]));
+    const __half hi = __float2half_rn(__uint_as_float(kLevelBitsDev[b & 15]));
+    tab[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+             (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+  }
+  // Dequantized absmax of the CTA's rows over the slice.
+  for (int i = tid; i < kGemvRows * nb; i += kGemvThreads) {
+    const int r = i / nb, j = i - r * nb;
+    const int64_t n = row0 + r;
+    float v = 0.0f;
+    if (n < p.N) {
+      const int64_t bi = n * p.nblk + kb0 + j;
+      v = dequant_absmax(p.a8[bi], p.s2[bi / kGroup]);
+    }
+    ahat_s[r * p.bs + j] = v;
+  }
+  // Activations of the slice: per-token power-of-two scale, then fp16.
+  const int nkv = nb * kBlock;
+  for (int tk = warp; tk < 16; tk += kGemvThreads / 32) {
+    const bool valid = tk < mt;
+    const uint2* xr = reinterpret_cast<const uint2*>(
+        p.X + (m0 + (valid ? tk : 0)) * p.K + static_cast<int64_t>(kb0) * kBlock);
+    float mx = 0.0f;
+    if (valid) {
+      for (int i = lane; i < nkv / 4; i += 32) {
+        const uint2 v = __ldg(xr + i);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))));
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    int e = 0;
+    if (mx > 0.0f) {
+      const int E = max(1, static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu));
+      e = min(141 - E, 126);
+    }
+    const float scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    if (lane == 0) xinv[tk] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    uint2* dst = reinterpret_cast<uint2*>(xs + tk * xstride_b);
+    for (int i = lane; i < nkv / 4; i += 32) {
+      uint2 o = make_uint2(0u, 0u);
+      if (valid) {
+        const uint2 v = __ldg(xr + i);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
+        const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
+        o.x = *reinterpret_cast<const uint32_t*>(&h0);
+        o.y = *reinterpret_cast<const uint32_t*>(&h1);
+      }
+      dst[i] = o;
+    }
+  }
+  __syncthreads();
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+
+  const uint8_t* tab_b = reinterpret_cast<const uint8_t*>(tab) + lane * 4;
+  const float* ah_g = ahat_s + (warp * 16 + g) * p.bs;
+  const float* ah_g8 = ah_g + 8 * p.bs;
+
+  for (int j0 = 0; j0 < nb; j0 += 4) {
+    uint2 nxt[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int jn = j0 + 4 + j;
+      nxt[j][0] = (vg && jn < nb) ? ldg_codes(cg_ptr + jn * 32) : make_uint2(0u, 0u);
+      nxt[j][1] = (vg8 && jn < nb) ? ldg_codes(cg8_ptr + jn * 32) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = j0 + jj;
+      if (j < nb) {
+        float part[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) part[nt][i] = 0.0f;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t wg = (s < 2) ? cur[jj][0].x : cur[jj][0].y;
+          const uint32_t wg8 = (s < 2) ? cur[jj][1].x : cur[jj][1].y;
+          const int sh = 16 * (s & 1);
+          // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg >> sh) & 0xffu) << 7));
+          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg >> (sh + 8)) & 0xffu) << 7));
+          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg8 >> sh) & 0xffu) << 7));
+          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = *reinterpret_cast<const uint2*>(
+                xs + (nt * 8 + g) * xstride_b + (j * 64 + t * 16 + 4 * s) * 2);
+            mma_f16(part[nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+        const float ag = ah_g[j], ag8 = ah_g8[j];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[nt][0] = fmaf(ag, part[nt][0], acc[nt][0]);
+          acc[nt][1] = fmaf(ag, part[nt][1], acc[nt][1]);
+          acc[nt][2] = fmaf(ag8, part[nt][2], acc[nt][2]);
+          acc[nt][3] = fmaf(ag8, part[nt][3], acc[nt][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      cur[j][0] = nxt[j][0];
+      cur[j][1] = nxt[j][1];
+    }
+  }
+
+  // Epilogue: undo the token scales, stage [16 tokens x 128 rows] in shared
+  // memory, then one 16-byte store (or vector atomic add) per 4 rows.
+  __syncthreads();
+  float* out_s = reinterpret_cast<float*>(smem);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
+    const int rg = warp * 16 + g;
+    out_s[tk0 * kOutStride + rg] = acc[nt][0] * xinv[tk0];
+    out_s[tk1 * kOutStride + rg] = acc[nt][1] * xinv[tk1];
+    out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * xinv[tk0];
+    out_s[tk1 * kOutStride + rg + 8] = acc[nt][3] * xinv[tk1];
+  }
+  __syncthreads();
+  for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
+    const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
+    if (tk < mt && row0 + r4 < p.N) {
+      const float4 v = *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4);
+      float4* dst = reinterpret_cast<float4*>(p.Y + (m0 + tk) * p.N + row0 + r4);
+      if (p.slices == 1) {
+        *dst = v;
+      } else {
+        atomicAdd(dst, v);
+      }
+    }
+  }
+}
+
+// Input gradient for small M in plain fp32: dX[m, k] = sum_n dY[m, n] w[n, k].
+// CTA = 256 consecutive k (4 absmax blocks) x a slice of rows n; one thread
+// per k column; dY and the dequantized absmax of 64 rows at a time are staged
+// in shared memory. Slices of n are summed with atomics into a zeroed dX.
+constexpr int kDxThreads = 256;
+constexpr int kDxRows = 64;
+constexpr int kDxMaxM = 16;
+
+__global__ void __launch_bounds__(kDxThreads)
+simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __restrict__ codes,
+               const uint8_t* __restrict__ a8, const float* __restrict__ s2, int64_t N,
+               int64_t K, float* __restrict__ dX, int64_t rows_per_slice, int atomic_out) {
+  __shared__ float s_levels[16];
+  __shared__ float s_ahat[kDxRows][4];
+  __shared__ float s_dy[kDxMaxM][kDxRows];
+  const int tid = threadIdx.x;
+  if (tid < 16) s_levels[tid] = __uint_as_float(kLevelBitsDev[tid]);
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * kDxThreads + tid;
+  const int64_t kb_base = (static_cast<int64_t>(blockIdx.x) * kDxThreads) / kBlock;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.z) * kDxMaxM;
+  const int mt = static_cast<int>(min(static_cast<int64_t>(kDxMaxM), M - m0));
+  const int64_t n_begin = blockIdx.y * rows_per_slice;
+  const int64_t n_end = min(N, n_begin + rows_per_slice);
+  const int64_t nblk = K / kBlock;
+  float acc[kDxMaxM];
+#pragma unroll
+  for (int m = 0; m < kDxMaxM; ++m) acc[m] = 0.0f;
+
+  for (int64_t n0 = n_begin; n0 < n_end; n0 += kDxRows) {
+    __syncthreads();
+    {
+      const int r = tid >> 2, j = tid & 3;
+      const int64_t n = n0 + r;
+      float v = 0.0f;
+      if (n < n_end && kb_base + j < nblk) {
+        const int64_t bi = n * nblk + kb_base + j;
+        v = dequant_absmax(a8[bi], s2[bi / kGroup]);
+      }
+      s_ahat[r][j] = v;
+    }
+    for (int i = tid; i < kDxMaxM * kDxRows; i += kDxThreads) {
+      const int m = i / kDxRows, r = i % kDxRows;
+      const int64_t n = n0 + r;
+      float v = 0.0f;
+      if (m < mt && n < n_end) {
+        const uint16_t bits = dY[(m0 + m) * N + n];
+        v = __bfloat162float(__ushort_as_bfloat16(bits));
+      }
+      s_dy[m][r] = v;
+    }
+    __syncthreads();
+    if (k < K) {
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kDxRows), n_end - n0));
+      for (int r = 0; r < rows; ++r) {
+        const uint8_t byte = codes[((n0 + r) * K + k) >> 1];
+        const uint32_t q = (k & 1) ? (byte & 15u) : (byte >> 4);
+        const float w = __fmul_rn(s_levels[q], s_ahat[r][tid >> 6]);
+#pragma unroll
+        for (int m = 0; m < kDxMaxM; ++m) acc[m] = fmaf(s_dy[m][r], w, acc[m]);
+      }
+    }
+  }
+  if (k < K) {
+#pragma unroll
+    for (int m = 0; m < kDxMaxM; ++m) {
+      if (m < mt) {
+        float* dst = dX + (m0 + m) * K + k;
+        if (atomic_out) atomicAdd(dst, acc[m]);
+        else *dst = acc[m];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
+                            const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
+                            int num_sms, cudaStream_t st) {
+  GemvArgs a;
+  a.X = X;
+  a.codes = codes;
+  a.a8 = a8;
+  a.s2 = s2;
+  a.Y = Y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.nblk = static_cast<int>(K / kBlock);
+  // K-slices: aim for about two CTAs per SM in total.
+  const int64_t row_ctas = (N + kGemvRows - 1) / kGemvRows;
+  int64_t want = (2 * static_cast<int64_t>(num_sms) + row_ctas - 1) / row_ctas;
+  want = std::max<int64_t>(1, std::min<int64_t>(want, a.nblk));
+  int bs = static_cast<int>((a.nblk + want - 1) / want);
+  bs = std::max(1, std::min(bs, kMaxSliceBlocks));
+  a.bs = bs;
+  a.slices = (a.nblk + bs - 1) / bs;
+  const int nt = (M <= 8) ? 1 : 2;
+  const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
+  const size_t smem = kTabBytes + static_cast<size_t>(kGemvRows) * bs * 4 + 64 +
+                      16 * static_cast<size_t>(bs * 128 + 8);
+  if (a.slices > 1) {
+    cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(static_cast<unsigned>(row_ctas), static_cast<unsigned>(a.slices),
+            static_cast<unsigned>(mtiles));
+  // The largest slice needs ~113 KB of dynamic shared memory; opt in once.
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const int max_smem = kTabBytes + kGemvRows * kMaxSliceBlocks * 4 + 64 +
+                         16 * (kMaxSliceBlocks * 128 + 8);
+    cudaFuncSetAttribute(gemv_fwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  });
+  if (nt == 1) {
+    gemv_fwd_kernel<1><<<grid, kGemvThreads, smem, st>>>(a);
+  } else {
+    gemv_fwd_kernel<2><<<grid, kGemvThreads, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,
+                           const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* dX,
+                           int num_sms, cudaStream_t st) {
+  const int64_t kctas = (K + kDxThreads - 1) / kDxThreads;
+  const int64_t mtiles = (M + kDxMaxM - 1) / kDxMaxM;
+  int64_t slices = (2 * static_cast<int64_t>(num_sms) + kctas * mtiles - 1) / (kctas * mtiles);
+  slices = std::max<int64_t>(1, std::min<int64_t>(slices, (N + kDxRows - 1) / kDxRows));
+  int64_t rows_per_slice = (N + slices - 1) / slices;
+  rows_per_slice = ((rows_per_slice + kDxRows - 1) / kDxRows) * kDxRows;
+  slices = (N + rows_per_slice - 1) / rows_per_slice;
+  if (slices > 1) {
+    cudaError_t e = cudaMemsetAsync(dX, 0, static_cast<size_t>(M) * K * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(static_cast<unsigned>(kctas), static_cast<unsigned>(slices),
+            static_cast<unsigned>(mtiles));
+  simt_dx_kernel<<<grid, kDxThreads, 0, st>>>(dY, M, codes, a8, s2, N, K, dX, rows_per_slice,
+                                              slices > 1 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace nf4

@@ -1,0 +1,148 @@
+// NF4 blockwise quantization with 8-bit double-quantized absmax, and the
+// stand-alone dequantization ("Zenbit", zenbit.nf4 bullet; "bitsandbytes",
+// NF4 and double-quantization paragraphs).
+//
+// Both kernels are HBM-bound streaming passes: quantize reads 4 B and writes
+// 0.516 B per weight, dequantize reads 0.516 B and writes 4 B per weight.
+#include "common.cuh"
+
+namespace nf4 {
+namespace {
+
+// Nearest level of an fp32 x in [-1, 1], ties to the lower index: the number
+// of decision thresholds strictly below x.
+__device__ __forceinline__ uint32_t nearest_code(float x) {
+  uint32_t q = 0;
+#pragma unroll
+  for (int i = 0; i < 15; ++i) q += (x > __uint_as_float(threshold_bits(i))) ? 1u : 0u;
+  return q;
+}
+
+// Codes of the four weights of a float4 packed as two bytes (little-endian
+// u16): element 4j in the high nibble of the first byte.
+__device__ __forceinline__ uint32_t quantize4(float4 v, float a) {
+  // a == 0: the block is all zero and every weight takes level 0 (code 7).
+  const bool nz = a > 0.0f;
+  const float x0 = nz ? __fdiv_rn(v.x, a) : 0.0f;
+  const float x1 = nz ? __fdiv_rn(v.y, a) : 0.0f;
+  const float x2 = nz ? __fdiv_rn(v.z, a) : 0.0f;
+  const float x3 = nz ? __fdiv_rn(v.w, a) : 0.0f;
+  const uint32_t b0 = (nearest_code(x0) << 4) | nearest_code(x1);
+  const uint32_t b1 = (nearest_code(x2) << 4) | nearest_code(x3);
+  return b0 | (b1 << 8);
+}
+
+__device__ __forceinline__ float abs_max4(float4 v) {
+  return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+
+constexpr int kQThreads = 256;   // one thread per block of the group
+constexpr int kQLoads = 16;      // float4 loads per lane: 32 blocks per warp
+
+// One CTA per double-quant group of 256 blocks (16384 weights). Warp w owns
+// blocks [32w, 32w + 32) of the group. Load i of a lane covers float4 number
+// 32 i + lane of the warp's span: lanes 0-15 hold block 2i, lanes 16-31 block
+// 2i + 1, so the block absmax is a 16-lane shuffle reduction. All 16 loads of
+// a lane are issued before any is used (64 KB in flight per CTA).
+__global__ void __launch_bounds__(kQThreads)
+quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restrict__ codes,
+                uint8_t* __restrict__ a8_out, float* __restrict__ s2_out) {
+  __shared__ float s_absmax[kGroup];
+  __shared__ float s_warp_max[kQThreads / 32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kGroup;
+  const int nblk = static_cast<int>(min(static_cast<int64_t>(kGroup), n_blocks - blk0));
+  const int wblk0 = warp * 32;  // first block of this warp within the group
+
+  const float4* src = reinterpret_cast<const float4*>(W) + blk0 * (kBlock / 4) + wblk0 * 16;
+  float4 v[kQLoads];
+#pragma unroll
+  for (int i = 0; i < kQLoads; ++i) {
+    const int b = wblk0 + 2 * i + (lane >> 4);
+    v[i] = (b < nblk) ? __ldcs(src + 32 * i + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  uint16_t* dst = reinterpret_cast<uint16_t*>(codes) + blk0 * (kBlock / 4) + wblk0 * 16;
+#pragma unroll
+  for (int i = 0; i < kQLoads; ++i) {
+    float a = abs_max4(v[i]);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    const int b = wblk0 + 2 * i + (lane >> 4);
+    if (b < nblk) {
+      dst[32 * i + lane] = static_cast<uint16_t>(quantize4(v[i], a));
+      if ((lane & 15) == 0) s_absmax[b] = a;
+    }
+  }
+  __syncthreads();
+
+  // Second level: s2 = max absmax of the group, a8 = round(255 * a / s2).
+  const int t = threadIdx.x;
+  const float a = (t < nblk) ? s_absmax[t] : 0.0f;
+  float m = a;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) s_warp_max[warp] = m;
+  __syncthreads();
+  float s2 = s_warp_max[0];
+#pragma unroll
+  for (int w = 1; w < kQThreads / 32; ++w) s2 = fmaxf(s2, s_warp_max[w]);
+  if (t < nblk) {
+    const uint32_t q =
+        (s2 > 0.0f) ? __float2uint_rn(__fdiv_rn(__fmul_rn(255.0f, a), s2)) : 0u;
+    a8_out[blk0 + t] = static_cast<uint8_t>(q);
+  }
+  if (t == 0) s2_out[blockIdx.x] = s2;
+}
+
+// Dequantize: one thread per 32 weights (16 code bytes, half a block).
+__global__ void __launch_bounds__(256)
+dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ a8,
+                  const float* __restrict__ s2, int64_t n_chunks, float* __restrict__ out) {
+  __shared__ float s_levels[16];
+  if (threadIdx.x < 16) s_levels[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
+  __syncthreads();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_chunks) return;
+  const int64_t blk = i >> 1;
+  const float ahat = dequant_absmax(a8[blk], s2[blk / kGroup]);
+  const uint4 c = __ldg(reinterpret_cast<const uint4*>(codes) + i);
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+  float4* o = reinterpret_cast<float4*>(out) + i * 8;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = words[j];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t b0 = (w >> (16 * h)) & 0xffu, b1 = (w >> (16 * h + 8)) & 0xffu;
+      float4 r;
+      r.x = __fmul_rn(s_levels[b0 >> 4], ahat);
+      r.y = __fmul_rn(s_levels[b0 & 15], ahat);
+      r.z = __fmul_rn(s_levels[b1 >> 4], ahat);
+      r.w = __fmul_rn(s_levels[b1 & 15], ahat);
+      __stcs(o + 2 * j + h, r);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* W, int64_t n_elems, uint8_t* codes, uint8_t* a8,
+                            float* s2, cudaStream_t st) {
+  const int64_t n_blocks = n_elems / kBlock;
+  const int64_t n_groups = (n_blocks + kGroup - 1) / kGroup;
+  quantize_kernel<<<static_cast<unsigned>(n_groups), kQThreads, 0, st>>>(W, n_blocks, codes, a8,
+                                                                         s2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const float* s2,
+                              int64_t n_elems, float* out, cudaStream_t st) {
+  const int64_t n_chunks = n_elems / 32;
+  const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
+  dequantize_kernel<<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
+  return cudaGetLastError();
+}
+
+}  // namespace nf4

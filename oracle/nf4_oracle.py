@@ -204,12 +204,18 @@ def dequant_absmax(a8: np.ndarray, s2: np.ndarray) -> np.ndarray:
     return (prod / np.float32(255.0)).astype(np.float32)
 
 
-def dequantize_flat(packed: np.ndarray, a8: np.ndarray, s2: np.ndarray) -> np.ndarray:
-    """Weights second: what = fl32(c[q] * ahat) (fp32 [n])."""
+def dequantize_codes(codes: np.ndarray, ahat: np.ndarray) -> np.ndarray:
+    """Weights second: what = fl32(c[q] * ahat) for codes [nblocks, 64] and the
+    blocks' dequantized absmax [nblocks] (fp32 [nblocks, 64])."""
     lv = nf4_levels()
+    q = np.asarray(codes, dtype=np.uint8).reshape(-1, BLOCKSIZE)
+    return (lv[q] * np.asarray(ahat, dtype=np.float32)[:, None]).astype(np.float32)
+
+
+def dequantize_flat(packed: np.ndarray, a8: np.ndarray, s2: np.ndarray) -> np.ndarray:
+    """Dequantize a whole flat weight (fp32 [n])."""
     ahat = dequant_absmax(a8, s2)
-    q = unpack_nibbles(packed).reshape(-1, BLOCKSIZE)
-    return (lv[q] * ahat[:, None]).astype(np.float32).reshape(-1)
+    return dequantize_codes(unpack_nibbles(packed), ahat).reshape(-1)
 
 
 def dequantize(packed, a8, s2, rows: int, cols: int) -> np.ndarray:

@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports every symbol the header declares, carries
+the oracle's NF4 table bit for bit, and rejects invalid arguments on the host
+before touching a device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import dequant_gemm_gb300 as nf4
+from oracle import nf4_oracle as o
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nf4gemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf4_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(nf4.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = nf4.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_codebook_matches_oracle_bits():
+    got = nf4.nf4_codebook().numpy().astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), o.nf4_levels().view(np.uint32))
+
+
+def test_status_strings():
+    for code in range(8):
+        assert nf4.status_string(code)
+    assert nf4.status_string(99) == "unknown status"
+
+
+def _weight(rows=8, cols=64, codes=16, a8=16, s2=16, blocksize=64, group=256):
+    return nf4.nf4_weight(codes, a8, s2, rows, cols, blocksize, group)
+
+
+P = 1 << 20   # a fake, 16-byte aligned address: never dereferenced by validation
+
+
+@pytest.mark.parametrize("blocksize", [32, 128, 0])
+def test_quantize_rejects_blocksize(blocksize):
+    assert nf4.lib().nf4_quantize(P, 8, 64, blocksize, P, P, P, None) == 4
+
+
+def test_quantize_rejects_shapes_and_pointers():
+    L = nf4.lib()
+    assert L.nf4_quantize(P, -1, 64, 64, P, P, P, None) == 2
+    assert L.nf4_quantize(P, 8, 96, 64, P, P, P, None) == 2      # cols % 64
+    assert L.nf4_quantize(None, 8, 64, 64, P, P, P, None) == 1
+    assert L.nf4_quantize(P, 8, 64, 64, P, None, P, None) == 1
+    assert L.nf4_quantize(P + 4, 8, 64, 64, P, P, P, None) == 3
+    assert L.nf4_quantize(P, 8, 64, 64, P, P + 8, P, None) == 3
+    # empty extents are a no-op that touches no pointer
+    assert L.nf4_quantize(None, 0, 64, 64, None, None, None, None) == 0
+    assert L.nf4_quantize(None, 8, 0, 64, None, None, None, None) == 0
+
+
+def test_matmul_validation():
+    L = nf4.lib()
+    w = _weight(codes=P, a8=P, s2=P)
+    assert L.nf4_matmul_fwd(P, 4, None, P, None) == 1
+    assert L.nf4_matmul_fwd(P, -1, ctypes.byref(w), P, None) == 2
+    assert L.nf4_matmul_fwd(P, 0, ctypes.byref(w), None, None) == 0      # M = 0
+    bad = _weight(blocksize=32, codes=P, a8=P, s2=P)
+    assert L.nf4_matmul_fwd(P, 4, ctypes.byref(bad), P, None) == 4
+    bad = _weight(group=128, codes=P, a8=P, s2=P)
+    assert L.nf4_matmul_bwd_dx(P, 4, ctypes.byref(bad), P, None) == 4
+    rag = _weight(rows=12, codes=P, a8=P, s2=P)                          # rows % 8
+    assert L.nf4_matmul_fwd(P, 4, ctypes.byref(rag), P, None) == 2
+    assert L.nf4_matmul_bwd_dx(P, 4, ctypes.byref(rag), P, None) == 2
+    odd = _weight(cols=96, codes=P, a8=P, s2=P)
+    assert L.nf4_matmul_fwd(P, 4, ctypes.byref(odd), P, None) == 2
+    nul = _weight(codes=None, a8=P, s2=P)
+    assert L.nf4_matmul_fwd(P, 4, ctypes.byref(nul), P, None) == 1
+    assert L.nf4_matmul_fwd(None, 4, ctypes.byref(w), P, None) == 1
+    assert L.nf4_matmul_bwd_dx(P, 4, ctypes.byref(w), None, None) == 1
+    assert L.nf4_matmul_fwd(P + 2, 4, ctypes.byref(w), P, None) == 3
+    assert L.nf4_matmul_bwd_dx(P, 4, ctypes.byref(w), P + 4, None) == 3
+    mis = _weight(codes=P + 1, a8=P, s2=P)
+    assert L.nf4_dequantize(ctypes.byref(mis), P, None) == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_device_reports_device_error():
+    L = nf4.lib()
+    w = _weight(codes=P, a8=P, s2=P)
+    assert L.nf4_quantize(P, 8, 64, 64, P, P, P, None) == 5
+    assert L.nf4_matmul_fwd(P, 4, ctypes.byref(w), P, None) == 5

@@ -132,3 +132,13 @@ def test_memory_size_invariant_matches_quoted_savings():
     assert 0.75 <= saving_fp32 <= 0.89            # "~75-89% vs fp32"
     dq_extra = 1 - bits / 4.5                     # vs fp32 absmax per block
     assert 0.05 <= dq_extra <= 0.10               # "further 5-10%"
+
+
+def test_oracle_views_match_full_dequant():
+    from tests.oracle_views import OracleWeight
+    W = (np.random.default_rng(21).standard_normal((24, 704)) * 0.02).astype(np.float32)
+    full = o.dequantize(*o.quantize(W), 24, 704)
+    ow = OracleWeight(W)
+    assert np.array_equal(ow.rows([0, 5, 23]), full[[0, 5, 23]])
+    cols = OracleWeight.columns_of([0, 3, 10])
+    assert np.array_equal(ow.col_blocks([0, 3, 10]), full[:, cols])

@@ -1,0 +1,286 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Quantize and dequantize are bit-exact (codes, absmax codes, scales, fp32
+dequantized weights). The fused matmuls meet the stated tolerance against the
+oracle's fp64 dequantize-then-multiply: relative Frobenius error <= 2e-3 and
+max error <= 5e-3 * max|Y_ref|. Small cases are compared in full; full-size
+workloads on sampled rows / columns the oracle computes one by one, and in
+full against an fp32 PyTorch product of the (bit-exact) dequantized weight.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import dequant_gemm_gb300 as nf4
+from dequant_gemm_gb300 import workloads as wl
+from oracle import nf4_oracle as o
+from tests.oracle_views import OracleWeight, sample_indices
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+torch.backends.cuda.matmul.allow_tf32 = False   # the fp32 cross-check must be fp32
+REL_FRO, MAX_REL = 2e-3, 5e-3
+
+
+def assert_tol(Y, Y_ref, what=""):
+    rf, mr = o.rel_frobenius(Y, Y_ref), o.max_rel_to_max(Y, Y_ref)
+    assert rf <= REL_FRO and mr <= MAX_REL, f"{what}: rel_fro={rf:.3e} max_rel={mr:.3e}"
+
+
+def assert_quant_groups(W_np, q, groups):
+    codes = q.codes.cpu().numpy()
+    a8 = q.absmax_q.cpu().numpy()
+    s2 = q.absmax_scale.cpu().numpy()
+    flat = W_np.reshape(-1)
+    for g in groups:
+        lo, hi = g * 16384, min((g + 1) * 16384, flat.size)
+        pc, pa, ps = o.quantize_flat(flat[lo:hi])
+        assert np.array_equal(codes[lo // 2:hi // 2], pc), f"codes differ in group {g}"
+        assert np.array_equal(a8[lo // 64:hi // 64], pa), f"absmax codes differ in group {g}"
+        assert s2[g].view(np.uint32) == ps[0].view(np.uint32), f"s2 differs in group {g}"
+
+
+def assert_quant_full(W_np, q):
+    pc, pa, ps = o.quantize(W_np)
+    assert np.array_equal(q.codes.cpu().numpy(), pc)
+    assert np.array_equal(q.absmax_q.cpu().numpy(), pa)
+    assert np.array_equal(q.absmax_scale.cpu().numpy().view(np.uint32), ps.view(np.uint32))
+    return pc, pa, ps
+
+
+@functools.lru_cache(maxsize=None)
+def weight_np(rows, cols, seed, outlier_frac=0.0):
+    return wl.weight(rows, cols, seed=seed, outlier_frac=outlier_frac).numpy()
+
+
+# ---------------------------------------------------------------- quantize --
+def test_quantize_tiny_full_and_dequant():
+    W = weight_np(256, 256, 0)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    pc, pa, ps = assert_quant_full(W, q)
+    Wd = nf4.nf4_dequantize(q).cpu().numpy()
+    ref = o.dequantize(pc, pa, ps, 256, 256)
+    assert np.array_equal(Wd.view(np.uint32), ref.view(np.uint32))
+
+
+def test_quantize_decode_full_with_outliers():
+    W = weight_np(4096, 4096, 0, 0.001)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    pc, pa, ps = assert_quant_full(W, q)
+    Wd = nf4.nf4_dequantize(q).cpu().numpy()
+    ref = o.dequantize(pc, pa, ps, 4096, 4096)
+    assert np.array_equal(Wd.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,cols", [(11008, 4096), (4096, 11008), (18944, 3584),
+                                       (3584, 18944), (512, 3584)])
+def test_quantize_full_size_sampled_groups(rows, cols):
+    W = weight_np(rows, cols, 0)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    ng = q.absmax_scale.numel()
+    assert_quant_groups(W, q, sample_indices(ng, 24, seed=rows))
+    # dequantize agrees bit for bit on the same groups
+    Wd = nf4.nf4_dequantize(q).cpu().numpy().reshape(-1)
+    flat = W.reshape(-1)
+    for g in sample_indices(ng, 6, seed=cols):
+        lo, hi = g * 16384, min((g + 1) * 16384, flat.size)
+        ref = o.dequantize_flat(*o.quantize_flat(flat[lo:hi]))
+        assert np.array_equal(Wd[lo:hi].view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 64), (3, 192), (100, 192), (257, 128), (5, 16384 + 64)])
+def test_quantize_ragged_shapes(rows, cols):
+    W = weight_np(rows, cols, 3)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    assert_quant_full(W, q)
+
+
+def test_quantize_special_cases():
+    rng = np.random.default_rng(5)
+    W = (rng.standard_normal((64, 1024)) * 0.02).astype(np.float32)
+    flat = W.reshape(-1)
+    flat[0:64] = 0.0                                  # all-zero block
+    flat[64:128] = 0.0
+    flat[64 + 7] = -0.0                               # -0 in an all-zero block
+    flat[64 + 9] = 3.0                                # single nonzero
+    flat[192:256] = np.linspace(-1, 1, 64)            # exact +-absmax
+    flat[256:320] = 1e-30 * rng.standard_normal(64)   # tiny block
+    flat[320:384] = 1e30 * rng.standard_normal(64)    # huge block
+    flat[384:448] = 2.0 ** -140                       # subnormal, all equal
+    flat[16384:32768] = 0.0                           # an all-zero group
+    c = o.nf4_levels().astype(np.float64)
+    mids = ((c[:-1] + c[1:]) / 2).astype(np.float32)  # values on the decision edges
+    flat[448:463] = mids
+    flat[463] = 1.0
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    pc, pa, ps = assert_quant_full(W, q)
+    Wd = nf4.nf4_dequantize(q).cpu().numpy()
+    ref = o.dequantize(pc, pa, ps, 64, 1024)
+    assert np.array_equal(Wd.view(np.uint32), ref.view(np.uint32))
+
+
+def test_quantize_writes_only_its_outputs():
+    W = torch.from_numpy(weight_np(96, 320, 7)).to(DEV)
+    pad = 64
+    n = 96 * 320
+    codes = torch.full((n // 2 + 2 * pad,), 0xA5, dtype=torch.uint8, device=DEV)
+    a8 = torch.full((n // 64 + 2 * pad,), 0x5A, dtype=torch.uint8, device=DEV)
+    s2 = torch.full((2 + 2 * 16,), 7.0, dtype=torch.float32, device=DEV)
+    q = nf4.NF4Weight(codes[pad:pad + n // 2], a8[pad:pad + n // 64], s2[16:18], 96, 320)
+    nf4.nf4_quantize(W, out=q)
+    torch.cuda.synchronize()
+    assert torch.all(codes[:pad] == 0xA5) and torch.all(codes[pad + n // 2:] == 0xA5)
+    assert torch.all(a8[:pad] == 0x5A) and torch.all(a8[pad + n // 64:] == 0x5A)
+    assert torch.all(s2[:16] == 7.0) and torch.all(s2[18:] == 7.0)
+    assert_quant_full(W.cpu().numpy(), q)
+
+
+# ----------------------------------------------------------------- forward --
+def run_fwd(W_np, X_bf16):
+    q = nf4.nf4_quantize(torch.from_numpy(W_np).to(DEV))
+    Y = nf4.nf4_matmul_fwd(X_bf16.to(DEV), q)
+    return q, Y.cpu().numpy()
+
+
+def test_fwd_tiny_full():
+    W = weight_np(256, 256, 0)
+    X = wl.activations(8, 256)
+    _, Y = run_fwd(W, X)
+    Wh = o.dequantize(*o.quantize(W), 256, 256)
+    assert_tol(Y, o.matmul_fwd(X.float().numpy(), Wh), "tiny fwd")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_fwd_decode_full(M):
+    W = weight_np(4096, 4096, 0, 0.001)
+    X = wl.activations(M, 4096)
+    _, Y = run_fwd(W, X)
+    Wh = OracleWeight(W).rows(np.arange(4096))
+    assert_tol(Y, o.matmul_fwd(X.float().numpy(), Wh), f"decode fwd M={M}")
+
+
+@pytest.mark.parametrize("M", [2, 3, 7, 9, 15, 17, 33, 100, 130, 300])
+def test_fwd_ragged_tokens(M):
+    W = weight_np(520, 1024, 8)
+    X = wl.activations(M, 1024, seed=M)
+    _, Y = run_fwd(W, X)
+    Wh = o.dequantize(*o.quantize(W), 520, 1024)
+    assert_tol(Y, o.matmul_fwd(X.float().numpy(), Wh), f"ragged fwd M={M}")
+
+
+def check_fwd_large(W, M, seed):
+    X = wl.activations(M, W.shape[1], seed=seed)
+    q, Y = run_fwd(W, X)
+    ow = OracleWeight(W)
+    rows = sample_indices(W.shape[0], 96, seed=seed)
+    Y_ref = o.matmul_fwd(X.float().numpy(), ow.rows(rows))
+    assert_tol(Y[:, rows], Y_ref, f"fwd {W.shape} M={M} sampled rows")
+    # full output against fp32 torch on the bit-exact dequantized weight
+    Wd = nf4.nf4_dequantize(q)
+    Yt = (X.to(DEV).float() @ Wd.T).double().cpu().numpy()
+    assert_tol(Y, Yt, f"fwd {W.shape} M={M} full vs fp32")
+    assert np.isfinite(Y).all()
+
+
+def test_fwd_prefill_up():
+    check_fwd_large(weight_np(11008, 4096, 0), 4096, 1)
+
+
+@pytest.mark.parametrize("proj", [p for p in wl.QWEN_LAYER])
+@pytest.mark.parametrize("M", [1, 64, 2048])
+def test_fwd_qwen_layer(proj, M):
+    check_fwd_large(weight_np(proj.rows, proj.cols, proj.seed), M, 100 + M)
+
+
+# ---------------------------------------------------------------- backward --
+def run_dx(W_np, dY_bf16):
+    q = nf4.nf4_quantize(torch.from_numpy(W_np).to(DEV))
+    dX = nf4.nf4_matmul_bwd_dx(dY_bf16.to(DEV), q)
+    return q, dX.cpu().numpy()
+
+
+def test_dx_tiny_full():
+    W = weight_np(256, 256, 0)
+    dY = wl.activations(8, 256, std=0.01)
+    _, dX = run_dx(W, dY)
+    Wh = o.dequantize(*o.quantize(W), 256, 256)
+    assert_tol(dX, o.matmul_bwd_dx(dY.float().numpy(), Wh), "tiny dX")
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 40, 129])
+def test_dx_ragged_tokens(M):
+    W = weight_np(264, 1088, 9)
+    dY = wl.activations(M, 264, std=0.01, seed=M)
+    _, dX = run_dx(W, dY)
+    Wh = o.dequantize(*o.quantize(W), 264, 1088)
+    assert_tol(dX, o.matmul_bwd_dx(dY.float().numpy(), Wh), f"ragged dX M={M}")
+
+
+def check_dx_large(W, M, seed):
+    dY = wl.activations(M, W.shape[0], std=0.01, seed=seed)
+    q, dX = run_dx(W, dY)
+    ow = OracleWeight(W)
+    kbs = sample_indices(W.shape[1] // 64, 4, seed=seed)
+    cols = OracleWeight.columns_of(kbs)
+    dX_ref = o.matmul_bwd_dx(dY.float().numpy(), ow.col_blocks(kbs))
+    assert_tol(dX[:, cols], dX_ref, f"dX {W.shape} M={M} sampled columns")
+    Wd = nf4.nf4_dequantize(q)
+    dXt = (dY.to(DEV).float() @ Wd).double().cpu().numpy()
+    assert_tol(dX, dXt, f"dX {W.shape} M={M} full vs fp32")
+
+
+def test_dx_bwd_down():
+    check_dx_large(weight_np(4096, 11008, 0), 2048, 1)
+
+
+@pytest.mark.parametrize("proj", [p for p in wl.QWEN_LAYER])
+def test_dx_qwen_layer(proj):
+    check_dx_large(weight_np(proj.rows, proj.cols, proj.seed), 2048, 7)
+
+
+# ------------------------------------------------------------------- misc --
+def test_empty_and_zero_extents():
+    q = nf4.nf4_quantize(torch.from_numpy(weight_np(64, 128, 1)).to(DEV))
+    X = torch.empty(0, 128, dtype=torch.bfloat16, device=DEV)
+    assert nf4.nf4_matmul_fwd(X, q).shape == (0, 64)
+    dY = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    assert nf4.nf4_matmul_bwd_dx(dY, q).shape == (0, 128)
+    e = nf4.nf4_quantize(torch.empty(0, 64, dtype=torch.float32, device=DEV))
+    assert e.codes.numel() == 0
+    assert nf4.nf4_poll_device_status() == 0
+
+
+def test_fwd_output_guard_bytes():
+    W = weight_np(136, 256, 2)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    for M in (3, 40):
+        X = wl.activations(M, 256, seed=M).to(DEV)
+        n = M * 136
+        buf = torch.full((n + 64,), 123.0, dtype=torch.float32, device=DEV)
+        Y = buf[32:32 + n].view(M, 136)
+        nf4.nf4_matmul_fwd(X, q, out=Y)
+        dbuf = torch.full((M * 256 + 64,), 321.0, dtype=torch.float32, device=DEV)
+        dX = dbuf[32:32 + M * 256].view(M, 256)
+        dY = wl.activations(M, 136, std=0.01, seed=M + 1).to(DEV)
+        nf4.nf4_matmul_bwd_dx(dY, q, out=dX)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:32] == 123.0) and torch.all(buf[32 + n:] == 123.0)
+        assert torch.all(dbuf[:32] == 321.0) and torch.all(dbuf[32 + M * 256:] == 321.0)
+    assert nf4.nf4_poll_device_status() == 0
+
+
+def test_non_default_stream():
+    W = weight_np(512, 512, 4)
+    X = wl.activations(16, 512).to(DEV)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    Y0 = nf4.nf4_matmul_fwd(X, q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        q2 = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+        Y1 = nf4.nf4_matmul_fwd(X, q2)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(q.codes, q2.codes)
+    assert torch.allclose(Y0, Y1, rtol=0, atol=1e-5 * Y0.abs().max().item())
