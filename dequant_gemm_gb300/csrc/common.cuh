@@ -76,6 +76,12 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const flo
 cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
                             const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
                             int num_sms, cudaStream_t st);
+cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
+                          const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
+                          int* status, cudaStream_t st);
+cudaError_t launch_tc_dx(const uint16_t* dY, int64_t M, const uint8_t* codes, const uint8_t* a8,
+                         const float* s2, int64_t N, int64_t K, float* dX, int num_sms,
+                         int* status, cudaStream_t st);
 cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,
                            const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* dX,
                            int num_sms, cudaStream_t st);

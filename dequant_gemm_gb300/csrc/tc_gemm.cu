@@ -1,0 +1,407 @@
+// Large-M fused NF4-dequant matmuls on the sm_103a tensor cores (tcgen05):
+//   forward   Y[m, n]  = sum_k X[m, k]  * w[n, k]
+//   input grad dX[m, k] = sum_n dY[m, n] * w[n, k]      (no dW)
+// ("Zenbit", zenbit.pallas_nf4 bullet: compressed weight tiles streamed in and
+// dequantized on chip, full-precision weight never in HBM; dL/dX only.)
+//
+// One CTA computes a 128 x BN tile of D = A * B^T with the weight as the
+// 128-row A operand and the tokens as the BN-column B operand (BN = 64, 128 or
+// 256), looping over the reduction in stages of 64:
+//   * warp 0 (one thread) TMA-loads the stage's activation tile (bf16,
+//     128-byte swizzle, the K-major B operand) and its packed-code tile;
+//   * warps 2-9 dequantize the codes (level * dequantized absmax, rounded to
+//     bf16) and write them straight into tensor memory, where the MMA reads
+//     its A operand: the dequantized weight never touches shared memory;
+//   * warp 1 (one thread) issues tcgen05.mma (128 x BN x 16) into an fp32
+//     accumulator in tensor memory and commits each stage back to the
+//     producer;
+//   * warps 2-9 then read the accumulator with tcgen05.ld and store fp32
+//     outputs (coalesced: 32 consecutive outputs of one token per warp store).
+// The forward walks a tile of 128 weight rows along K; the input gradient
+// walks a tile of 128 weight columns along N, reading each column's nibbles
+// down 64 rows per stage (the transposed walk). When the output tiles alone
+// cannot fill the GPU the reduction is split across CTAs and summed with
+// atomics into a zeroed output.
+//
+// Every mbarrier wait is bounded; a CTA that gives up records a timeout in the
+// device status word, skips the remaining work and still releases its tensor
+// memory.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace nf4 {
+namespace {
+
+constexpr int kTcThreads = 320;              // 10 warps
+constexpr int kDqThreads = 256;              // warps 2-9
+constexpr int kStages = 4;
+constexpr int kTileRows = 128;               // MMA M
+constexpr int kMaxBN = 256;                  // MMA N
+constexpr int kActStageBytes = kMaxBN * 128; // 64 bf16 per token row
+constexpr int kCodesStageBytes = 4096;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemA0 = 256;            // columns [256, 384): A-operand slots
+
+constexpr int kOffAct = 0;
+constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
+constexpr int kOffAhat = kOffCodes + kStages * kCodesStageBytes;
+constexpr int kOffLut = kOffAhat + kStages * 128 * 4;
+constexpr int kOffBars = kOffLut + 64;
+constexpr int kNumBars = 3 * kStages + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+
+struct TcArgs {
+  const uint8_t* a8;
+  const float* s2;
+  float* out;        // Y [M, N] or dX [M, K]
+  int64_t M, N, K;
+  int nblk;          // K / 64
+  int bn;            // token tile
+  int stages_total;
+  int stages_per_split;
+  int atomic_out;
+  int* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <bool kDx>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
+               const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* lut = reinterpret_cast<float*>(smem + kOffLut);
+  float* ahat_s = reinterpret_cast<float*>(smem + kOffAhat);
+  const uint32_t bars = tc::smem_addr(smem + kOffBars);
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto dq_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  auto empty_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
+  const uint32_t accum_bar = bars + 8u * (3 * kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * p.bn;
+  const int s_begin = blockIdx.z * p.stages_per_split;
+  const int nst = min(p.stages_per_split, p.stages_total - s_begin);
+
+  if (threadIdx.x < 16) lut[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(full_bar(s), 1);
+      tc::mbar_init(dq_bar(s), kDqThreads);
+      tc::mbar_init(empty_bar(s), 1);
+    }
+    tc::mbar_init(accum_bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensormap(&tm_act);
+    tc::prefetch_tensormap(&tm_codes);
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    report_status(p.status, kStatusTimeout);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      const uint32_t tx = static_cast<uint32_t>(p.bn) * 128u + kCodesStageBytes;
+      int issued = 0;
+      for (int i = 0; i < nst && !*abort_flag; ++i) {
+        const int slot = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!tc::mbar_wait(empty_bar(slot), ph ^ 1)) { fail(); break; }
+        const int s = s_begin + i;
+        tc::mbar_arrive_expect_tx(full_bar(slot), tx);
+        const uint32_t act = tc::smem_addr(smem + kOffAct + slot * kActStageBytes);
+        const uint32_t cod = tc::smem_addr(smem + kOffCodes + slot * kCodesStageBytes);
+        tc::tma_load_2d(act, &tm_act, s * 64, static_cast<int32_t>(m0), full_bar(slot));
+        if (!kDx) {
+          tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
+        } else {
+          tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(r0 / 2), s * 64, full_bar(slot));
+        }
+        ++issued;
+      }
+      if (*abort_flag) {  // let copies in flight land before the CTA exits
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+          tc::mbar_wait(full_bar(i % kStages), (i / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, static_cast<uint32_t>(p.bn));
+      for (int i = 0; i < nst && !*abort_flag; ++i) {
+        const int slot = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!tc::mbar_wait(dq_bar(slot), ph) || !tc::mbar_wait(full_bar(slot), ph)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t a = tmem + kTmemA0 + 32u * slot;
+        const uint32_t b = tc::smem_addr(smem + kOffAct + slot * kActStageBytes);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tc::mma_bf16_tmem_a(tmem, a + 8u * j, tc::sw128_kmajor_desc(b + 32u * j), idesc,
+                              (i | j) != 0 ? 1u : 0u);
+        }
+        tc::mma_commit(empty_bar(slot));
+      }
+      tc::mma_commit(accum_bar);
+      if (!tc::mbar_wait(accum_bar, 0)) fail();   // all MMAs done before teardown
+    }
+  } else {
+    // ---------------------------------------------------- dequant + store --
+    const int q = warp & 3;             // TMEM lane quarter of this warp
+    const int h = (warp - 2) >> 2;      // which half of each stage's columns
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const float* ahat_slots = ahat_s;
+    if (!kDx) {
+      const int row = 32 * q + lane;
+      const int64_t n = r0 + row;
+      const bool vrow = n < p.N;
+      uint32_t a8v = 0;
+      float s2v = 0.0f;
+      if (vrow && nst > 0) {
+        const int64_t bi = n * p.nblk + s_begin;
+        a8v = p.a8[bi];
+        s2v = p.s2[bi >> 8];
+      }
+      for (int i = 0; i < nst; ++i) {
+        const int slot = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
+        if (vrow && i + 1 < nst) {
+          const int64_t bi = n * p.nblk + s_begin + i + 1;
+          a8v = p.a8[bi];
+          s2v = p.s2[bi >> 8];
+        }
+        if (*abort_flag) continue;
+        if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
+        const uint4 c = *reinterpret_cast<const uint4*>(smem + kOffCodes + slot * kCodesStageBytes +
+                                                        row * 32 + 16 * h);
+        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t byte = (words[j] >> (8 * b)) & 0xffu;
+            v[4 * j + b] = pack_bf16x2(__fmul_rn(lut[byte >> 4], ahat), __fmul_rn(lut[byte & 15u], ahat));
+          }
+        }
+        tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * h, v);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(dq_bar(slot));
+      }
+    } else {
+      const int kl = 32 * q + lane;     // weight column within the tile
+      const int kbl = kl >> 6;          // its absmax block within the tile
+      const int sh = (kl & 1) ? 0 : 4;  // even column: high nibble
+      // dequantized-absmax table of each stage: 64 rows x 2 blocks, one entry
+      // per thread of the first half
+      const int e_row = kl >> 1, e_blk = kl & 1;
+      const int64_t e_kb = (r0 >> 6) + e_blk;
+      uint32_t a8v = 0;
+      float s2v = 0.0f;
+      bool e_valid = false;
+      auto load_entry = [&](int s) {
+        const int64_t n = static_cast<int64_t>(s) * 64 + e_row;
+        e_valid = (n < p.N) && (e_kb < p.nblk);
+        if (e_valid) {
+          const int64_t bi = n * p.nblk + e_kb;
+          a8v = p.a8[bi];
+          s2v = p.s2[bi >> 8];
+        }
+      };
+      if (h == 0 && nst > 0) load_entry(s_begin);
+      for (int i = 0; i < nst; ++i) {
+        const int slot = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        float* ah = const_cast<float*>(ahat_slots) + slot * 128;
+        if (h == 0) {
+          ah[e_row * 2 + e_blk] = e_valid ? dequant_absmax(a8v, s2v) : 0.0f;
+          if (i + 1 < nst) load_entry(s_begin + i + 1);
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (*abort_flag) continue;
+        if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
+        const uint8_t* cs = smem + kOffCodes + slot * kCodesStageBytes + (kl >> 1);
+        uint32_t v[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int rr = 32 * h + 2 * jj;
+          const uint32_t b0 = cs[rr * 64], b1 = cs[(rr + 1) * 64];
+          const float w0 = __fmul_rn(lut[(b0 >> sh) & 15u], ah[rr * 2 + kbl]);
+          const float w1 = __fmul_rn(lut[(b1 >> sh) & 15u], ah[(rr + 1) * 2 + kbl]);
+          v[jj] = pack_bf16x2(w0, w1);
+        }
+        tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * h, v);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(dq_bar(slot));
+      }
+    }
+
+    // epilogue: accumulator lanes are tile rows, columns are tokens
+    if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail();
+    tc::fence_after_sync();
+    if (!*abort_flag) {
+      const int64_t rg = r0 + 32 * q + lane;
+      const int64_t nd = kDx ? p.K : p.N;
+      const bool vrow = rg < nd;
+      const int half = p.bn / 2;
+      for (int c = h * half; c < (h + 1) * half; c += 16) {
+        uint32_t v[16];
+        tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int64_t m = m0 + c + j;
+          if (vrow && m < p.M) {
+            float* dst = p.out + m * nd + rg;
+            if (p.atomic_out) atomicAdd(dst, __uint_as_float(v[j]));
+            else *dst = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer, inner] with the given row pitch in bytes.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kDx>
+cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, const uint8_t* a8,
+                      const float* s2, int64_t N, int64_t K, float* out, int num_sms, int* status,
+                      cudaStream_t st) {
+  TcArgs a;
+  a.a8 = a8;
+  a.s2 = s2;
+  a.out = out;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.nblk = static_cast<int>(K / kBlock);
+  a.status = status;
+  a.bn = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  const int64_t nd = kDx ? K : N;            // tile-row dimension
+  const int64_t red = kDx ? N : K;           // reduction dimension
+  const int64_t row_tiles = (nd + kTileRows - 1) / kTileRows;
+  const int64_t m_tiles = (M + a.bn - 1) / a.bn;
+  a.stages_total = static_cast<int>((red + 63) / 64);
+  int splits = 1;
+  const int64_t ctas = row_tiles * m_tiles;
+  if (ctas < num_sms) {
+    splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms / ctas,
+                                                                      a.stages_total / 2)));
+  }
+  a.stages_per_split = (a.stages_total + splits - 1) / splits;
+  splits = (a.stages_total + a.stages_per_split - 1) / a.stages_per_split;
+  a.atomic_out = splits > 1 ? 1 : 0;
+
+  CUtensorMap tm_act, tm_codes;
+  // activations: [M, red] bf16, box 64 (reduction) x bn (tokens), 128-byte swizzle
+  if (!encode_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, static_cast<uint64_t>(red),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(red) * 2, 64,
+                 static_cast<uint32_t>(a.bn), CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // packed codes: [N, K/2] bytes; the forward takes 32 B x 128 rows, the input
+  // gradient 64 B (128 columns) x 64 rows
+  if (!encode_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), kDx ? 64 : 32,
+                 kDx ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(tc_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (a.atomic_out) {
+    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(M) * nd * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
+            static_cast<unsigned>(splits));
+  tc_gemm_kernel<kDx><<<grid, kTcThreads, kSmemBytes, st>>>(tm_act, tm_codes, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
+                          const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
+                          int* status, cudaStream_t st) {
+  return launch_tc<false>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
+}
+
+cudaError_t launch_tc_dx(const uint16_t* dY, int64_t M, const uint8_t* codes, const uint8_t* a8,
+                         const float* s2, int64_t N, int64_t K, float* dX, int num_sms,
+                         int* status, cudaStream_t st) {
+  return launch_tc<true>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
+}
+
+}  // namespace nf4
