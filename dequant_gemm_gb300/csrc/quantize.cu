@@ -9,27 +9,80 @@
 namespace nf4 {
 namespace {
 
-// Nearest level of an fp32 x in [-1, 1], ties to the lower index: the number
-// of decision thresholds strictly below x.
-__device__ __forceinline__ uint32_t nearest_code(float x) {
-  uint32_t q = 0;
+// Normalisation: the IEEE quotient x = fl32(w / a), computed as one
+// Markstein correction of the product with the correctly rounded reciprocal:
+// with r = RN(1/a), q0 = RN(w r) is within an ulp of w / a, the remainder
+// w - a q0 is exact in one FMA, and RN(q0 + rem r) is the correctly rounded
+// quotient (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990). The theorem
+// needs the intermediate values to stay normal: blocks whose absmax is below
+// 2^-64 are scaled by 2^64 first (exact), and |w| <= 1e36 keeps 1/a normal.
+struct BlockDivisor {
+  float a;      // absmax (scaled)
+  float r;      // RN(1 / a)
+  float s;      // power-of-two pre-scale of the weights
+  bool nz;      // a > 0
+};
+
+__device__ __forceinline__ BlockDivisor make_divisor(float a) {
+  BlockDivisor d;
+  d.nz = a > 0.0f;
+  d.s = (a < 5.421010862427522e-20f) ? 1.8446744073709552e19f : 1.0f;   // 2^-64, 2^64
+  d.a = __fmul_rn(a, d.s);
+  d.r = d.nz ? __frcp_rn(d.a) : 0.0f;
+  return d;
+}
+
+__device__ __forceinline__ float normalise(float w, const BlockDivisor& d) {
+  const float ws = __fmul_rn(w, d.s);
+  const float q0 = __fmul_rn(ws, d.r);
+  const float rem = __fmaf_rn(-q0, d.a, ws);
+  const float x = __fmaf_rn(rem, d.r, q0);
+  return d.nz ? x : 0.0f;   // an all-zero block maps to level 0
+}
+
+// Nearest level of x in [-1, 1], ties to the lower index, through 33 buckets
+// of width 1/16: b = trunc(16 x + 16). No decision threshold lies within
+// 0.0017 of a multiple of 1/16 and neighbouring thresholds are more than 1/16
+// apart, so every bucket holds at most one threshold and its lower edge is
+// not near one; the code is lo[b] + (x > thr[b]) with lo[b] the number of
+// thresholds below the bucket and thr[b] the threshold inside it (2 if none).
+struct Bucket {
+  float thr;
+  uint32_t lo;
+};
+
+__device__ __forceinline__ void build_buckets(Bucket* tab) {
+  const int b = threadIdx.x;
+  if (b <= 32) {
+    const float lo_edge = (b - 16) * 0.0625f, hi_edge = (b - 15) * 0.0625f;
+    uint32_t lo = 0;
+    float thr = 2.0f;
 #pragma unroll
-  for (int i = 0; i < 15; ++i) q += (x > __uint_as_float(threshold_bits(i))) ? 1u : 0u;
-  return q;
+    for (int i = 0; i < 15; ++i) {
+      const float t = __uint_as_float(threshold_bits(i));
+      lo += (t < lo_edge) ? 1u : 0u;
+      if (t > lo_edge && t < hi_edge) thr = t;
+    }
+    tab[b].thr = thr;
+    tab[b].lo = lo;
+  }
+}
+
+__device__ __forceinline__ uint32_t nearest_code(float x, const Bucket* tab) {
+  const int b = __float2int_rz(__fmaf_rn(x, 16.0f, 16.0f));
+  const Bucket e = tab[b];
+  return e.lo + ((x > e.thr) ? 1u : 0u);
 }
 
 // Codes of the four weights of a float4 packed as two bytes (little-endian
 // u16): element 4j in the high nibble of the first byte.
-__device__ __forceinline__ uint32_t quantize4(float4 v, float a) {
-  // a == 0: the block is all zero and every weight takes level 0 (code 7).
-  const bool nz = a > 0.0f;
-  const float x0 = nz ? __fdiv_rn(v.x, a) : 0.0f;
-  const float x1 = nz ? __fdiv_rn(v.y, a) : 0.0f;
-  const float x2 = nz ? __fdiv_rn(v.z, a) : 0.0f;
-  const float x3 = nz ? __fdiv_rn(v.w, a) : 0.0f;
-  const uint32_t b0 = (nearest_code(x0) << 4) | nearest_code(x1);
-  const uint32_t b1 = (nearest_code(x2) << 4) | nearest_code(x3);
-  return b0 | (b1 << 8);
+__device__ __forceinline__ uint32_t quantize4(float4 v, const BlockDivisor& d, const Bucket* tab) {
+  const uint32_t q0 = nearest_code(normalise(v.x, d), tab);
+  const uint32_t q1 = nearest_code(normalise(v.y, d), tab);
+  const uint32_t q2 = nearest_code(normalise(v.z, d), tab);
+  const uint32_t q3 = nearest_code(normalise(v.w, d), tab);
+  return (q0 << 4) | q1 | (q2 << 12) | (q3 << 8);
 }
 
 __device__ __forceinline__ float abs_max4(float4 v) {
@@ -49,6 +102,8 @@ quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restri
                 uint8_t* __restrict__ a8_out, float* __restrict__ s2_out) {
   __shared__ float s_absmax[kGroup];
   __shared__ float s_warp_max[kQThreads / 32];
+  __shared__ Bucket s_buckets[33];
+  build_buckets(s_buckets);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kGroup;
@@ -63,6 +118,7 @@ quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restri
     v[i] = (b < nblk) ? __ldcs(src + 32 * i + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
+  __syncthreads();   // bucket table ready
   uint16_t* dst = reinterpret_cast<uint16_t*>(codes) + blk0 * (kBlock / 4) + wblk0 * 16;
 #pragma unroll
   for (int i = 0; i < kQLoads; ++i) {
@@ -71,7 +127,7 @@ quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restri
     for (int off = 8; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
     const int b = wblk0 + 2 * i + (lane >> 4);
     if (b < nblk) {
-      dst[32 * i + lane] = static_cast<uint16_t>(quantize4(v[i], a));
+      dst[32 * i + lane] = static_cast<uint16_t>(quantize4(v[i], make_divisor(a), s_buckets));
       if ((lane & 15) == 0) s_absmax[b] = a;
     }
   }

@@ -284,3 +284,30 @@ def test_non_default_stream():
     torch.cuda.synchronize()
     assert torch.equal(q.codes, q2.codes)
     assert torch.allclose(Y0, Y1, rtol=0, atol=1e-5 * Y0.abs().max().item())
+
+
+def test_quantize_quotients_on_decision_edges():
+    """Weights w = fl32(m * a) +- a few ulps for every decision midpoint m and
+    many absmax values a (tiny, subnormal and huge included): the quotients
+    w / a land on or next to the thresholds, where only the correctly rounded
+    IEEE quotient gives the oracle's codes."""
+    rng = np.random.default_rng(17)
+    c = o.nf4_levels().astype(np.float64)
+    mids = (c[:-1] + c[1:]) / 2
+    nblocks = 4096
+    absmax = np.concatenate([
+        rng.uniform(1e-3, 1.0, nblocks - 64),
+        10.0 ** rng.uniform(-38, -30, 16), 10.0 ** rng.uniform(-44, -39, 16),
+        10.0 ** rng.uniform(20, 35, 16), rng.uniform(0.5, 2.0, 16)]).astype(np.float32)
+    W = np.empty((nblocks, 64), dtype=np.float32)
+    W[:, 0] = absmax * np.where(rng.random(nblocks) < 0.5, 1, -1).astype(np.float32)
+    for j in range(1, 64):
+        m = mids[rng.integers(0, 15, nblocks)] * np.where(rng.random(nblocks) < 0.5, 1, -1)
+        m = np.clip(m, -0.999, 0.999)
+        base = (m * absmax.astype(np.float64)).astype(np.float32)
+        k = rng.integers(-3, 4, nblocks).astype(np.int32)
+        W[:, j] = (base.view(np.int32) + k).view(np.float32)
+    W = np.where(np.abs(W) > np.abs(W[:, :1]), W[:, :1], W).astype(np.float32)
+    W = W.reshape(256, 1024)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    assert_quant_full(W, q)
