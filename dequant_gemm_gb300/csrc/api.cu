@@ -126,7 +126,7 @@ nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, flo
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (M <= kSmallM)
     return launched(nf4::launch_gemv_fwd(X, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,
-                                         w->cols, Y, d->num_sms, st));
+                                         w->cols, Y, d->num_sms, d->status, st));
   return launched(nf4::launch_tc_fwd(X, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,
                                      w->cols, Y, d->num_sms, d->status, st));
 }

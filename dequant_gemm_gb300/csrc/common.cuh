@@ -75,7 +75,7 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const flo
                               int64_t n_elems, float* out, cudaStream_t st);
 cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
                             const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
-                            int num_sms, cudaStream_t st);
+                            int num_sms, int* status, cudaStream_t st);
 cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
                           const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
                           int* status, cudaStream_t st);

@@ -4,12 +4,14 @@
 // dequantized on chip; the full-precision weight never reaches HBM).
 //
 // Forward design (HBM-bound: 0.516 B of weight per 2*M flops):
-//  * CTA = 8 warps = 128 weight rows (16 per warp) x one K-slice of `bs`
-//    absmax blocks; K-slices of the same rows are summed with vector atomics
-//    into a zeroed Y when there is more than one.
+//  * CTA = 8 warps = 128 weight rows (16 per warp) x one K-slice. The S
+//    K-slices of the same rows form a thread-block cluster and reduce their
+//    partial sums through distributed shared memory, so every output is
+//    written once with a plain store (no zeroing pass, no atomics).
 //  * The weight is the A operand of mma.sync.m16n8k16 (16 rows per warp), the
 //    tokens are the N operand (8 per n-tile): the "swap AB" shape for skinny
-//    products.
+//    products. The first code loads of a thread are issued before the
+//    prologue.
 //  * Dequantization is factored as  sum_b ahat_b * (sum_{k in b} x_k c[q_k]):
 //    the MMA consumes the raw levels c[q] and each 64-weight block's partial
 //    sum is scaled by its dequantized absmax in fp32 afterwards. The levels
@@ -19,7 +21,9 @@
 //    bf16 values), and the scale is removed from the fp32 result.
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
-//    that every lookup of a warp hits 32 distinct banks.
+//    that every lookup of a warp hits 32 distinct banks. The table is a
+//    compile-time constant in device memory, brought into shared memory by
+//    one bulk asynchronous copy per CTA.
 //  * Within a block the 4 threads of an MMA quad each own 16 contiguous k
 //    (8 code bytes); the reduction order over k is permuted consistently in A
 //    and B, which leaves the sum unchanged.
@@ -27,6 +31,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace nf4 {
 namespace {
@@ -34,8 +39,40 @@ namespace {
 constexpr int kGemvThreads = 256;
 constexpr int kGemvRows = 128;
 constexpr int kTabBytes = 256 * 32 * 4;
-constexpr int kMaxSliceBlocks = 32;
-constexpr int kOutStride = kGemvRows + 4;   // floats, keeps rows 16-byte aligned
+constexpr int kMaxSliceBlocks = 48;
+constexpr int kMaxCluster = 8;
+constexpr int kRegBlocks = 8;                 // code blocks held in registers at a time
+constexpr int kOutStride = kGemvRows + 4;     // floats, keeps rows 16-byte aligned
+
+// fp32 -> fp16 round-to-nearest-even for the NF4 levels (all normal in fp16
+// or zero), evaluated at compile time.
+constexpr uint32_t level_to_f16(uint32_t b) {
+  const uint32_t sign = (b >> 16) & 0x8000u;
+  const uint32_t e = (b >> 23) & 0xffu;
+  if (e == 0) return sign;
+  const uint32_t m = b & 0x7fffffu;
+  uint32_t h = ((e - 127u + 15u) << 10) | (m >> 13);
+  const uint32_t rest = m & 0x1fffu;
+  if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;
+  return sign | h;
+}
+
+struct PairTable {
+  uint32_t w[256 * 32];
+};
+
+// Entry b of copy l at word 32 b + l: low half = fp16 level of the high
+// nibble (the even, lower-k element), high half = level of the low nibble.
+constexpr PairTable make_pair_table() {
+  PairTable t{};
+  for (int i = 0; i < 256 * 32; ++i) {
+    const int b = i >> 5;
+    t.w[i] = level_to_f16(kLevelBits[b >> 4]) | (level_to_f16(kLevelBits[b & 15]) << 16);
+  }
+  return t;
+}
+
+__device__ __align__(128) const PairTable kPairTable = make_pair_table();
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -54,6 +91,34 @@ __device__ __forceinline__ uint2 ldg_codes(const uint8_t* p) {
   return v;
 }
 
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 struct GemvArgs {
   const uint16_t* X;     // bf16 [M, K]
   const uint8_t* codes;  // [N*K/2]
@@ -62,50 +127,57 @@ struct GemvArgs {
   float* Y;              // fp32 [M, N]
   int64_t M, N, K;
   int nblk;              // K / 64
-  int bs;                // blocks per K-slice
-  int slices;            // number of K-slices
+  int slices;            // K-slices = cluster size along y
+  int max_nb;            // largest slice, in blocks
+  int* status;
 };
+
+__host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
+  return static_cast<int>((static_cast<int64_t>(nblk) * s) / slices);
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kGemvThreads)
 gemv_fwd_kernel(const GemvArgs p) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
-  float* ahat_s = reinterpret_cast<float*>(smem + kTabBytes);
-  float* xinv = ahat_s + kGemvRows * p.bs;
-  const int xstride_b = p.bs * 128 + 8;  // bytes per token row of the fp16 slice
-  uint8_t* xs = reinterpret_cast<uint8_t*>(xinv + 16);
+  float* ahat_s = reinterpret_cast<float*>(smem + kTabBytes);     // [128][max_nb]
+  float* xinv = ahat_s + kGemvRows * p.max_nb;                     // [16]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xinv + 16);
+  const int xstride_b = p.max_nb * 128 + 8;  // bytes per token row of the fp16 slice
+  uint8_t* xs = reinterpret_cast<uint8_t*>(bar + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kGemvRows;
-  const int kb0 = blockIdx.y * p.bs;
-  const int nb = min(p.bs, p.nblk - kb0);
+  const int slice = blockIdx.y;
+  const int kb0 = slice_begin(p.nblk, p.slices, slice);
+  const int nb = slice_begin(p.nblk, p.slices, slice + 1) - kb0;
   const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
   const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
   const int64_t rowg = row0 + warp * 16 + g, rowg8 = rowg + 8;
   const int64_t rowbytes = p.K / 2;
+  const uint32_t bar_a = tc::smem_addr(bar);
+
+  // Level table: one bulk copy, waited on before the main loop.
+  if (tid == 0) {
+    tc::mbar_init(bar_a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_arrive_expect_tx(bar_a, kTabBytes);
+    bulk_copy_g2s(tc::smem_addr(tab), &kPairTable, kTabBytes, bar_a);
+  }
 
   // Codes of this thread: rows g and g+8 of the warp, 8 bytes per block.
   const uint8_t* cg_ptr = p.codes + rowg * rowbytes + static_cast<int64_t>(kb0) * 32 + t * 8;
   const uint8_t* cg8_ptr = cg_ptr + 8 * rowbytes;
   const bool vg = rowg < p.N, vg8 = rowg8 < p.N;
-  uint2 cur[4][2];
+  uint2 cur[kRegBlocks][2];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kRegBlocks; ++j) {
     cur[j][0] = (vg && j < nb) ? ldg_codes(cg_ptr + j * 32) : make_uint2(0u, 0u);
     cur[j][1] = (vg8 && j < nb) ? ldg_codes(cg8_ptr + j * 32) : make_uint2(0u, 0u);
   }
 
-  // Level table: entry b of copy l at word 32 b + l; low half = level of the
-  // high nibble (the even, lower-k element), high half = level of the low one.
-  for (int i = tid; i < 256 * 32; i += kGemvThreads) {
-    const int b = i >> 5;
-    const __half lo = __float2half_rn(__uint_as_float(kLevelBitsDev[b >> 4]));
-    const __half hi = __float2half_rn(__uint_as_float(kLevelBitsDev[b & 15]));
-    tab[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-             (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-  }
   // Dequantized absmax of the CTA's rows over the slice.
   for (int i = tid; i < kGemvRows * nb; i += kGemvThreads) {
     const int r = i / nb, j = i - r * nb;
@@ -115,25 +187,45 @@ gemv_fwd_kernel(const GemvArgs p) {
       const int64_t bi = n * p.nblk + kb0 + j;
       v = dequant_absmax(p.a8[bi], p.s2[bi / kGroup]);
     }
-    ahat_s[r * p.bs + j] = v;
+    ahat_s[r * p.max_nb + j] = v;
   }
-  // Activations of the slice: per-token power-of-two scale, then fp16.
-  const int nkv = nb * kBlock;
-  for (int tk = warp; tk < 16; tk += kGemvThreads / 32) {
-    const bool valid = tk < mt;
-    const uint2* xr = reinterpret_cast<const uint2*>(
-        p.X + (m0 + (valid ? tk : 0)) * p.K + static_cast<int64_t>(kb0) * kBlock);
+
+  // Activations of the slice: per-token power-of-two scale, then fp16. Warp w
+  // converts tokens w and w + 8 (those below mt); slices of up to 16 blocks
+  // go through registers in one pass, longer ones are read twice.
+  const int nkv4 = nb * (kBlock / 4);        // uint2 (4 bf16) per token row
+  for (int tk = warp; tk < mt; tk += kGemvThreads / 32) {
+    const uint2* xr = reinterpret_cast<const uint2*>(p.X + (m0 + tk) * p.K +
+                                                     static_cast<int64_t>(kb0) * kBlock);
+    uint2* dst = reinterpret_cast<uint2*>(xs + tk * xstride_b);
+    auto absmax4 = [](uint2 v) {
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+    };
+    auto convert = [](uint2 v, float scale) {
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
+      const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
+      return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    };
+    constexpr int kRegX = 8;                 // 8 uint2 per lane = 16 blocks
+    uint2 xv[kRegX];
     float mx = 0.0f;
-    if (valid) {
-      for (int i = lane; i < nkv / 4; i += 32) {
-        const uint2 v = __ldg(xr + i);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))));
-      }
+    const bool in_regs = nkv4 <= 32 * kRegX;
+    if (in_regs) {
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int u = 0; u < kRegX; ++u) {
+        const int i = lane + 32 * u;
+        xv[u] = (i < nkv4) ? __ldg(xr + i) : make_uint2(0u, 0u);
+        mx = fmaxf(mx, absmax4(xv[u]));
+      }
+    } else {
+      for (int i = lane; i < nkv4; i += 32) mx = fmaxf(mx, absmax4(__ldg(xr + i)));
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     int e = 0;
     if (mx > 0.0f) {
       const int E = max(1, static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu));
@@ -141,22 +233,19 @@ gemv_fwd_kernel(const GemvArgs p) {
     }
     const float scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
     if (lane == 0) xinv[tk] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    uint2* dst = reinterpret_cast<uint2*>(xs + tk * xstride_b);
-    for (int i = lane; i < nkv / 4; i += 32) {
-      uint2 o = make_uint2(0u, 0u);
-      if (valid) {
-        const uint2 v = __ldg(xr + i);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-        const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
-        const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
-        o.x = *reinterpret_cast<const uint32_t*>(&h0);
-        o.y = *reinterpret_cast<const uint32_t*>(&h1);
+    if (in_regs) {
+#pragma unroll
+      for (int u = 0; u < kRegX; ++u) {
+        const int i = lane + 32 * u;
+        if (i < nkv4) dst[i] = convert(xv[u], scale);
       }
-      dst[i] = o;
+    } else {
+      for (int i = lane; i < nkv4; i += 32) dst[i] = convert(__ldg(xr + i), scale);
     }
   }
   __syncthreads();
+  const bool tab_ok = tc::mbar_wait(bar_a, 0);
+  if (!tab_ok) report_status(p.status, kStatusTimeout);
 
   float acc[NT][4];
 #pragma unroll
@@ -165,19 +254,16 @@ gemv_fwd_kernel(const GemvArgs p) {
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
   const uint8_t* tab_b = reinterpret_cast<const uint8_t*>(tab) + lane * 4;
-  const float* ah_g = ahat_s + (warp * 16 + g) * p.bs;
-  const float* ah_g8 = ah_g + 8 * p.bs;
+  const float* ah_g = ahat_s + (warp * 16 + g) * p.max_nb;
+  const float* ah_g8 = ah_g + 8 * p.max_nb;
+  // B fragments of padding tokens are zero instead of being read
+  bool tok_ok[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < mt;
 
-  for (int j0 = 0; j0 < nb; j0 += 4) {
-    uint2 nxt[4][2];
+  for (int j0 = 0; j0 < nb && tab_ok; j0 += kRegBlocks) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int jn = j0 + 4 + j;
-      nxt[j][0] = (vg && jn < nb) ? ldg_codes(cg_ptr + jn * 32) : make_uint2(0u, 0u);
-      nxt[j][1] = (vg8 && jn < nb) ? ldg_codes(cg8_ptr + jn * 32) : make_uint2(0u, 0u);
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int jj = 0; jj < kRegBlocks; ++jj) {
       const int j = j0 + jj;
       if (j < nb) {
         float part[NT][4];
@@ -197,8 +283,10 @@ gemv_fwd_kernel(const GemvArgs p) {
           const uint32_t a3 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = *reinterpret_cast<const uint2*>(
-                xs + (nt * 8 + g) * xstride_b + (j * 64 + t * 16 + 4 * s) * 2);
+            uint2 b = make_uint2(0u, 0u);
+            if (tok_ok[nt])
+              b = *reinterpret_cast<const uint2*>(xs + (nt * 8 + g) * xstride_b +
+                                                  (j * 64 + t * 16 + 4 * s) * 2);
             mma_f16(part[nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -212,38 +300,52 @@ gemv_fwd_kernel(const GemvArgs p) {
         }
       }
     }
+    // refill the register ring with the next blocks of the slice
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      cur[j][0] = nxt[j][0];
-      cur[j][1] = nxt[j][1];
+    for (int jj = 0; jj < kRegBlocks; ++jj) {
+      const int jn = j0 + kRegBlocks + jj;
+      cur[jj][0] = (vg && jn < nb) ? ldg_codes(cg_ptr + jn * 32) : make_uint2(0u, 0u);
+      cur[jj][1] = (vg8 && jn < nb) ? ldg_codes(cg8_ptr + jn * 32) : make_uint2(0u, 0u);
     }
   }
 
-  // Epilogue: undo the token scales, stage [16 tokens x 128 rows] in shared
-  // memory, then one 16-byte store (or vector atomic add) per 4 rows.
+  // Epilogue: undo the token scales and stage this slice's partial
+  // [16 tokens x 128 rows] in shared memory (over the level table).
   __syncthreads();
   float* out_s = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
     const int rg = warp * 16 + g;
-    out_s[tk0 * kOutStride + rg] = acc[nt][0] * xinv[tk0];
-    out_s[tk1 * kOutStride + rg] = acc[nt][1] * xinv[tk1];
-    out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * xinv[tk0];
-    out_s[tk1 * kOutStride + rg + 8] = acc[nt][3] * xinv[tk1];
+    const float i0 = tk0 < mt ? xinv[tk0] : 0.0f, i1 = tk1 < mt ? xinv[tk1] : 0.0f;
+    out_s[tk0 * kOutStride + rg] = acc[nt][0] * i0;
+    out_s[tk1 * kOutStride + rg] = acc[nt][1] * i1;
+    out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * i0;
+    out_s[tk1 * kOutStride + rg + 8] = acc[nt][3] * i1;
   }
-  __syncthreads();
-  for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
-    const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
-    if (tk < mt && row0 + r4 < p.N) {
-      const float4 v = *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4);
-      float4* dst = reinterpret_cast<float4*>(p.Y + (m0 + tk) * p.N + row0 + r4);
-      if (p.slices == 1) {
-        *dst = v;
-      } else {
-        atomicAdd(dst, v);
+  if (p.slices == 1) {
+    __syncthreads();
+    for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
+      const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
+      if (tk < mt && row0 + r4 < p.N)
+        *reinterpret_cast<float4*>(p.Y + (m0 + tk) * p.N + row0 + r4) =
+            *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4);
+    }
+  } else {
+    // Cluster reduction: CTA `rank` sums rows [rank*rpc, (rank+1)*rpc) of every
+    // slice's partial through distributed shared memory and stores them.
+    cluster_sync();
+    const uint32_t rank = cluster_ctarank();
+    const int rpc = kGemvRows / p.slices;
+    for (int i = tid; i < 8 * NT * rpc; i += kGemvThreads) {
+      const int tk = i / rpc, r = static_cast<int>(rank) * rpc + (i % rpc);
+      if (tk < mt && row0 + r < p.N) {
+        float v = 0.0f;
+        for (int c = 0; c < p.slices; ++c) v += ld_dsmem(out_s + tk * kOutStride + r, c);
+        p.Y[(m0 + tk) * p.N + row0 + r] = v;
       }
     }
+    cluster_sync();   // no CTA leaves while its partial may still be read
   }
 }
 
@@ -325,7 +427,7 @@ simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __rest
 
 cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
                             const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
-                            int num_sms, cudaStream_t st) {
+                            int num_sms, int* status, cudaStream_t st) {
   GemvArgs a;
   a.X = X;
   a.codes = codes;
@@ -336,38 +438,44 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   a.N = N;
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
-  // K-slices: aim for about two CTAs per SM in total.
+  a.status = status;
+  // K-slices (cluster size): aim for about two CTAs per SM, at most 8, each
+  // slice at least one block and at most kMaxSliceBlocks blocks.
   const int64_t row_ctas = (N + kGemvRows - 1) / kGemvRows;
-  int64_t want = (2 * static_cast<int64_t>(num_sms) + row_ctas - 1) / row_ctas;
-  want = std::max<int64_t>(1, std::min<int64_t>(want, a.nblk));
-  int bs = static_cast<int>((a.nblk + want - 1) / want);
-  bs = std::max(1, std::min(bs, kMaxSliceBlocks));
-  a.bs = bs;
-  a.slices = (a.nblk + bs - 1) / bs;
+  int slices = 1;
+  while (slices < kMaxCluster && row_ctas * slices < 2 * static_cast<int64_t>(num_sms) &&
+         slices * 2 <= a.nblk)
+    slices *= 2;
+  while (slices < kMaxCluster && (a.nblk + slices - 1) / slices > kMaxSliceBlocks) slices *= 2;
+  if ((a.nblk + slices - 1) / slices > kMaxSliceBlocks) return cudaErrorInvalidValue;
+  a.slices = slices;
+  a.max_nb = (a.nblk + slices - 1) / slices;
   const int nt = (M <= 8) ? 1 : 2;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
-  const size_t smem = kTabBytes + static_cast<size_t>(kGemvRows) * bs * 4 + 64 +
-                      16 * static_cast<size_t>(bs * 128 + 8);
-  if (a.slices > 1) {
-    cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), st);
-    if (e != cudaSuccess) return e;
-  }
-  dim3 grid(static_cast<unsigned>(row_ctas), static_cast<unsigned>(a.slices),
-            static_cast<unsigned>(mtiles));
-  // The largest slice needs ~113 KB of dynamic shared memory; opt in once.
+  const size_t smem = kTabBytes + static_cast<size_t>(kGemvRows) * a.max_nb * 4 + 64 + 16 +
+                      8 * nt * static_cast<size_t>(a.max_nb * 128 + 8);
   static std::once_flag once;
   std::call_once(once, [] {
-    const int max_smem = kTabBytes + kGemvRows * kMaxSliceBlocks * 4 + 64 +
+    const int max_smem = kTabBytes + kGemvRows * kMaxSliceBlocks * 4 + 64 + 16 +
                          16 * (kMaxSliceBlocks * 128 + 8);
     cudaFuncSetAttribute(gemv_fwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   });
-  if (nt == 1) {
-    gemv_fwd_kernel<1><<<grid, kGemvThreads, smem, st>>>(a);
-  } else {
-    gemv_fwd_kernel<2><<<grid, kGemvThreads, smem, st>>>(a);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(slices),
+                     static_cast<unsigned>(mtiles));
+  cfg.blockDim = dim3(kGemvThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(slices);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (nt == 1) return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1>, a);
+  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2>, a);
 }
 
 cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,

@@ -9,17 +9,23 @@
 // 256), looping over the reduction in stages of 64:
 //   * warp 0 (one thread) TMA-loads the stage's activation tile (bf16,
 //     128-byte swizzle, the K-major B operand) and its packed-code tile;
-//   * warps 2-9 dequantize the codes (level * dequantized absmax, rounded to
-//     bf16) and write them straight into tensor memory, where the MMA reads
-//     its A operand: the dequantized weight never touches shared memory;
+//   * warps 2-9, in two groups of four that take alternate stages,
+//     dequantize the codes (level * dequantized absmax, rounded to bf16) and
+//     write them straight into tensor memory, where the MMA reads its A
+//     operand: the dequantized weight never touches shared memory. The
+//     forward looks up both levels of a code byte at once in a 256-entry pair
+//     table kept in 32 lane-private copies (every lookup of a warp hits 32
+//     distinct banks); the input gradient builds, per stage, a table of the 16
+//     levels pre-multiplied by each row's dequantized absmax;
 //   * warp 1 (one thread) issues tcgen05.mma (128 x BN x 16) into an fp32
 //     accumulator in tensor memory and commits each stage back to the
 //     producer;
 //   * warps 2-9 then read the accumulator with tcgen05.ld and store fp32
 //     outputs (coalesced: 32 consecutive outputs of one token per warp store).
-// The forward walks a tile of 128 weight rows along K; the input gradient
-// walks a tile of 128 weight columns along N, reading each column's nibbles
-// down 64 rows per stage (the transposed walk). When the output tiles alone
+// The forward walks a tile of 128 weight rows along K, one row per dequant
+// thread; the input gradient walks a tile of 128 weight columns along N, one
+// column per dequant thread, reading its nibbles down the stage's 64 rows
+// (the transposed walk). When the output tiles alone
 // cannot fill the GPU the reduction is split across CTAs and summed with
 // atomics into a zeroed output.
 //
@@ -36,7 +42,7 @@ namespace nf4 {
 namespace {
 
 constexpr int kTcThreads = 320;              // 10 warps
-constexpr int kDqThreads = 256;              // warps 2-9
+constexpr int kDqGroupThreads = 128;         // warps 2-5 and 6-9, alternate stages
 constexpr int kStages = 4;
 constexpr int kTileRows = 128;               // MMA M
 constexpr int kMaxBN = 256;                  // MMA N
@@ -45,11 +51,15 @@ constexpr int kCodesStageBytes = 4096;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA0 = 256;            // columns [256, 384): A-operand slots
 
+constexpr int kPairLutBytes = 256 * 32 * 8;           // forward: (c[hi], c[lo]) x 32 copies
+constexpr int kScaledLutBytes = kStages * 64 * 2 * 16 * 4;  // dX: per stage [64][2][16]
+constexpr int kLutBytes = kPairLutBytes > kScaledLutBytes ? kPairLutBytes : kScaledLutBytes;
+
 constexpr int kOffAct = 0;
 constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
-constexpr int kOffAhat = kOffCodes + kStages * kCodesStageBytes;
-constexpr int kOffLut = kOffAhat + kStages * 128 * 4;
-constexpr int kOffBars = kOffLut + 64;
+constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
+constexpr int kOffLevels = kOffLut + kLutBytes;
+constexpr int kOffBars = kOffLevels + 64;
 constexpr int kNumBars = 3 * kStages + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
@@ -79,8 +89,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* lut = reinterpret_cast<float*>(smem + kOffLut);
-  float* ahat_s = reinterpret_cast<float*>(smem + kOffAhat);
+  float* levels = reinterpret_cast<float*>(smem + kOffLevels);
   const uint32_t bars = tc::smem_addr(smem + kOffBars);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto dq_bar = [&](int s) { return bars + 8u * (kStages + s); };
@@ -95,11 +104,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   const int s_begin = blockIdx.z * p.stages_per_split;
   const int nst = min(p.stages_per_split, p.stages_total - s_begin);
 
-  if (threadIdx.x < 16) lut[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
+  if (threadIdx.x < 16) levels[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
+  if (!kDx && warp >= 2) {
+    // pair table: entry b, copy l at float2 index 32 b + l
+    float2* pair = reinterpret_cast<float2*>(smem + kOffLut);
+    for (int b = warp - 2; b < 256; b += 8)
+      pair[32 * b + lane] = make_float2(__uint_as_float(kLevelBitsDev[b >> 4]),
+                                        __uint_as_float(kLevelBitsDev[b & 15]));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      tc::mbar_init(dq_bar(s), kDqThreads);
+      tc::mbar_init(dq_bar(s), kDqGroupThreads);
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
@@ -174,61 +190,65 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   } else {
     // ---------------------------------------------------- dequant + store --
     const int q = warp & 3;             // TMEM lane quarter of this warp
-    const int h = (warp - 2) >> 2;      // which half of each stage's columns
+    const int grp = (warp - 2) >> 2;    // dequant group: takes stages i % 2 == grp
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const float* ahat_slots = ahat_s;
+    const int gt = 32 * q + lane;       // thread index within the group (= TMEM lane)
     if (!kDx) {
-      const int row = 32 * q + lane;
-      const int64_t n = r0 + row;
+      const int64_t n = r0 + gt;        // this thread's weight row
       const bool vrow = n < p.N;
+      const uint8_t* pair_b = smem + kOffLut + lane * 8;
       uint32_t a8v = 0;
       float s2v = 0.0f;
-      if (vrow && nst > 0) {
-        const int64_t bi = n * p.nblk + s_begin;
-        a8v = p.a8[bi];
-        s2v = p.s2[bi >> 8];
-      }
-      for (int i = 0; i < nst; ++i) {
-        const int slot = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
-        if (vrow && i + 1 < nst) {
-          const int64_t bi = n * p.nblk + s_begin + i + 1;
+      auto load_scale = [&](int i) {
+        if (vrow && i < nst) {
+          const int64_t bi = n * p.nblk + s_begin + i;
           a8v = p.a8[bi];
           s2v = p.s2[bi >> 8];
         }
+      };
+      load_scale(grp);
+      for (int i = grp; i < nst; i += 2) {
+        const int slot = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
+        load_scale(i + 2);
         if (*abort_flag) continue;
         if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
-        const uint4 c = *reinterpret_cast<const uint4*>(smem + kOffCodes + slot * kCodesStageBytes +
-                                                        row * 32 + 16 * h);
-        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-        uint32_t v[16];
+        const uint8_t* crow = smem + kOffCodes + slot * kCodesStageBytes + gt * 32;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint4 c = *reinterpret_cast<const uint4*>(crow + 16 * hf);
+          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+          uint32_t v[16];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint32_t byte = (words[j] >> (8 * b)) & 0xffu;
-            v[4 * j + b] = pack_bf16x2(__fmul_rn(lut[byte >> 4], ahat), __fmul_rn(lut[byte & 15u], ahat));
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const uint32_t byte = (words[j] >> (8 * b)) & 0xffu;
+              const float2 lv = *reinterpret_cast<const float2*>(pair_b + (byte << 8));
+              v[4 * j + b] = pack_bf16x2(__fmul_rn(lv.x, ahat), __fmul_rn(lv.y, ahat));
+            }
           }
+          tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
         }
-        tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * h, v);
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(dq_bar(slot));
       }
     } else {
-      const int kl = 32 * q + lane;     // weight column within the tile
+      const int kl = gt;                // weight column within the tile
       const int kbl = kl >> 6;          // its absmax block within the tile
       const int sh = (kl & 1) ? 0 : 4;  // even column: high nibble
-      // dequantized-absmax table of each stage: 64 rows x 2 blocks, one entry
-      // per thread of the first half
-      const int e_row = kl >> 1, e_blk = kl & 1;
+      // Per stage, thread gt owns row gt >> 1 of block gt & 1 of the scaled
+      // level table: 16 levels times that row-block's dequantized absmax.
+      const int e_row = gt >> 1, e_blk = gt & 1;
       const int64_t e_kb = (r0 >> 6) + e_blk;
       uint32_t a8v = 0;
       float s2v = 0.0f;
       bool e_valid = false;
-      auto load_entry = [&](int s) {
-        const int64_t n = static_cast<int64_t>(s) * 64 + e_row;
+      auto load_entry = [&](int i) {
+        if (i >= nst) return;
+        const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + e_row;
         e_valid = (n < p.N) && (e_kb < p.nblk);
         if (e_valid) {
           const int64_t bi = n * p.nblk + e_kb;
@@ -236,29 +256,38 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           s2v = p.s2[bi >> 8];
         }
       };
-      if (h == 0 && nst > 0) load_entry(s_begin);
-      for (int i = 0; i < nst; ++i) {
+      load_entry(grp);
+      for (int i = grp; i < nst; i += 2) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        float* ah = const_cast<float*>(ahat_slots) + slot * 128;
-        if (h == 0) {
-          ah[e_row * 2 + e_blk] = e_valid ? dequant_absmax(a8v, s2v) : 0.0f;
-          if (i + 1 < nst) load_entry(s_begin + i + 1);
+        float* tab = reinterpret_cast<float*>(smem + kOffLut) + slot * (64 * 2 * 16);
+        {
+          const float ahat = e_valid ? dequant_absmax(a8v, s2v) : 0.0f;
+          float4* dst = reinterpret_cast<float4*>(tab + (e_row * 2 + e_blk) * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(__fmul_rn(levels[4 * j], ahat), __fmul_rn(levels[4 * j + 1], ahat),
+                                 __fmul_rn(levels[4 * j + 2], ahat), __fmul_rn(levels[4 * j + 3], ahat));
+          load_entry(i + 2);
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        // the group's 128 threads meet here (named barrier 1 + group)
+        if (grp == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+        else asm volatile("bar.sync 2, 128;" ::: "memory");
         if (*abort_flag) continue;
         if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
         const uint8_t* cs = smem + kOffCodes + slot * kCodesStageBytes + (kl >> 1);
-        uint32_t v[16];
+        const float* tb = tab + kbl * 16;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int rr = 32 * h + 2 * jj;
-          const uint32_t b0 = cs[rr * 64], b1 = cs[(rr + 1) * 64];
-          const float w0 = __fmul_rn(lut[(b0 >> sh) & 15u], ah[rr * 2 + kbl]);
-          const float w1 = __fmul_rn(lut[(b1 >> sh) & 15u], ah[(rr + 1) * 2 + kbl]);
-          v[jj] = pack_bf16x2(w0, w1);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int rr = 32 * hf + 2 * jj;
+            const uint32_t b0 = cs[rr * 64], b1 = cs[(rr + 1) * 64];
+            v[jj] = pack_bf16x2(tb[rr * 32 + ((b0 >> sh) & 15u)], tb[(rr + 1) * 32 + ((b1 >> sh) & 15u)]);
+          }
+          tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
         }
-        tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * h, v);
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(dq_bar(slot));
@@ -273,7 +302,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       const int64_t nd = kDx ? p.K : p.N;
       const bool vrow = rg < nd;
       const int half = p.bn / 2;
-      for (int c = h * half; c < (h + 1) * half; c += 16) {
+      for (int c = grp * half; c < (grp + 1) * half; c += 16) {
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
         tc::tmem_wait_ld();

@@ -304,10 +304,12 @@ def test_quantize_quotients_on_decision_edges():
     for j in range(1, 64):
         m = mids[rng.integers(0, 15, nblocks)] * np.where(rng.random(nblocks) < 0.5, 1, -1)
         m = np.clip(m, -0.999, 0.999)
-        base = (m * absmax.astype(np.float64)).astype(np.float32)
+        base = np.abs(m * absmax.astype(np.float64)).astype(np.float32)
         k = rng.integers(-3, 4, nblocks).astype(np.int32)
-        W[:, j] = (base.view(np.int32) + k).view(np.float32)
+        mag = np.maximum(base.view(np.int32) + k, 0).view(np.float32)   # step |w| by k ulps
+        W[:, j] = np.where(m < 0, -mag, mag)
     W = np.where(np.abs(W) > np.abs(W[:, :1]), W[:, :1], W).astype(np.float32)
+    assert np.isfinite(W).all()
     W = W.reshape(256, 1024)
     q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
     assert_quant_full(W, q)
