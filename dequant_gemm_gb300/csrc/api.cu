@@ -51,9 +51,10 @@ nf4_status current_device(DeviceInfo** out) {
   return NF4_OK;
 }
 
-// Token counts up to this use the streaming small-M kernels; larger ones the
+// Token counts up to these use the streaming small-M kernels; larger ones the
 // tensor-memory GEMM.
-constexpr int64_t kSmallM = 16;
+constexpr int64_t kSmallMFwd = 64;
+constexpr int64_t kSmallMDx = 16;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -124,7 +125,7 @@ nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, flo
   DeviceInfo* d = nullptr;
   if (nf4_status s = current_device(&d)) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (M <= kSmallM)
+  if (M <= kSmallMFwd)
     return launched(nf4::launch_gemv_fwd(X, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,
                                          w->cols, Y, d->num_sms, d->status, st));
   return launched(nf4::launch_tc_fwd(X, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,
@@ -147,7 +148,7 @@ nf4_status nf4_matmul_bwd_dx(const uint16_t* dY, int64_t M, const nf4_weight* w,
   DeviceInfo* d = nullptr;
   if (nf4_status s = current_device(&d)) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (M <= kSmallM)
+  if (M <= kSmallMDx)
     return launched(nf4::launch_simt_dx(dY, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,
                                         w->cols, dX, d->num_sms, st));
   return launched(nf4::launch_tc_dx(dY, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,

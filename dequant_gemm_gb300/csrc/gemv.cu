@@ -1,4 +1,4 @@
-// Small-M fused NF4-dequant matmul: Y = X * dequant(W)^T for M <= 16 tokens
+// Small-M fused NF4-dequant matmul: Y = X * dequant(W)^T for M <= 64 tokens
 // (decode shapes), and a plain fp32 input-gradient kernel for small M
 // ("Zenbit", zenbit.pallas_nf4 bullet: the compressed weight is streamed and
 // dequantized on chip; the full-precision weight never reaches HBM).
@@ -9,9 +9,10 @@
 //    partial sums through distributed shared memory, so every output is
 //    written once with a plain store (no zeroing pass, no atomics).
 //  * The weight is the A operand of mma.sync.m16n8k16 (16 rows per warp), the
-//    tokens are the N operand (8 per n-tile): the "swap AB" shape for skinny
-//    products. The first code loads of a thread are issued before the
-//    prologue.
+//    tokens are the N operand (8 per n-tile, up to 8 n-tiles): the "swap AB"
+//    shape for skinny products. Each weight is dequantized once per CTA for
+//    all of its tokens. Every global load of the prologue (codes, absmax
+//    codes, scales, activations) is issued before any of them is used.
 //  * Dequantization is factored as  sum_b ahat_b * (sum_{k in b} x_k c[q_k]):
 //    the MMA consumes the raw levels c[q] and each 64-weight block's partial
 //    sum is scaled by its dequantized absmax in fp32 afterwards. The levels
@@ -142,8 +143,8 @@ gemv_fwd_kernel(const GemvArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
   float* ahat_s = reinterpret_cast<float*>(smem + kTabBytes);     // [128][max_nb]
-  float* xinv = ahat_s + kGemvRows * p.max_nb;                     // [16]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(xinv + 16);
+  float* xinv = ahat_s + kGemvRows * p.max_nb;                     // [64]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xinv + 64);
   const int xstride_b = p.max_nb * 128 + 8;  // bytes per token row of the fp16 slice
   uint8_t* xs = reinterpret_cast<uint8_t*>(bar + 2);
 
@@ -178,71 +179,118 @@ gemv_fwd_kernel(const GemvArgs p) {
     cur[j][1] = (vg8 && j < nb) ? ldg_codes(cg8_ptr + j * 32) : make_uint2(0u, 0u);
   }
 
-  // Dequantized absmax of the CTA's rows over the slice.
-  for (int i = tid; i < kGemvRows * nb; i += kGemvThreads) {
-    const int r = i / nb, j = i - r * nb;
-    const int64_t n = row0 + r;
-    float v = 0.0f;
-    if (n < p.N) {
-      const int64_t bi = n * p.nblk + kb0 + j;
-      v = dequant_absmax(p.a8[bi], p.s2[bi / kGroup]);
-    }
-    ahat_s[r * p.max_nb + j] = v;
+  // Activations, pass 1: per-token max |x| of the slice (positive floats
+  // order as integers, so a shared atomicMax on the bits reduces them).
+  unsigned int* xmax = reinterpret_cast<unsigned int*>(xinv);   // reused for 2^-e below
+  if (tid < 8 * NT) xmax[tid] = 0u;
+  const int nkv4 = nb * (kBlock / 4);        // uint2 (4 bf16) per token row
+  const int nx = mt * nkv4;
+  const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K + static_cast<int64_t>(kb0) * kBlock);
+  const int64_t xrow4 = p.K / 4;
+  auto xload = [&](int i) {
+    const int tk = i / nkv4, c = i - tk * nkv4;
+    return __ldg(xbase + tk * xrow4 + c);
+  };
+  auto absmax4 = [](uint2 v) {
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+  };
+  constexpr int kXBatch = 8;
+  uint2 xv[kXBatch];
+#pragma unroll
+  for (int u = 0; u < kXBatch; ++u) {
+    const int i = tid + kGemvThreads * u;
+    xv[u] = (i < nx) ? xload(i) : make_uint2(0u, 0u);
   }
 
-  // Activations of the slice: per-token power-of-two scale, then fp16. Warp w
-  // converts tokens w and w + 8 (those below mt); slices of up to 16 blocks
-  // go through registers in one pass, longer ones are read twice.
-  const int nkv4 = nb * (kBlock / 4);        // uint2 (4 bf16) per token row
-  for (int tk = warp; tk < mt; tk += kGemvThreads / 32) {
-    const uint2* xr = reinterpret_cast<const uint2*>(p.X + (m0 + tk) * p.K +
-                                                     static_cast<int64_t>(kb0) * kBlock);
-    uint2* dst = reinterpret_cast<uint2*>(xs + tk * xstride_b);
-    auto absmax4 = [](uint2 v) {
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-      return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-    };
-    auto convert = [](uint2 v, float scale) {
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-      const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
-      const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
-      return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-    };
-    constexpr int kRegX = 8;                 // 8 uint2 per lane = 16 blocks
-    uint2 xv[kRegX];
-    float mx = 0.0f;
-    const bool in_regs = nkv4 <= 32 * kRegX;
-    if (in_regs) {
+  // Dequantized absmax of the CTA's rows over the slice: loads first.
+  constexpr int kAhBatch = 4;
+  {
+    uint32_t av[kAhBatch];
+    float sv[kAhBatch];
+    for (int base = tid; base < kGemvRows * nb; base += kGemvThreads * kAhBatch) {
 #pragma unroll
-      for (int u = 0; u < kRegX; ++u) {
-        const int i = lane + 32 * u;
-        xv[u] = (i < nkv4) ? __ldg(xr + i) : make_uint2(0u, 0u);
-        mx = fmaxf(mx, absmax4(xv[u]));
+      for (int u = 0; u < kAhBatch; ++u) {
+        const int i = base + kGemvThreads * u;
+        av[u] = 0u;
+        sv[u] = 0.0f;
+        if (i < kGemvRows * nb) {
+          const int r = i / nb, j = i - r * nb;
+          const int64_t n = row0 + r;
+          if (n < p.N) {
+            const int64_t bi = n * p.nblk + kb0 + j;
+            av[u] = __ldg(p.a8 + bi);
+            sv[u] = __ldg(p.s2 + bi / kGroup);
+          }
+        }
       }
-    } else {
-      for (int i = lane; i < nkv4; i += 32) mx = fmaxf(mx, absmax4(__ldg(xr + i)));
-    }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int u = 0; u < kAhBatch; ++u) {
+        const int i = base + kGemvThreads * u;
+        if (i < kGemvRows * nb) {
+          const int r = i / nb, j = i - r * nb;
+          ahat_s[r * p.max_nb + j] = dequant_absmax(av[u], sv[u]);
+        }
+      }
+    }
+  }
+  __syncthreads();   // xmax zeroed
+  {
+    int last_tk = -1;
+    float mx = 0.0f;
+    auto flush = [&]() {
+      if (last_tk >= 0 && mx > 0.0f) atomicMax(xmax + last_tk, __float_as_uint(mx));
+    };
+    for (int base = 0; base < nx; base += kGemvThreads * kXBatch) {
+#pragma unroll
+      for (int u = 0; u < kXBatch; ++u) {
+        const int i = base + tid + kGemvThreads * u;
+        if (i < nx) {
+          const uint2 v = (base == 0) ? xv[u] : xload(i);
+          const int tk = i / nkv4;
+          if (tk != last_tk) {
+            flush();
+            last_tk = tk;
+            mx = 0.0f;
+          }
+          mx = fmaxf(mx, absmax4(v));
+        }
+      }
+    }
+    flush();
+  }
+  __syncthreads();
+  // Pass 2: scale each token by 2^e (max |x| into [2^14, 2^15)) and convert.
+  if (tid < 8 * NT) {
+    const float mx = __uint_as_float(xmax[tid]);
     int e = 0;
     if (mx > 0.0f) {
       const int E = max(1, static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu));
       e = min(141 - E, 126);
     }
-    const float scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-    if (lane == 0) xinv[tk] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    if (in_regs) {
+    xinv[tid] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);   // scale for now
+  }
+  __syncthreads();
+  for (int base = 0; base < nx; base += kGemvThreads * kXBatch) {
 #pragma unroll
-      for (int u = 0; u < kRegX; ++u) {
-        const int i = lane + 32 * u;
-        if (i < nkv4) dst[i] = convert(xv[u], scale);
+    for (int u = 0; u < kXBatch; ++u) {
+      const int i = base + tid + kGemvThreads * u;
+      if (i < nx) {
+        const uint2 v = (base == 0) ? xv[u] : xload(i);
+        const int tk = i / nkv4, c = i - tk * nkv4;
+        const float scale = xinv[tk];
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
+        const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
+        reinterpret_cast<uint2*>(xs + tk * xstride_b)[c] =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
       }
-    } else {
-      for (int i = lane; i < nkv4; i += 32) dst[i] = convert(__ldg(xr + i), scale);
     }
   }
+  __syncthreads();
+  if (tid < 8 * NT) xinv[tid] = 1.0f / xinv[tid];   // exact: a power of two
   __syncthreads();
   const bool tab_ok = tc::mbar_wait(bar_a, 0);
   if (!tab_ok) report_status(p.status, kStatusTimeout);
@@ -310,14 +358,22 @@ gemv_fwd_kernel(const GemvArgs p) {
   }
 
   // Epilogue: undo the token scales and stage this slice's partial
-  // [16 tokens x 128 rows] in shared memory (over the level table).
+  // [8 NT tokens x 128 rows] in shared memory (over the level table and,
+  // for 64 tokens, the start of the absmax table, both no longer read).
+  float inv0[NT], inv1[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int tk0 = nt * 8 + 2 * t;
+    inv0[nt] = tk0 < mt ? xinv[tk0] : 0.0f;
+    inv1[nt] = tk0 + 1 < mt ? xinv[tk0 + 1] : 0.0f;
+  }
   __syncthreads();
   float* out_s = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
     const int rg = warp * 16 + g;
-    const float i0 = tk0 < mt ? xinv[tk0] : 0.0f, i1 = tk1 < mt ? xinv[tk1] : 0.0f;
+    const float i0 = inv0[nt], i1 = inv1[nt];
     out_s[tk0 * kOutStride + rg] = acc[nt][0] * i0;
     out_s[tk1 * kOutStride + rg] = acc[nt][1] * i1;
     out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * i0;
@@ -425,6 +481,19 @@ simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __rest
 
 }  // namespace
 
+// Dynamic shared memory of one GEMV CTA: level table, absmax table,
+// 64 token scales, the mbarrier, and the fp16 activation slice.
+constexpr size_t gemv_smem_bytes(int nt, int max_nb) {
+  return kTabBytes + static_cast<size_t>(kGemvRows) * max_nb * 4 + 64 * 4 + 16 +
+         8 * static_cast<size_t>(nt) * (static_cast<size_t>(max_nb) * 128 + 8);
+}
+constexpr size_t kGemvSmemLimit = 220 * 1024;
+
+template <int NT>
+cudaError_t launch_gemv_nt(const cudaLaunchConfig_t& cfg, const GemvArgs& a) {
+  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<NT>, a);
+}
+
 cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
                             const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
                             int num_sms, int* status, cudaStream_t st) {
@@ -450,16 +519,19 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   if ((a.nblk + slices - 1) / slices > kMaxSliceBlocks) return cudaErrorInvalidValue;
   a.slices = slices;
   a.max_nb = (a.nblk + slices - 1) / slices;
-  const int nt = (M <= 8) ? 1 : 2;
+  // n-tiles of 8 tokens per CTA: all tokens at once when the activation slice
+  // fits, otherwise fewer tokens per CTA and more CTAs along z.
+  int nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
+  while (nt > 1 && gemv_smem_bytes(nt, a.max_nb) > kGemvSmemLimit) nt /= 2;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
-  const size_t smem = kTabBytes + static_cast<size_t>(kGemvRows) * a.max_nb * 4 + 64 + 16 +
-                      8 * nt * static_cast<size_t>(a.max_nb * 128 + 8);
+  const size_t smem = gemv_smem_bytes(nt, a.max_nb);
   static std::once_flag once;
   std::call_once(once, [] {
-    const int max_smem = kTabBytes + kGemvRows * kMaxSliceBlocks * 4 + 64 + 16 +
-                         16 * (kMaxSliceBlocks * 128 + 8);
-    cudaFuncSetAttribute(gemv_fwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    const int lim = static_cast<int>(kGemvSmemLimit);
+    cudaFuncSetAttribute(gemv_fwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(gemv_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(gemv_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(slices),
@@ -474,8 +546,12 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (nt == 1) return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1>, a);
-  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2>, a);
+  switch (nt) {
+    case 1: return launch_gemv_nt<1>(cfg, a);
+    case 2: return launch_gemv_nt<2>(cfg, a);
+    case 4: return launch_gemv_nt<4>(cfg, a);
+    default: return launch_gemv_nt<8>(cfg, a);
+  }
 }
 
 cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,

@@ -16,46 +16,49 @@ namespace {
 // quotient (P. Markstein, "Computation of elementary functions on the IBM
 // RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990). The theorem
 // needs the intermediate values to stay normal: blocks whose absmax is below
-// 2^-64 are scaled by 2^64 first (exact), and |w| <= 1e36 keeps 1/a normal.
+// 2^-64 (and all-zero blocks) take the plain IEEE division instead, and
+// |w| <= 1e36 keeps 1/a normal.
 struct BlockDivisor {
-  float a;      // absmax (scaled)
-  float r;      // RN(1 / a)
-  float s;      // power-of-two pre-scale of the weights
-  bool nz;      // a > 0
+  float a;      // absmax
+  float r;      // RN(1 / a) on the fast path
+  bool slow;    // a < 2^-64
 };
 
 __device__ __forceinline__ BlockDivisor make_divisor(float a) {
   BlockDivisor d;
-  d.nz = a > 0.0f;
-  d.s = (a < 5.421010862427522e-20f) ? 1.8446744073709552e19f : 1.0f;   // 2^-64, 2^64
-  d.a = __fmul_rn(a, d.s);
-  d.r = d.nz ? __frcp_rn(d.a) : 0.0f;
+  d.a = a;
+  d.slow = a < 5.421010862427522e-20f;   // 2^-64
+  d.r = d.slow ? 0.0f : __frcp_rn(a);
   return d;
 }
 
 __device__ __forceinline__ float normalise(float w, const BlockDivisor& d) {
-  const float ws = __fmul_rn(w, d.s);
-  const float q0 = __fmul_rn(ws, d.r);
-  const float rem = __fmaf_rn(-q0, d.a, ws);
-  const float x = __fmaf_rn(rem, d.r, q0);
-  return d.nz ? x : 0.0f;   // an all-zero block maps to level 0
+  if (!d.slow) {
+    const float q0 = __fmul_rn(w, d.r);
+    const float rem = __fmaf_rn(-q0, d.a, w);
+    return __fmaf_rn(rem, d.r, q0);
+  }
+  return d.a > 0.0f ? __fdiv_rn(w, d.a) : 0.0f;   // an all-zero block maps to level 0
 }
 
 // Nearest level of x in [-1, 1], ties to the lower index, through 33 buckets
-// of width 1/16: b = trunc(16 x + 16). No decision threshold lies within
-// 0.0017 of a multiple of 1/16 and neighbouring thresholds are more than 1/16
-// apart, so every bucket holds at most one threshold and its lower edge is
-// not near one; the code is lo[b] + (x > thr[b]) with lo[b] the number of
+// of width 1/16 centred on the multiples of 1/16: b = round(16 x + 16), read
+// from the low bits of fl32(16 x + 16 + 1.5 * 2^23). No decision threshold lies
+// within 0.004 of a bucket edge (an odd multiple of 1/32) and neighbouring
+// thresholds are more than 1/16 apart, so a bucket holds at most one
+// threshold and an x rounded into the neighbouring bucket at an edge gets the
+// same code; the code is lo[b] + (x > thr[b]) with lo[b] the number of
 // thresholds below the bucket and thr[b] the threshold inside it (2 if none).
-struct Bucket {
-  float thr;
-  uint32_t lo;
+struct Buckets {
+  float thr[33];
+  uint32_t lo[33];
 };
 
-__device__ __forceinline__ void build_buckets(Bucket* tab) {
+__device__ __forceinline__ void build_buckets(Buckets* tab) {
   const int b = threadIdx.x;
   if (b <= 32) {
-    const float lo_edge = (b - 16) * 0.0625f, hi_edge = (b - 15) * 0.0625f;
+    const float lo_edge = static_cast<float>(2 * b - 33) * 0.03125f;
+    const float hi_edge = lo_edge + 0.0625f;
     uint32_t lo = 0;
     float thr = 2.0f;
 #pragma unroll
@@ -64,20 +67,19 @@ __device__ __forceinline__ void build_buckets(Bucket* tab) {
       lo += (t < lo_edge) ? 1u : 0u;
       if (t > lo_edge && t < hi_edge) thr = t;
     }
-    tab[b].thr = thr;
-    tab[b].lo = lo;
+    tab->thr[b] = thr;
+    tab->lo[b] = lo;
   }
 }
 
-__device__ __forceinline__ uint32_t nearest_code(float x, const Bucket* tab) {
-  const int b = __float2int_rz(__fmaf_rn(x, 16.0f, 16.0f));
-  const Bucket e = tab[b];
-  return e.lo + ((x > e.thr) ? 1u : 0u);
+__device__ __forceinline__ uint32_t nearest_code(float x, const Buckets* tab) {
+  const uint32_t b = __float_as_uint(__fmaf_rn(x, 16.0f, 12582928.0f)) & 63u;
+  return tab->lo[b] + ((x > tab->thr[b]) ? 1u : 0u);
 }
 
 // Codes of the four weights of a float4 packed as two bytes (little-endian
 // u16): element 4j in the high nibble of the first byte.
-__device__ __forceinline__ uint32_t quantize4(float4 v, const BlockDivisor& d, const Bucket* tab) {
+__device__ __forceinline__ uint32_t quantize4(float4 v, const BlockDivisor& d, const Buckets* tab) {
   const uint32_t q0 = nearest_code(normalise(v.x, d), tab);
   const uint32_t q1 = nearest_code(normalise(v.y, d), tab);
   const uint32_t q2 = nearest_code(normalise(v.z, d), tab);
@@ -102,8 +104,8 @@ quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restri
                 uint8_t* __restrict__ a8_out, float* __restrict__ s2_out) {
   __shared__ float s_absmax[kGroup];
   __shared__ float s_warp_max[kQThreads / 32];
-  __shared__ Bucket s_buckets[33];
-  build_buckets(s_buckets);
+  __shared__ Buckets s_buckets;
+  build_buckets(&s_buckets);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kGroup;
@@ -127,7 +129,7 @@ quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restri
     for (int off = 8; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
     const int b = wblk0 + 2 * i + (lane >> 4);
     if (b < nblk) {
-      dst[32 * i + lane] = static_cast<uint16_t>(quantize4(v[i], make_divisor(a), s_buckets));
+      dst[32 * i + lane] = static_cast<uint16_t>(quantize4(v[i], make_divisor(a), &s_buckets));
       if ((lane & 15) == 0) s_absmax[b] = a;
     }
   }

@@ -52,7 +52,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA0 = 256;            // columns [256, 384): A-operand slots
 
 constexpr int kPairLutBytes = 256 * 32 * 8;           // forward: (c[hi], c[lo]) x 32 copies
-constexpr int kScaledLutBytes = kStages * 64 * 2 * 16 * 4;  // dX: per stage [64][2][16]
+// dX: per stage 64 rows x 2 blocks of 16 scaled levels, each entry padded to
+// 20 floats so that the 16-byte stores of a warp land on distinct banks
+constexpr int kScaledEntry = 20;
+constexpr int kScaledLutBytes = kStages * 64 * 2 * kScaledEntry * 4;
 constexpr int kLutBytes = kPairLutBytes > kScaledLutBytes ? kPairLutBytes : kScaledLutBytes;
 
 constexpr int kOffAct = 0;
@@ -260,10 +263,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       for (int i = grp; i < nst; i += 2) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        float* tab = reinterpret_cast<float*>(smem + kOffLut) + slot * (64 * 2 * 16);
+        float* tab = reinterpret_cast<float*>(smem + kOffLut) + slot * (64 * 2 * kScaledEntry);
         {
           const float ahat = e_valid ? dequant_absmax(a8v, s2v) : 0.0f;
-          float4* dst = reinterpret_cast<float4*>(tab + (e_row * 2 + e_blk) * 16);
+          float4* dst = reinterpret_cast<float4*>(tab + (e_row * 2 + e_blk) * kScaledEntry);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             dst[j] = make_float4(__fmul_rn(levels[4 * j], ahat), __fmul_rn(levels[4 * j + 1], ahat),
@@ -276,7 +279,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         if (*abort_flag) continue;
         if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
         const uint8_t* cs = smem + kOffCodes + slot * kCodesStageBytes + (kl >> 1);
-        const float* tb = tab + kbl * 16;
+        const float* tb = tab + kbl * kScaledEntry;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t v[16];
@@ -284,7 +287,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           for (int jj = 0; jj < 16; ++jj) {
             const int rr = 32 * hf + 2 * jj;
             const uint32_t b0 = cs[rr * 64], b1 = cs[(rr + 1) * 64];
-            v[jj] = pack_bf16x2(tb[rr * 32 + ((b0 >> sh) & 15u)], tb[(rr + 1) * 32 + ((b1 >> sh) & 15u)]);
+            v[jj] = pack_bf16x2(tb[rr * (2 * kScaledEntry) + ((b0 >> sh) & 15u)],
+                                tb[(rr + 1) * (2 * kScaledEntry) + ((b1 >> sh) & 15u)]);
           }
           tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
         }
