@@ -179,31 +179,6 @@ gemv_fwd_kernel(const GemvArgs p) {
     cur[j][1] = (vg8 && j < nb) ? ldg_codes(cg8_ptr + j * 32) : make_uint2(0u, 0u);
   }
 
-  // Activations, pass 1: per-token max |x| of the slice (positive floats
-  // order as integers, so a shared atomicMax on the bits reduces them).
-  unsigned int* xmax = reinterpret_cast<unsigned int*>(xinv);   // reused for 2^-e below
-  if (tid < 8 * NT) xmax[tid] = 0u;
-  const int nkv4 = nb * (kBlock / 4);        // uint2 (4 bf16) per token row
-  const int nx = mt * nkv4;
-  const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K + static_cast<int64_t>(kb0) * kBlock);
-  const int64_t xrow4 = p.K / 4;
-  auto xload = [&](int i) {
-    const int tk = i / nkv4, c = i - tk * nkv4;
-    return __ldg(xbase + tk * xrow4 + c);
-  };
-  auto absmax4 = [](uint2 v) {
-    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-    return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-  };
-  constexpr int kXBatch = 8;
-  uint2 xv[kXBatch];
-#pragma unroll
-  for (int u = 0; u < kXBatch; ++u) {
-    const int i = tid + kGemvThreads * u;
-    xv[u] = (i < nx) ? xload(i) : make_uint2(0u, 0u);
-  }
-
   // Dequantized absmax of the CTA's rows over the slice: loads first.
   constexpr int kAhBatch = 4;
   {
@@ -235,62 +210,98 @@ gemv_fwd_kernel(const GemvArgs p) {
       }
     }
   }
-  __syncthreads();   // xmax zeroed
+  // Activations: warp w stages tokens w + 8u (u < NT). Per chunk of 128
+  // uint2 (8 blocks) every load of the warp is issued before any is used;
+  // per-token max |x| -> power-of-two scale into [2^14, 2^15) -> fp16. A
+  // slice of at most 8 blocks is converted straight from registers, longer
+  // slices are read a second time.
   {
-    int last_tk = -1;
-    float mx = 0.0f;
-    auto flush = [&]() {
-      if (last_tk >= 0 && mx > 0.0f) atomicMax(xmax + last_tk, __float_as_uint(mx));
+    const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
+    const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K +
+                                                        static_cast<int64_t>(kb0) * kBlock);
+    const int64_t xrow4 = p.K / 4;
+    auto absmax4 = [](uint2 v) {
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
     };
-    for (int base = 0; base < nx; base += kGemvThreads * kXBatch) {
+    auto convert = [](uint2 v, float scale) {
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
+      const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
+      return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    };
+    uint2 xv[NT][4];
+    float mx[NT];
 #pragma unroll
-      for (int u = 0; u < kXBatch; ++u) {
-        const int i = base + tid + kGemvThreads * u;
-        if (i < nx) {
-          const uint2 v = (base == 0) ? xv[u] : xload(i);
-          const int tk = i / nkv4;
-          if (tk != last_tk) {
-            flush();
-            last_tk = tk;
-            mx = 0.0f;
+    for (int u = 0; u < NT; ++u) mx[u] = 0.0f;
+    for (int c0 = 0; c0 < nkv4; c0 += 128) {
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const int tk = warp + 8 * u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int i = c0 + lane + 32 * c;
+          xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NT; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mx[u] = fmaxf(mx[u], absmax4(xv[u][c]));
+    }
+    float scale[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1)
+        mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], off));
+      int e = 0;
+      if (mx[u] > 0.0f) {
+        const int E = max(1, static_cast<int>((__float_as_uint(mx[u]) >> 23) & 0xffu));
+        e = min(141 - E, 126);
+      }
+      scale[u] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+      const int tk = warp + 8 * u;
+      if (lane == 0 && tk < 8 * NT) xinv[tk] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    }
+    if (nkv4 <= 128) {
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const int tk = warp + 8 * u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int i = lane + 32 * c;
+          if (tk < mt && i < nkv4)
+            reinterpret_cast<uint2*>(xs + tk * xstride_b)[i] = convert(xv[u][c], scale[u]);
+        }
+      }
+    } else {
+      for (int c0 = 0; c0 < nkv4; c0 += 128) {
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+          const int tk = warp + 8 * u;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = c0 + lane + 32 * c;
+            xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
           }
-          mx = fmaxf(mx, absmax4(v));
+        }
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+          const int tk = warp + 8 * u;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = c0 + lane + 32 * c;
+            if (tk < mt && i < nkv4)
+              reinterpret_cast<uint2*>(xs + tk * xstride_b)[i] = convert(xv[u][c], scale[u]);
+          }
         }
       }
     }
-    flush();
   }
-  __syncthreads();
-  // Pass 2: scale each token by 2^e (max |x| into [2^14, 2^15)) and convert.
-  if (tid < 8 * NT) {
-    const float mx = __uint_as_float(xmax[tid]);
-    int e = 0;
-    if (mx > 0.0f) {
-      const int E = max(1, static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu));
-      e = min(141 - E, 126);
-    }
-    xinv[tid] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);   // scale for now
-  }
-  __syncthreads();
-  for (int base = 0; base < nx; base += kGemvThreads * kXBatch) {
-#pragma unroll
-    for (int u = 0; u < kXBatch; ++u) {
-      const int i = base + tid + kGemvThreads * u;
-      if (i < nx) {
-        const uint2 v = (base == 0) ? xv[u] : xload(i);
-        const int tk = i / nkv4, c = i - tk * nkv4;
-        const float scale = xinv[tk];
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-        const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
-        const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
-        reinterpret_cast<uint2*>(xs + tk * xstride_b)[c] =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-      }
-    }
-  }
-  __syncthreads();
-  if (tid < 8 * NT) xinv[tid] = 1.0f / xinv[tid];   // exact: a power of two
+
   __syncthreads();
   const bool tab_ok = tc::mbar_wait(bar_a, 0);
   if (!tab_ok) report_status(p.status, kStatusTimeout);

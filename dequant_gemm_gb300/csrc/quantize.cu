@@ -18,27 +18,10 @@ namespace {
 // needs the intermediate values to stay normal: blocks whose absmax is below
 // 2^-64 (and all-zero blocks) take the plain IEEE division instead, and
 // |w| <= 1e36 keeps 1/a normal.
-struct BlockDivisor {
-  float a;      // absmax
-  float r;      // RN(1 / a) on the fast path
-  bool slow;    // a < 2^-64
-};
-
-__device__ __forceinline__ BlockDivisor make_divisor(float a) {
-  BlockDivisor d;
-  d.a = a;
-  d.slow = a < 5.421010862427522e-20f;   // 2^-64
-  d.r = d.slow ? 0.0f : __frcp_rn(a);
-  return d;
-}
-
-__device__ __forceinline__ float normalise(float w, const BlockDivisor& d) {
-  if (!d.slow) {
-    const float q0 = __fmul_rn(w, d.r);
-    const float rem = __fmaf_rn(-q0, d.a, w);
-    return __fmaf_rn(rem, d.r, q0);
-  }
-  return d.a > 0.0f ? __fdiv_rn(w, d.a) : 0.0f;   // an all-zero block maps to level 0
+__device__ __forceinline__ float markstein_div(float w, float a, float r) {
+  const float q0 = __fmul_rn(w, r);
+  const float rem = __fmaf_rn(-q0, a, w);
+  return __fmaf_rn(rem, r, q0);
 }
 
 // Nearest level of x in [-1, 1], ties to the lower index, through 33 buckets
@@ -49,12 +32,12 @@ __device__ __forceinline__ float normalise(float w, const BlockDivisor& d) {
 // threshold and an x rounded into the neighbouring bucket at an edge gets the
 // same code; the code is lo[b] + (x > thr[b]) with lo[b] the number of
 // thresholds below the bucket and thr[b] the threshold inside it (2 if none).
-struct Buckets {
-  float thr[33];
-  uint32_t lo[33];
+struct Bucket {
+  float thr;
+  uint32_t lo;
 };
 
-__device__ __forceinline__ void build_buckets(Buckets* tab) {
+__device__ __forceinline__ void build_buckets(Bucket* tab) {
   const int b = threadIdx.x;
   if (b <= 32) {
     const float lo_edge = static_cast<float>(2 * b - 33) * 0.03125f;
@@ -67,24 +50,22 @@ __device__ __forceinline__ void build_buckets(Buckets* tab) {
       lo += (t < lo_edge) ? 1u : 0u;
       if (t > lo_edge && t < hi_edge) thr = t;
     }
-    tab->thr[b] = thr;
-    tab->lo[b] = lo;
+    tab[b].thr = thr;
+    tab[b].lo = lo;
   }
 }
 
-__device__ __forceinline__ uint32_t nearest_code(float x, const Buckets* tab) {
+__device__ __forceinline__ uint32_t nearest_code(float x, const Bucket* tab) {
   const uint32_t b = __float_as_uint(__fmaf_rn(x, 16.0f, 12582928.0f)) & 63u;
-  return tab->lo[b] + ((x > tab->thr[b]) ? 1u : 0u);
+  const Bucket e = tab[b];
+  return e.lo + ((x > e.thr) ? 1u : 0u);
 }
 
-// Codes of the four weights of a float4 packed as two bytes (little-endian
-// u16): element 4j in the high nibble of the first byte.
-__device__ __forceinline__ uint32_t quantize4(float4 v, const BlockDivisor& d, const Buckets* tab) {
-  const uint32_t q0 = nearest_code(normalise(v.x, d), tab);
-  const uint32_t q1 = nearest_code(normalise(v.y, d), tab);
-  const uint32_t q2 = nearest_code(normalise(v.z, d), tab);
-  const uint32_t q3 = nearest_code(normalise(v.w, d), tab);
-  return (q0 << 4) | q1 | (q2 << 12) | (q3 << 8);
+// Two bytes of codes for four consecutive weights (little-endian u16):
+// element 4j in the high nibble of the first byte.
+__device__ __forceinline__ uint32_t pack4(const float (&x)[4], const Bucket* tab) {
+  return (nearest_code(x[0], tab) << 4) | nearest_code(x[1], tab) |
+         (nearest_code(x[2], tab) << 12) | (nearest_code(x[3], tab) << 8);
 }
 
 __device__ __forceinline__ float abs_max4(float4 v) {
@@ -92,45 +73,65 @@ __device__ __forceinline__ float abs_max4(float4 v) {
 }
 
 constexpr int kQThreads = 256;   // one thread per block of the group
-constexpr int kQLoads = 16;      // float4 loads per lane: 32 blocks per warp
 
 // One CTA per double-quant group of 256 blocks (16384 weights). Warp w owns
-// blocks [32w, 32w + 32) of the group. Load i of a lane covers float4 number
-// 32 i + lane of the warp's span: lanes 0-15 hold block 2i, lanes 16-31 block
-// 2i + 1, so the block absmax is a 16-lane shuffle reduction. All 16 loads of
-// a lane are issued before any is used (64 KB in flight per CTA).
+// blocks [32w, 32w + 32) of the group, 4 blocks per step: 8 lanes per block,
+// each holding float4 number `sub` and `sub + 8` of it (128 contiguous bytes
+// per block per load), so a lane's 8 weights share one absmax (3 shuffle
+// steps) and one reciprocal. All 16 loads of a lane are issued before any is
+// used (64 KB in flight per CTA).
 __global__ void __launch_bounds__(kQThreads)
 quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restrict__ codes,
                 uint8_t* __restrict__ a8_out, float* __restrict__ s2_out) {
   __shared__ float s_absmax[kGroup];
   __shared__ float s_warp_max[kQThreads / 32];
-  __shared__ Buckets s_buckets;
-  build_buckets(&s_buckets);
+  __shared__ Bucket s_buckets[33];
+  build_buckets(s_buckets);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane & 7;
   const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kGroup;
   const int nblk = static_cast<int>(min(static_cast<int64_t>(kGroup), n_blocks - blk0));
-  const int wblk0 = warp * 32;  // first block of this warp within the group
 
-  const float4* src = reinterpret_cast<const float4*>(W) + blk0 * (kBlock / 4) + wblk0 * 16;
-  float4 v[kQLoads];
+  const float4* src = reinterpret_cast<const float4*>(W) + blk0 * (kBlock / 4);
+  float4 v[8][2];
 #pragma unroll
-  for (int i = 0; i < kQLoads; ++i) {
-    const int b = wblk0 + 2 * i + (lane >> 4);
-    v[i] = (b < nblk) ? __ldcs(src + 32 * i + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < 8; ++j) {
+    const int b = warp * 32 + 4 * j + (lane >> 3);
+    const bool ok = b < nblk;
+    v[j][0] = ok ? __ldcs(src + b * 16 + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[j][1] = ok ? __ldcs(src + b * 16 + sub + 8) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-
   __syncthreads();   // bucket table ready
-  uint16_t* dst = reinterpret_cast<uint16_t*>(codes) + blk0 * (kBlock / 4) + wblk0 * 16;
+
+  uint16_t* dst = reinterpret_cast<uint16_t*>(codes + blk0 * (kBlock / 2));
 #pragma unroll
-  for (int i = 0; i < kQLoads; ++i) {
-    float a = abs_max4(v[i]);
+  for (int j = 0; j < 8; ++j) {
+    float a = fmaxf(abs_max4(v[j][0]), abs_max4(v[j][1]));
 #pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    const int b = wblk0 + 2 * i + (lane >> 4);
+    for (int off = 4; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    const int b = warp * 32 + 4 * j + (lane >> 3);
+    float x[2][4];
+    const float w[2][4] = {{v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w},
+                           {v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w}};
+    if (a >= 5.421010862427522e-20f) {   // 2^-64: fast exact quotient
+      const float r = __frcp_rn(a);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[h][e] = markstein_div(w[h][e], a, r);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[h][e] = (a > 0.0f) ? __fdiv_rn(w[h][e], a) : 0.0f;
+    }
     if (b < nblk) {
-      dst[32 * i + lane] = static_cast<uint16_t>(quantize4(v[i], make_divisor(a), &s_buckets));
-      if ((lane & 15) == 0) s_absmax[b] = a;
+      // block b's 32 code bytes: float4 `sub` -> bytes 2 sub, 2 sub + 1;
+      // float4 `sub + 8` -> bytes 16 + 2 sub, 17 + 2 sub
+      dst[b * 16 + sub] = static_cast<uint16_t>(pack4(x[0], s_buckets));
+      dst[b * 16 + 8 + sub] = static_cast<uint16_t>(pack4(x[1], s_buckets));
+      if (sub == 0) s_absmax[b] = a;
     }
   }
   __syncthreads();
