@@ -53,7 +53,7 @@ nf4_status current_device(DeviceInfo** out) {
 
 // Token counts up to these use the streaming small-M kernels; larger ones the
 // tensor-memory GEMM.
-constexpr int64_t kSmallMFwd = 64;
+constexpr int64_t kSmallMFwd = 16;
 constexpr int64_t kSmallMDx = 16;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -1,4 +1,4 @@
-// Small-M fused NF4-dequant matmul: Y = X * dequant(W)^T for M <= 64 tokens
+// Small-M fused NF4-dequant matmul: Y = X * dequant(W)^T for M <= 16 tokens
 // (decode shapes), and a plain fp32 input-gradient kernel for small M
 // ("Zenbit", zenbit.pallas_nf4 bullet: the compressed weight is streamed and
 // dequantized on chip; the full-precision weight never reaches HBM).
@@ -9,7 +9,7 @@
 //    partial sums through distributed shared memory, so every output is
 //    written once with a plain store (no zeroing pass, no atomics).
 //  * The weight is the A operand of mma.sync.m16n8k16 (16 rows per warp), the
-//    tokens are the N operand (8 per n-tile, up to 8 n-tiles): the "swap AB"
+//    tokens are the N operand (8 per n-tile, one or two n-tiles): the "swap AB"
 //    shape for skinny products. Each weight is dequantized once per CTA for
 //    all of its tokens. Every global load of the prologue (codes, absmax
 //    codes, scales, activations) is issued before any of them is used.
@@ -75,20 +75,33 @@ constexpr PairTable make_pair_table() {
 
 __device__ __align__(128) const PairTable kPairTable = make_pair_table();
 
+// Not volatile: independent MMA chains of different blocks may interleave.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The codes are read-only for the kernel's lifetime: a plain (non-volatile)
+// non-coherent load the compiler may schedule freely.
 __device__ __forceinline__ uint2 ldg_codes(const uint8_t* p) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
 
@@ -312,7 +325,8 @@ gemv_fwd_kernel(const GemvArgs p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
-  const uint8_t* tab_b = reinterpret_cast<const uint8_t*>(tab) + lane * 4;
+  const uint32_t tab_b = tc::smem_addr(tab) + lane * 4;   // this lane's copy of the table
+  const uint32_t xs_a = tc::smem_addr(xs) + g * xstride_b + t * 32;
   const float* ah_g = ahat_s + (warp * 16 + g) * p.max_nb;
   const float* ah_g8 = ah_g + 8 * p.max_nb;
   // B fragments of padding tokens are zero instead of being read
@@ -336,16 +350,14 @@ gemv_fwd_kernel(const GemvArgs p) {
           const uint32_t wg8 = (s < 2) ? cur[jj][1].x : cur[jj][1].y;
           const int sh = 16 * (s & 1);
           // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
-          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg >> sh) & 0xffu) << 7));
-          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg >> (sh + 8)) & 0xffu) << 7));
-          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg8 >> sh) & 0xffu) << 7));
-          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
+          const uint32_t a0 = lds32(tab_b + (((wg >> sh) & 0xffu) << 7));
+          const uint32_t a2 = lds32(tab_b + (((wg >> (sh + 8)) & 0xffu) << 7));
+          const uint32_t a1 = lds32(tab_b + (((wg8 >> sh) & 0xffu) << 7));
+          const uint32_t a3 = lds32(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             uint2 b = make_uint2(0u, 0u);
-            if (tok_ok[nt])
-              b = *reinterpret_cast<const uint2*>(xs + (nt * 8 + g) * xstride_b +
-                                                  (j * 64 + t * 16 + 4 * s) * 2);
+            if (tok_ok[nt]) b = lds64(xs_a + nt * 8 * xstride_b + j * 128 + 8 * s);
             mma_f16(part[nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -532,7 +544,7 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   a.max_nb = (a.nblk + slices - 1) / slices;
   // n-tiles of 8 tokens per CTA: all tokens at once when the activation slice
   // fits, otherwise fewer tokens per CTA and more CTAs along z.
-  int nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
+  int nt = M <= 8 ? 1 : 2;
   while (nt > 1 && gemv_smem_bytes(nt, a.max_nb) > kGemvSmemLimit) nt /= 2;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
   const size_t smem = gemv_smem_bytes(nt, a.max_nb);
@@ -541,8 +553,6 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
     const int lim = static_cast<int>(kGemvSmemLimit);
     cudaFuncSetAttribute(gemv_fwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
     cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    cudaFuncSetAttribute(gemv_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    cudaFuncSetAttribute(gemv_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(slices),
@@ -557,12 +567,7 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  switch (nt) {
-    case 1: return launch_gemv_nt<1>(cfg, a);
-    case 2: return launch_gemv_nt<2>(cfg, a);
-    case 4: return launch_gemv_nt<4>(cfg, a);
-    default: return launch_gemv_nt<8>(cfg, a);
-  }
+  return nt == 1 ? launch_gemv_nt<1>(cfg, a) : launch_gemv_nt<2>(cfg, a);
 }
 
 cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,

@@ -63,7 +63,7 @@ constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
 constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
 constexpr int kOffLevels = kOffLut + kLutBytes;
 constexpr int kOffBars = kOffLevels + 64;
-constexpr int kNumBars = 3 * kStages + 1;
+constexpr int kNumBars = 3 * kStages + 2;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 
@@ -79,6 +79,35 @@ struct TcArgs {
   int atomic_out;
   int* status;
 };
+
+// Forward pair table: entry b (a code byte), copy l at float2 index 32 b + l
+// holds (c[b >> 4], c[b & 15]); a compile-time constant brought into shared
+// memory by one bulk copy per CTA.
+struct PairLevels {
+  uint32_t w[256 * 32 * 2];
+};
+
+constexpr PairLevels make_pair_levels() {
+  PairLevels t{};
+  for (int i = 0; i < 256 * 32; ++i) {
+    const int b = i >> 5;
+    t.w[2 * i] = kLevelBits[b >> 4];
+    t.w[2 * i + 1] = kLevelBits[b & 15];
+  }
+  return t;
+}
+
+__device__ __align__(128) const PairLevels kPairLevels = make_pair_levels();
+static_assert(sizeof(PairLevels) == kPairLutBytes, "pair table size");
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -98,6 +127,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   auto dq_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto empty_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
   const uint32_t accum_bar = bars + 8u * (3 * kStages);
+  const uint32_t lut_bar = bars + 8u * (3 * kStages + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -108,13 +138,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   const int nst = min(p.stages_per_split, p.stages_total - s_begin);
 
   if (threadIdx.x < 16) levels[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
-  if (!kDx && warp >= 2) {
-    // pair table: entry b, copy l at float2 index 32 b + l
-    float2* pair = reinterpret_cast<float2*>(smem + kOffLut);
-    for (int b = warp - 2; b < 256; b += 8)
-      pair[32 * b + lane] = make_float2(__uint_as_float(kLevelBitsDev[b >> 4]),
-                                        __uint_as_float(kLevelBitsDev[b & 15]));
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
@@ -122,8 +145,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
+    tc::mbar_init(lut_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
+    if (!kDx) {
+      tc::mbar_arrive_expect_tx(lut_bar, kPairLutBytes);
+      bulk_copy_g2s(tc::smem_addr(smem + kOffLut), &kPairLevels, kPairLutBytes, lut_bar);
+    }
   }
   if (warp == 0 && lane == 0) {
     tc::prefetch_tensormap(&tm_act);
@@ -210,6 +238,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
       };
       load_scale(grp);
+      if (!tc::mbar_wait(lut_bar, 0)) fail();
       for (int i = grp; i < nst; i += 2) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
