@@ -125,11 +125,14 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Read a float of CTA `rank`'s shared memory at this CTA's address of `local`.
+// Volatile (kept between the cluster barriers) but without a memory clobber,
+// so several of these are issued back to back before their results are used.
 __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
   uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(local)), "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(local)), "r"(rank));
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
   return v;
 }
 
@@ -146,8 +149,9 @@ struct GemvArgs {
   int* status;
 };
 
+// First absmax block of K-slice s (nblk * slices stays far below 2^31).
 __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
-  return static_cast<int>((static_cast<int64_t>(nblk) * s) / slices);
+  return (nblk * s) / slices;
 }
 
 template <int NT>
@@ -192,37 +196,33 @@ gemv_fwd_kernel(const GemvArgs p) {
     cur[j][1] = (vg8 && j < nb) ? ldg_codes(cg8_ptr + j * 32) : make_uint2(0u, 0u);
   }
 
-  // Dequantized absmax of the CTA's rows over the slice: loads first.
-  constexpr int kAhBatch = 4;
+  // Dequantized absmax of the CTA's rows over the slice: thread t owns row
+  // t / 2 and every other block of it; all loads of a batch come first.
   {
-    uint32_t av[kAhBatch];
-    float sv[kAhBatch];
-    for (int base = tid; base < kGemvRows * nb; base += kGemvThreads * kAhBatch) {
+    const int r = tid >> 1, par = tid & 1;
+    const int64_t n = row0 + r;
+    const bool vrow = n < p.N;
+    const int64_t bi0 = n * p.nblk + kb0;
+    float* arow = ahat_s + r * p.max_nb;
+    constexpr int kAh = 4;
+    for (int j0 = par; j0 < nb; j0 += 2 * kAh) {
+      uint32_t av[kAh];
+      float sv[kAh];
 #pragma unroll
-      for (int u = 0; u < kAhBatch; ++u) {
-        const int i = base + kGemvThreads * u;
-        av[u] = 0u;
-        sv[u] = 0.0f;
-        if (i < kGemvRows * nb) {
-          const int r = i / nb, j = i - r * nb;
-          const int64_t n = row0 + r;
-          if (n < p.N) {
-            const int64_t bi = n * p.nblk + kb0 + j;
-            av[u] = __ldg(p.a8 + bi);
-            sv[u] = __ldg(p.s2 + bi / kGroup);
-          }
-        }
+      for (int u = 0; u < kAh; ++u) {
+        const int j = j0 + 2 * u;
+        const bool ok = vrow && j < nb;
+        av[u] = ok ? static_cast<uint32_t>(__ldg(p.a8 + bi0 + j)) : 0u;
+        sv[u] = ok ? __ldg(p.s2 + ((bi0 + j) >> 8)) : 0.0f;
       }
 #pragma unroll
-      for (int u = 0; u < kAhBatch; ++u) {
-        const int i = base + kGemvThreads * u;
-        if (i < kGemvRows * nb) {
-          const int r = i / nb, j = i - r * nb;
-          ahat_s[r * p.max_nb + j] = dequant_absmax(av[u], sv[u]);
-        }
+      for (int u = 0; u < kAh; ++u) {
+        const int j = j0 + 2 * u;
+        if (j < nb) arow[j] = dequant_absmax(av[u], sv[u]);
       }
     }
   }
+
   // Activations: warp w stages tokens w + 8u (u < NT). Per chunk of 128
   // uint2 (8 blocks) every load of the warp is issued before any is used;
   // per-token max |x| -> power-of-two scale into [2^14, 2^15) -> fp16. A
@@ -415,12 +415,19 @@ gemv_fwd_kernel(const GemvArgs p) {
     // slice's partial through distributed shared memory and stores them.
     cluster_sync();
     const uint32_t rank = cluster_ctarank();
-    const int rpc = kGemvRows / p.slices;
+    const int rpc = kGemvRows / p.slices;          // rows reduced by this CTA
+    const int rpc_shift = 31 - __clz(rpc);         // rpc is a power of two
     for (int i = tid; i < 8 * NT * rpc; i += kGemvThreads) {
-      const int tk = i / rpc, r = static_cast<int>(rank) * rpc + (i % rpc);
+      const int tk = i >> rpc_shift, r = static_cast<int>(rank) * rpc + (i & (rpc - 1));
       if (tk < mt && row0 + r < p.N) {
+        const float* src = out_s + tk * kOutStride + r;
+        float part[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)   // all remote loads in flight at once
+          part[c] = (c < p.slices) ? ld_dsmem(src, c) : 0.0f;
         float v = 0.0f;
-        for (int c = 0; c < p.slices; ++c) v += ld_dsmem(out_s + tk * kOutStride + r, c);
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) v += part[c];
         p.Y[(m0 + tk) * p.N + row0 + r] = v;
       }
     }
