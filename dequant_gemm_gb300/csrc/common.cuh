@@ -1,6 +1,7 @@
 // Shared definitions of the NF4 CUDA library (device side and host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -69,6 +70,12 @@ __device__ __forceinline__ float dequant_absmax(uint32_t a8, float s2) {
 
 // Kernel launchers (each returns cudaGetLastError() of its launch).
 namespace nf4 {
+// Encodes a 2-D row-major tensor map [outer, inner] with the given row pitch
+// (bytes), box and swizzle; zero fill out of bounds. False on failure.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle);
+
 cudaError_t launch_quantize(const float* W, int64_t n_elems, uint8_t* codes, uint8_t* a8,
                             float* s2, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const float* s2,

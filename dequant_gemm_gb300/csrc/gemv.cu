@@ -8,11 +8,15 @@
 //    K-slices of the same rows form a thread-block cluster and reduce their
 //    partial sums through distributed shared memory, so every output is
 //    written once with a plain store (no zeroing pass, no atomics).
+//  * A producer warp streams the CTA's packed codes with 2-D TMA boxes of
+//    128 rows x 128 bytes (four absmax blocks), 128-byte swizzled, through a
+//    ring of four shared-memory slots; the eight compute warps read them
+//    bank-conflict free. The absmax codes, scales and activations of the
+//    prologue are loaded with all requests issued before any is used.
 //  * The weight is the A operand of mma.sync.m16n8k16 (16 rows per warp), the
 //    tokens are the N operand (8 per n-tile, one or two n-tiles): the "swap AB"
 //    shape for skinny products. Each weight is dequantized once per CTA for
-//    all of its tokens. Every global load of the prologue (codes, absmax
-//    codes, scales, activations) is issued before any of them is used.
+//    all of its tokens.
 //  * Dequantization is factored as  sum_b ahat_b * (sum_{k in b} x_k c[q_k]):
 //    the MMA consumes the raw levels c[q] and each 64-weight block's partial
 //    sum is scaled by its dequantized absmax in fp32 afterwards. The levels
@@ -37,12 +41,10 @@
 namespace nf4 {
 namespace {
 
-constexpr int kGemvThreads = 256;
 constexpr int kGemvRows = 128;
 constexpr int kTabBytes = 256 * 32 * 4;
 constexpr int kMaxSliceBlocks = 48;
 constexpr int kMaxCluster = 8;
-constexpr int kRegBlocks = 8;                 // code blocks held in registers at a time
 constexpr int kOutStride = kGemvRows + 4;     // floats, keeps rows 16-byte aligned
 
 // fp32 -> fp16 round-to-nearest-even for the NF4 levels (all normal in fp16
@@ -83,14 +85,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// The codes are read-only for the kernel's lifetime: a plain (non-volatile)
-// non-coherent load the compiler may schedule freely.
-__device__ __forceinline__ uint2 ldg_codes(const uint8_t* p) {
-  uint2 v;
-  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -138,7 +132,6 @@ __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
 
 struct GemvArgs {
   const uint16_t* X;     // bf16 [M, K]
-  const uint8_t* codes;  // [N*K/2]
   const uint8_t* a8;     // [N*K/64]
   const float* s2;       // [groups]
   float* Y;              // fp32 [M, N]
@@ -146,6 +139,7 @@ struct GemvArgs {
   int nblk;              // K / 64
   int slices;            // K-slices = cluster size along y
   int max_nb;            // largest slice, in blocks
+  int ring;              // code-box slots (1..kMaxRing)
   int* status;
 };
 
@@ -154,16 +148,43 @@ __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
   return (nblk * s) / slices;
 }
 
+constexpr int kComputeWarps = 8;
+constexpr int kGemvThreads = 32 * (kComputeWarps + 1);   // + one TMA producer warp
+constexpr int kMaxRing = 4;                 // code boxes in flight, at most
+constexpr int kBoxBlocks = 4;               // absmax blocks per box (128 B of codes per row)
+constexpr int kBoxBytes = kGemvRows * 128;  // 16 KB: 128 rows x 128 B
+
+// Shared memory (offsets from a 1024-byte aligned base): level table, code
+// ring, absmax table, token scales, mbarriers, fp16 activation slice.
+constexpr int kOffRing = kTabBytes;
+__host__ __device__ constexpr int gemv_off_ahat(int ring) { return kOffRing + ring * kBoxBytes; }
+__host__ __device__ constexpr int gemv_off_xinv(int ring, int max_nb) {
+  return gemv_off_ahat(ring) + kGemvRows * max_nb * 4;
+}
+__host__ __device__ constexpr int gemv_off_bars(int ring, int max_nb) {
+  return gemv_off_xinv(ring, max_nb) + 64 * 4;
+}
+__host__ __device__ constexpr int gemv_off_xs(int ring, int max_nb) {
+  return gemv_off_bars(ring, max_nb) + (1 + 2 * kMaxRing) * 8 + 8;
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kGemvThreads)
-gemv_fwd_kernel(const GemvArgs p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
-  float* ahat_s = reinterpret_cast<float*>(smem + kTabBytes);     // [128][max_nb]
-  float* xinv = ahat_s + kGemvRows * p.max_nb;                     // [64]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(xinv + 64);
+  float* ahat_s = reinterpret_cast<float*>(smem + gemv_off_ahat(p.ring));   // [128][max_nb]
+  float* xinv = reinterpret_cast<float*>(smem + gemv_off_xinv(p.ring, p.max_nb));  // [64]
+  const uint32_t bars = tc::smem_addr(smem + gemv_off_bars(p.ring, p.max_nb));
+  const uint32_t tab_bar = bars;
+  auto full_bar = [&](int s) { return bars + 8u * (1 + s); };
+  auto empty_bar = [&](int s) { return bars + 8u * (1 + kMaxRing + s); };
   const int xstride_b = p.max_nb * 128 + 8;  // bytes per token row of the fp16 slice
-  uint8_t* xs = reinterpret_cast<uint8_t*>(bar + 2);
+  uint8_t* xs = smem + gemv_off_xs(p.ring, p.max_nb);
+  const int nring = p.ring;
+  const uint32_t ring = tc::smem_addr(smem + kOffRing);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -171,126 +192,98 @@ gemv_fwd_kernel(const GemvArgs p) {
   const int slice = blockIdx.y;
   const int kb0 = slice_begin(p.nblk, p.slices, slice);
   const int nb = slice_begin(p.nblk, p.slices, slice + 1) - kb0;
+  const int nboxes = (nb + kBoxBlocks - 1) / kBoxBlocks;
   const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
   const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
-  const int64_t rowg = row0 + warp * 16 + g, rowg8 = rowg + 8;
-  const int64_t rowbytes = p.K / 2;
-  const uint32_t bar_a = tc::smem_addr(bar);
 
-  // Level table: one bulk copy, waited on before the main loop.
   if (tid == 0) {
-    tc::mbar_init(bar_a, 1);
+    tc::mbar_init(tab_bar, 1);
+    for (int s = 0; s < kMaxRing; ++s) {
+      tc::mbar_init(full_bar(s), 1);
+      tc::mbar_init(empty_bar(s), kComputeWarps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    tc::mbar_arrive_expect_tx(bar_a, kTabBytes);
-    bulk_copy_g2s(tc::smem_addr(tab), &kPairTable, kTabBytes, bar_a);
   }
+  __syncthreads();
 
-  // Codes of this thread: rows g and g+8 of the warp, 8 bytes per block.
-  const uint8_t* cg_ptr = p.codes + rowg * rowbytes + static_cast<int64_t>(kb0) * 32 + t * 8;
-  const uint8_t* cg8_ptr = cg_ptr + 8 * rowbytes;
-  const bool vg = rowg < p.N, vg8 = rowg8 < p.N;
-  uint2 cur[kRegBlocks][2];
-#pragma unroll
-  for (int j = 0; j < kRegBlocks; ++j) {
-    cur[j][0] = (vg && j < nb) ? ldg_codes(cg_ptr + j * 32) : make_uint2(0u, 0u);
-    cur[j][1] = (vg8 && j < nb) ? ldg_codes(cg8_ptr + j * 32) : make_uint2(0u, 0u);
-  }
-
-  // Dequantized absmax of the CTA's rows over the slice: thread t owns row
-  // t / 2 and every other block of it; all loads of a batch come first.
-  {
-    const int r = tid >> 1, par = tid & 1;
-    const int64_t n = row0 + r;
-    const bool vrow = n < p.N;
-    const int64_t bi0 = n * p.nblk + kb0;
-    float* arow = ahat_s + r * p.max_nb;
-    constexpr int kAh = 4;
-    for (int j0 = par; j0 < nb; j0 += 2 * kAh) {
-      uint32_t av[kAh];
-      float sv[kAh];
-#pragma unroll
-      for (int u = 0; u < kAh; ++u) {
-        const int j = j0 + 2 * u;
-        const bool ok = vrow && j < nb;
-        av[u] = ok ? static_cast<uint32_t>(__ldg(p.a8 + bi0 + j)) : 0u;
-        sv[u] = ok ? __ldg(p.s2 + ((bi0 + j) >> 8)) : 0.0f;
+  bool ok = true;
+  if (warp == kComputeWarps) {
+    // ------------------------------------------------------------ producer --
+    // Level table, then the slice's code boxes (128 rows x 4 blocks each,
+    // 128-byte swizzled) through a ring of `nring` slots.
+    if (lane == 0) {
+      tc::prefetch_tensormap(&tm_codes);
+      tc::mbar_arrive_expect_tx(tab_bar, kTabBytes);
+      bulk_copy_g2s(tc::smem_addr(tab), &kPairTable, kTabBytes, tab_bar);
+      int issued = 0;
+      for (int b = 0; b < nboxes; ++b) {
+        const int slot = b % nring;
+        if (b >= nring && !tc::mbar_wait(empty_bar(slot), ((b / nring) - 1) & 1)) {
+          report_status(p.status, kStatusTimeout);
+          break;
+        }
+        tc::mbar_arrive_expect_tx(full_bar(slot), kBoxBytes);
+        tc::tma_load_2d(ring + slot * kBoxBytes, &tm_codes, (kb0 + kBoxBlocks * b) * 32,
+                        static_cast<int32_t>(row0), full_bar(slot));
+        ++issued;
       }
-#pragma unroll
-      for (int u = 0; u < kAh; ++u) {
-        const int j = j0 + 2 * u;
-        if (j < nb) arow[j] = dequant_absmax(av[u], sv[u]);
-      }
+      // copies still in flight land before the CTA may exit
+      for (int b = max(0, issued - nring); b < issued; ++b)
+        tc::mbar_wait(full_bar(b % nring), (b / nring) & 1);
     }
-  }
-
-  // Activations: warp w stages tokens w + 8u (u < NT). Per chunk of 128
-  // uint2 (8 blocks) every load of the warp is issued before any is used;
-  // per-token max |x| -> power-of-two scale into [2^14, 2^15) -> fp16. A
-  // slice of at most 8 blocks is converted straight from registers, longer
-  // slices are read a second time.
-  {
-    const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
-    const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K +
-                                                        static_cast<int64_t>(kb0) * kBlock);
-    const int64_t xrow4 = p.K / 4;
-    auto absmax4 = [](uint2 v) {
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-      return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-    };
-    auto convert = [](uint2 v, float scale) {
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-      const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
-      const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
-      return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-    };
-    uint2 xv[NT][4];
-    float mx[NT];
+  } else {
+    // Dequantized absmax of the CTA's rows over the slice: thread t owns row
+    // t / 2 and every other block of it; all loads of a batch come first.
+    {
+      const int r = tid >> 1, par = tid & 1;
+      const int64_t n = row0 + r;
+      const bool vrow = n < p.N;
+      const int64_t bi0 = n * p.nblk + kb0;
+      float* arow = ahat_s + r * p.max_nb;
+      constexpr int kAh = 4;
+      for (int j0 = par; j0 < nb; j0 += 2 * kAh) {
+        uint32_t av[kAh];
+        float sv[kAh];
 #pragma unroll
-    for (int u = 0; u < NT; ++u) mx[u] = 0.0f;
-    for (int c0 = 0; c0 < nkv4; c0 += 128) {
+        for (int u = 0; u < kAh; ++u) {
+          const int j = j0 + 2 * u;
+          const bool okj = vrow && j < nb;
+          av[u] = okj ? static_cast<uint32_t>(__ldg(p.a8 + bi0 + j)) : 0u;
+          sv[u] = okj ? __ldg(p.s2 + ((bi0 + j) >> 8)) : 0.0f;
+        }
 #pragma unroll
-      for (int u = 0; u < NT; ++u) {
-        const int tk = warp + 8 * u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int i = c0 + lane + 32 * c;
-          xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
+        for (int u = 0; u < kAh; ++u) {
+          const int j = j0 + 2 * u;
+          if (j < nb) arow[j] = dequant_absmax(av[u], sv[u]);
         }
       }
-#pragma unroll
-      for (int u = 0; u < NT; ++u)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) mx[u] = fmaxf(mx[u], absmax4(xv[u][c]));
     }
-    float scale[NT];
+    // Activations: warp w stages tokens w + 8u (u < NT). Per chunk of 128
+    // uint2 (8 blocks) every load of the warp is issued before any is used;
+    // per-token max |x| -> power-of-two scale into [2^14, 2^15) -> fp16. A
+    // slice of at most 8 blocks is converted straight from registers, longer
+    // slices are read a second time.
+    {
+      const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
+      const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K +
+                                                          static_cast<int64_t>(kb0) * kBlock);
+      const int64_t xrow4 = p.K / 4;
+      auto absmax4 = [](uint2 v) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+      };
+      auto convert = [](uint2 v, float scale) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
+        const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
+        return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+      };
+      uint2 xv[NT][4];
+      float mx[NT];
 #pragma unroll
-    for (int u = 0; u < NT; ++u) {
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1)
-        mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], off));
-      int e = 0;
-      if (mx[u] > 0.0f) {
-        const int E = max(1, static_cast<int>((__float_as_uint(mx[u]) >> 23) & 0xffu));
-        e = min(141 - E, 126);
-      }
-      scale[u] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-      const int tk = warp + 8 * u;
-      if (lane == 0 && tk < 8 * NT) xinv[tk] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    }
-    if (nkv4 <= 128) {
-#pragma unroll
-      for (int u = 0; u < NT; ++u) {
-        const int tk = warp + 8 * u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int i = lane + 32 * c;
-          if (tk < mt && i < nkv4)
-            reinterpret_cast<uint2*>(xs + tk * xstride_b)[i] = convert(xv[u][c], scale[u]);
-        }
-      }
-    } else {
+      for (int u = 0; u < NT; ++u) mx[u] = 0.0f;
       for (int c0 = 0; c0 < nkv4; c0 += 128) {
 #pragma unroll
         for (int u = 0; u < NT; ++u) {
@@ -299,6 +292,37 @@ gemv_fwd_kernel(const GemvArgs p) {
           for (int c = 0; c < 4; ++c) {
             const int i = c0 + lane + 32 * c;
             xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mx[u] = fmaxf(mx[u], absmax4(xv[u][c]));
+      }
+      float scale[NT];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], off));
+        int e = 0;
+        if (mx[u] > 0.0f) {
+          const int E = max(1, static_cast<int>((__float_as_uint(mx[u]) >> 23) & 0xffu));
+          e = min(141 - E, 126);
+        }
+        scale[u] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        if (lane == 0) xinv[warp + 8 * u] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      }
+      for (int c0 = 0; c0 < nkv4; c0 += 128) {
+        if (c0 > 0 || nkv4 > 128) {
+#pragma unroll
+          for (int u = 0; u < NT; ++u) {
+            const int tk = warp + 8 * u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int i = c0 + lane + 32 * c;
+              xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
+            }
           }
         }
 #pragma unroll
@@ -314,10 +338,7 @@ gemv_fwd_kernel(const GemvArgs p) {
       }
     }
   }
-
   __syncthreads();
-  const bool tab_ok = tc::mbar_wait(bar_a, 0);
-  if (!tab_ok) report_status(p.status, kStatusTimeout);
 
   float acc[NT][4];
 #pragma unroll
@@ -325,64 +346,73 @@ gemv_fwd_kernel(const GemvArgs p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
-  const uint32_t tab_b = tc::smem_addr(tab) + lane * 4;   // this lane's copy of the table
-  const uint32_t xs_a = tc::smem_addr(xs) + g * xstride_b + t * 32;
-  const float* ah_g = ahat_s + (warp * 16 + g) * p.max_nb;
-  const float* ah_g8 = ah_g + 8 * p.max_nb;
-  // B fragments of padding tokens are zero instead of being read
-  bool tok_ok[NT];
+  if (warp < kComputeWarps) {
+    ok = tc::mbar_wait(tab_bar, 0);
+    const uint32_t tab_b = tc::smem_addr(tab) + lane * 4;   // this lane's copy of the table
+    const uint32_t xs_a = tc::smem_addr(xs) + g * xstride_b + t * 32;
+    const float* ah_g = ahat_s + (warp * 16 + g) * p.max_nb;
+    const float* ah_g8 = ah_g + 8 * p.max_nb;
+    // swizzled offsets of this lane's 8 code bytes in rows g and g + 8 of the
+    // warp: 16-byte chunk c of a box row r sits at chunk c ^ (r & 7)
+    const uint32_t row_a = ring + (warp * 16 + g) * 128 + (t & 1) * 8;
+    const uint32_t row_b = row_a + 8 * 128;
+    bool tok_ok[NT];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < mt;
+    for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < mt;
 
-  for (int j0 = 0; j0 < nb && tab_ok; j0 += kRegBlocks) {
+    for (int b = 0; b < nboxes && ok; ++b) {
+      const int slot = b % nring;
+      if (!tc::mbar_wait(full_bar(slot), (b / nring) & 1)) {
+        ok = false;
+        break;
+      }
 #pragma unroll
-    for (int jj = 0; jj < kRegBlocks; ++jj) {
-      const int j = j0 + jj;
-      if (j < nb) {
-        float part[NT][4];
+      for (int jj = 0; jj < kBoxBlocks; ++jj) {
+        const int j = b * kBoxBlocks + jj;
+        if (j < nb) {
+          const uint32_t chunk = static_cast<uint32_t>((2 * jj + (t >> 1)) ^ g) << 4;
+          const uint2 cg = lds64(row_a + slot * kBoxBytes + chunk);
+          const uint2 cg8 = lds64(row_b + slot * kBoxBytes + chunk);
+          float part[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) part[nt][i] = 0.0f;
+            for (int i = 0; i < 4; ++i) part[nt][i] = 0.0f;
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint32_t wg = (s < 2) ? cur[jj][0].x : cur[jj][0].y;
-          const uint32_t wg8 = (s < 2) ? cur[jj][1].x : cur[jj][1].y;
-          const int sh = 16 * (s & 1);
-          // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
-          const uint32_t a0 = lds32(tab_b + (((wg >> sh) & 0xffu) << 7));
-          const uint32_t a2 = lds32(tab_b + (((wg >> (sh + 8)) & 0xffu) << 7));
-          const uint32_t a1 = lds32(tab_b + (((wg8 >> sh) & 0xffu) << 7));
-          const uint32_t a3 = lds32(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
+          for (int s = 0; s < 4; ++s) {
+            const uint32_t wg = (s < 2) ? cg.x : cg.y;
+            const uint32_t wg8 = (s < 2) ? cg8.x : cg8.y;
+            const int sh = 16 * (s & 1);
+            // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
+            const uint32_t a0 = lds32(tab_b + (((wg >> sh) & 0xffu) << 7));
+            const uint32_t a2 = lds32(tab_b + (((wg >> (sh + 8)) & 0xffu) << 7));
+            const uint32_t a1 = lds32(tab_b + (((wg8 >> sh) & 0xffu) << 7));
+            const uint32_t a3 = lds32(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              uint2 bx = make_uint2(0u, 0u);
+              if (tok_ok[nt]) bx = lds64(xs_a + nt * 8 * xstride_b + j * 128 + 8 * s);
+              mma_f16(part[nt], a0, a1, a2, a3, bx.x, bx.y);
+            }
+          }
+          const float ag = ah_g[j], ag8 = ah_g8[j];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            uint2 b = make_uint2(0u, 0u);
-            if (tok_ok[nt]) b = lds64(xs_a + nt * 8 * xstride_b + j * 128 + 8 * s);
-            mma_f16(part[nt], a0, a1, a2, a3, b.x, b.y);
+            acc[nt][0] = fmaf(ag, part[nt][0], acc[nt][0]);
+            acc[nt][1] = fmaf(ag, part[nt][1], acc[nt][1]);
+            acc[nt][2] = fmaf(ag8, part[nt][2], acc[nt][2]);
+            acc[nt][3] = fmaf(ag8, part[nt][3], acc[nt][3]);
           }
         }
-        const float ag = ah_g[j], ag8 = ah_g8[j];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          acc[nt][0] = fmaf(ag, part[nt][0], acc[nt][0]);
-          acc[nt][1] = fmaf(ag, part[nt][1], acc[nt][1]);
-          acc[nt][2] = fmaf(ag8, part[nt][2], acc[nt][2]);
-          acc[nt][3] = fmaf(ag8, part[nt][3], acc[nt][3]);
-        }
       }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty_bar(slot));   // slot free for the producer
     }
-    // refill the register ring with the next blocks of the slice
-#pragma unroll
-    for (int jj = 0; jj < kRegBlocks; ++jj) {
-      const int jn = j0 + kRegBlocks + jj;
-      cur[jj][0] = (vg && jn < nb) ? ldg_codes(cg_ptr + jn * 32) : make_uint2(0u, 0u);
-      cur[jj][1] = (vg8 && jn < nb) ? ldg_codes(cg8_ptr + jn * 32) : make_uint2(0u, 0u);
-    }
+    if (!ok) report_status(p.status, kStatusTimeout);
   }
 
   // Epilogue: undo the token scales and stage this slice's partial
-  // [8 NT tokens x 128 rows] in shared memory (over the level table and,
-  // for 64 tokens, the start of the absmax table, both no longer read).
+  // [8 NT tokens x 128 rows] in shared memory (over the level table).
   float inv0[NT], inv1[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -392,15 +422,16 @@ gemv_fwd_kernel(const GemvArgs p) {
   }
   __syncthreads();
   float* out_s = reinterpret_cast<float*>(smem);
+  if (warp < kComputeWarps) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
-    const int rg = warp * 16 + g;
-    const float i0 = inv0[nt], i1 = inv1[nt];
-    out_s[tk0 * kOutStride + rg] = acc[nt][0] * i0;
-    out_s[tk1 * kOutStride + rg] = acc[nt][1] * i1;
-    out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * i0;
-    out_s[tk1 * kOutStride + rg + 8] = acc[nt][3] * i1;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
+      const int rg = warp * 16 + g;
+      out_s[tk0 * kOutStride + rg] = acc[nt][0] * inv0[nt];
+      out_s[tk1 * kOutStride + rg] = acc[nt][1] * inv1[nt];
+      out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * inv0[nt];
+      out_s[tk1 * kOutStride + rg + 8] = acc[nt][3] * inv1[nt];
+    }
   }
   if (p.slices == 1) {
     __syncthreads();
@@ -511,17 +542,16 @@ simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __rest
 
 }  // namespace
 
-// Dynamic shared memory of one GEMV CTA: level table, absmax table,
-// 64 token scales, the mbarrier, and the fp16 activation slice.
-constexpr size_t gemv_smem_bytes(int nt, int max_nb) {
-  return kTabBytes + static_cast<size_t>(kGemvRows) * max_nb * 4 + 64 * 4 + 16 +
-         8 * static_cast<size_t>(nt) * (static_cast<size_t>(max_nb) * 128 + 8);
+// Dynamic shared memory of one GEMV CTA (plus 1 KB to align the base).
+constexpr size_t gemv_smem_bytes(int nt, int ring, int max_nb) {
+  return static_cast<size_t>(gemv_off_xs(ring, max_nb)) +
+         8 * static_cast<size_t>(nt) * (static_cast<size_t>(max_nb) * 128 + 8) + 1024;
 }
 constexpr size_t kGemvSmemLimit = 220 * 1024;
 
 template <int NT>
-cudaError_t launch_gemv_nt(const cudaLaunchConfig_t& cfg, const GemvArgs& a) {
-  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<NT>, a);
+cudaError_t launch_gemv_nt(const cudaLaunchConfig_t& cfg, const CUtensorMap& tm, const GemvArgs& a) {
+  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<NT>, tm, a);
 }
 
 cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
@@ -529,7 +559,6 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
                             int num_sms, int* status, cudaStream_t st) {
   GemvArgs a;
   a.X = X;
-  a.codes = codes;
   a.a8 = a8;
   a.s2 = s2;
   a.Y = Y;
@@ -549,12 +578,18 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   if ((a.nblk + slices - 1) / slices > kMaxSliceBlocks) return cudaErrorInvalidValue;
   a.slices = slices;
   a.max_nb = (a.nblk + slices - 1) / slices;
-  // n-tiles of 8 tokens per CTA: all tokens at once when the activation slice
-  // fits, otherwise fewer tokens per CTA and more CTAs along z.
+  a.ring = std::min(kMaxRing, (a.max_nb + kBoxBlocks - 1) / kBoxBlocks);
   int nt = M <= 8 ? 1 : 2;
-  while (nt > 1 && gemv_smem_bytes(nt, a.max_nb) > kGemvSmemLimit) nt /= 2;
+  while (nt > 1 && gemv_smem_bytes(nt, a.ring, a.max_nb) > kGemvSmemLimit) nt /= 2;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
-  const size_t smem = gemv_smem_bytes(nt, a.max_nb);
+  const size_t smem = gemv_smem_bytes(nt, a.ring, a.max_nb);
+  if (smem > kGemvSmemLimit) return cudaErrorInvalidValue;
+  // packed codes [N, K/2] bytes, box 128 B (4 absmax blocks) x 128 rows, 128-byte swizzle
+  CUtensorMap tm;
+  if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), 128, kGemvRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   static std::once_flag once;
   std::call_once(once, [] {
     const int lim = static_cast<int>(kGemvSmemLimit);
@@ -574,7 +609,7 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return nt == 1 ? launch_gemv_nt<1>(cfg, a) : launch_gemv_nt<2>(cfg, a);
+  return nt == 1 ? launch_gemv_nt<1>(cfg, tm, a) : launch_gemv_nt<2>(cfg, tm, a);
 }
 
 cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,

@@ -313,3 +313,25 @@ def test_quantize_quotients_on_decision_edges():
     W = W.reshape(256, 1024)
     q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
     assert_quant_full(W, q)
+
+
+@pytest.mark.parametrize("rows,cols", [(8, 64), (24, 128), (136, 64), (8, 4096)])
+@pytest.mark.parametrize("M", [1, 16, 40])
+def test_fwd_small_shapes(rows, cols, M):
+    """Shortest reductions and fewest rows the format allows, on the decode
+    and tensor-memory paths (the code tile is wider than the weight)."""
+    W = weight_np(rows, cols, 21)
+    X = wl.activations(M, cols, seed=rows + M)
+    _, Y = run_fwd(W, X)
+    Wh = o.dequantize(*o.quantize(W), rows, cols)
+    assert_tol(Y, o.matmul_fwd(X.float().numpy(), Wh), f"fwd {rows}x{cols} M={M}")
+
+
+@pytest.mark.parametrize("rows,cols", [(8, 64), (24, 128), (136, 64)])
+@pytest.mark.parametrize("M", [3, 40])
+def test_dx_small_shapes(rows, cols, M):
+    W = weight_np(rows, cols, 22)
+    dY = wl.activations(M, rows, std=0.01, seed=rows + M)
+    _, dX = run_dx(W, dY)
+    Wh = o.dequantize(*o.quantize(W), rows, cols)
+    assert_tol(dX, o.matmul_bwd_dx(dY.float().numpy(), Wh), f"dX {rows}x{cols} M={M}")
