@@ -207,31 +207,32 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   __syncthreads();
 
   bool ok = true;
-  if (warp == kComputeWarps) {
-    // ------------------------------------------------------------ producer --
-    // Level table, then the slice's code boxes (128 rows x 4 blocks each,
-    // 128-byte swizzled) through a ring of `nring` slots.
-    if (lane == 0) {
-      tc::prefetch_tensormap(&tm_codes);
-      tc::mbar_arrive_expect_tx(tab_bar, kTabBytes);
-      bulk_copy_g2s(tc::smem_addr(tab), &kPairTable, kTabBytes, tab_bar);
-      int issued = 0;
-      for (int b = 0; b < nboxes; ++b) {
-        const int slot = b % nring;
-        if (b >= nring && !tc::mbar_wait(empty_bar(slot), ((b / nring) - 1) & 1)) {
-          report_status(p.status, kStatusTimeout);
-          break;
-        }
-        tc::mbar_arrive_expect_tx(full_bar(slot), kBoxBytes);
-        tc::tma_load_2d(ring + slot * kBoxBytes, &tm_codes, (kb0 + kBoxBlocks * b) * 32,
-                        static_cast<int32_t>(row0), full_bar(slot));
-        ++issued;
+  // Producer (lane 0 of the last warp): level table and code boxes (128 rows
+  // x 4 blocks each, 128-byte swizzled) through a ring of `nring` slots. The
+  // first ring-full goes out before the prologue barrier; the rest, which
+  // waits for slots to free, after it.
+  const bool producer = warp == kComputeWarps && lane == 0;
+  int issued = 0;
+  auto issue_boxes = [&](int upto) {
+    for (int b = issued; b < upto; ++b) {
+      const int slot = b % nring;
+      if (b >= nring && !tc::mbar_wait(empty_bar(slot), ((b / nring) - 1) & 1)) {
+        report_status(p.status, kStatusTimeout);
+        return;
       }
-      // copies still in flight land before the CTA may exit
-      for (int b = max(0, issued - nring); b < issued; ++b)
-        tc::mbar_wait(full_bar(b % nring), (b / nring) & 1);
+      tc::mbar_arrive_expect_tx(full_bar(slot), kBoxBytes);
+      tc::tma_load_2d(ring + slot * kBoxBytes, &tm_codes, (kb0 + kBoxBlocks * b) * 32,
+                      static_cast<int32_t>(row0), full_bar(slot));
+      issued = b + 1;
     }
-  } else {
+  };
+  if (producer) {
+    tc::prefetch_tensormap(&tm_codes);
+    tc::mbar_arrive_expect_tx(tab_bar, kTabBytes);
+    bulk_copy_g2s(tc::smem_addr(tab), &kPairTable, kTabBytes, tab_bar);
+    issue_boxes(min(nboxes, nring));
+  }
+  if (warp < kComputeWarps) {
     // Dequantized absmax of the CTA's rows over the slice: thread t owns row
     // t / 2 and every other block of it; all loads of a batch come first.
     {
@@ -339,6 +340,12 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     }
   }
   __syncthreads();
+  if (producer) {
+    issue_boxes(nboxes);
+    // copies still in flight land before the CTA may exit
+    for (int b = max(0, issued - nring); b < issued; ++b)
+      tc::mbar_wait(full_bar(b % nring), (b / nring) & 1);
+  }
 
   float acc[NT][4];
 #pragma unroll
