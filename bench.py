@@ -40,6 +40,31 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 L2_BYTES = 129 * 1024 * 1024
 
 
+def traffic_per_launch(workload, category):
+    """Mean DRAM bytes (read + write) per launch of a kernel class, from the
+    committed ncu capture for this workload, or None when there is none or the
+    CUDA sources changed since it was taken."""
+    import glob
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    srcs = sorted(glob.glob(os.path.join(ROOT, "dequant_gemm_gb300", "csrc", "*.cu")) +
+                  glob.glob(os.path.join(ROOT, "dequant_gemm_gb300", "csrc", "*.cuh")))
+    h = hashlib.sha256(b"".join(open(p, "rb").read() for p in srcs)).hexdigest()
+    vals, stamp = [], None
+    for line in open(path):
+        if line.startswith("# sources_sha256"):
+            stamp = line.split()[-1]
+        elif line.strip() and not line.startswith("#"):
+            f = line.split()
+            if f[0] == category:
+                vals.append(int(f[2]) + int(f[3]))
+    if stamp != h or not vals:
+        return None
+    return sum(vals) / len(vals)
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -463,7 +488,9 @@ def main():
     else:
         roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": d["TFLOP/s"] / pk["bf16_tflops_sustained"]}
-    roof.update({"kernel": dom, "traffic": None, "peak_kind": f"{pk_kind} ("
+    roof.update({"kernel": dom, "traffic": traffic_per_launch(work.name, dom),
+                 "traffic_unit": "bytes per launch (ncu dram read+write)",
+                 "achieved_per": "launch-average over the class", "peak_kind": f"{pk_kind} ("
                  + ("sustained bf16" if roof["bound"] == "tensor" else "copy") + ")"})
 
     line = {
