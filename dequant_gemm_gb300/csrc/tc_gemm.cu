@@ -148,7 +148,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      tc::mbar_init(dq_bar(s), kPair ? 2 * kDqGroupThreads : kDqGroupThreads);
+      // one arrival per dequant warp of the stage's group, from both CTAs of a pair
+      tc::mbar_init(dq_bar(s), (kPair ? 2 : 1) * (kDqGroupThreads / 32));
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
@@ -263,8 +264,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const uint32_t ph = (i / kStages) & 1;
         const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
         load_scale(i + 2);
-        if (*abort_flag) continue;
-        if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
+        // warp-uniform: the stage is done by all lanes or by none (the
+        // arrival below follows a __syncwarp)
+        bool go = !*abort_flag;
+        if (go && !tc::mbar_wait(full_bar(slot), ph)) {
+          fail();
+          go = false;
+        }
+        if (!__all_sync(0xffffffffu, go)) continue;
         const uint8_t* crow = smem + kOffCodes + slot * kCodesStageBytes + gt * 32;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -284,8 +291,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        if (kPair) tc::mbar_arrive_cluster(tc::map_to_cta(dq_bar(slot), 0));
-        else tc::mbar_arrive(dq_bar(slot));
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair) tc::mbar_arrive_cluster(tc::map_to_cta(dq_bar(slot), 0));
+          else tc::mbar_arrive(dq_bar(slot));
+        }
       }
     } else {
       const int kl = gt;                // weight column within the tile
@@ -325,8 +335,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         // the group's 128 threads meet here (named barrier 1 + group)
         if (grp == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
         else asm volatile("bar.sync 2, 128;" ::: "memory");
-        if (*abort_flag) continue;
-        if (!tc::mbar_wait(full_bar(slot), ph)) { fail(); continue; }
+        // warp-uniform: the stage is done by all lanes or by none (the
+        // arrival below follows a __syncwarp)
+        bool go = !*abort_flag;
+        if (go && !tc::mbar_wait(full_bar(slot), ph)) {
+          fail();
+          go = false;
+        }
+        if (!__all_sync(0xffffffffu, go)) continue;
         const uint8_t* cs = smem + kOffCodes + slot * kCodesStageBytes + (kl >> 1);
         const float* tb = tab + kbl * kScaledEntry;
 #pragma unroll
@@ -343,8 +359,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        if (kPair) tc::mbar_arrive_cluster(tc::map_to_cta(dq_bar(slot), 0));
-        else tc::mbar_arrive(dq_bar(slot));
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair) tc::mbar_arrive_cluster(tc::map_to_cta(dq_bar(slot), 0));
+          else tc::mbar_arrive(dq_bar(slot));
+        }
       }
     }
 
