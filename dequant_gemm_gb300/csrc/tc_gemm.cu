@@ -148,8 +148,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      // one arrival per dequant warp of the stage's group, from both CTAs of a pair
-      tc::mbar_init(dq_bar(s), (kPair ? 2 : 1) * (kDqGroupThreads / 32));
+      // one arrival per dequant warp of the stage's group (+ the peer's relay)
+      tc::mbar_init(dq_bar(s), kDqGroupThreads / 32 + ((kPair && rank == 0) ? 1 : 0));
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
@@ -236,6 +236,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       }
       if (kPair) tc::mma_commit_pair(accum_bar);
       else tc::mma_commit(accum_bar);
+    } else if (kPair && lane == 0) {
+      // Peer CTA of a pair: relay "this CTA's stage is dequantized" to the
+      // issuing CTA with one cluster-scope arrive per stage, from a thread
+      // with no memory traffic of its own in flight.
+      const uint32_t remote0 = tc::map_to_cta(dq_bar(0), 0);
+      for (int i = 0; i < nst && !*abort_flag; ++i) {
+        const int slot = i % kStages;
+        if (!tc::mbar_wait(dq_bar(slot), (i / kStages) & 1)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        tc::fence_before_sync();
+        tc::mbar_arrive_cluster(remote0 + 8u * slot);
+      }
     }
     if (lane == 0 && !tc::mbar_wait(accum_bar, 0)) fail();   // all MMAs done before teardown
   } else {
@@ -292,10 +307,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          if (kPair) tc::mbar_arrive_cluster(tc::map_to_cta(dq_bar(slot), 0));
-          else tc::mbar_arrive(dq_bar(slot));
-        }
+        if (lane == 0) tc::mbar_arrive(dq_bar(slot));
       }
     } else {
       const int kl = gt;                // weight column within the tile
@@ -360,10 +372,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          if (kPair) tc::mbar_arrive_cluster(tc::map_to_cta(dq_bar(slot), 0));
-          else tc::mbar_arrive(dq_bar(slot));
-        }
+        if (lane == 0) tc::mbar_arrive(dq_bar(slot));
       }
     }
 
