@@ -114,7 +114,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <bool kDx, bool kPair>
+template <bool kDx>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                const TcArgs p) {
@@ -134,13 +134,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * p.bn;
-  // CTA pair: both CTAs dequantize their own 128 rows into their own tensor
-  // memory and load half of the token tile; the even CTA issues the 256-row
-  // MMA for both.
-  const uint32_t rank = kPair ? tc::cluster_rank() : 0u;
-  const bool issuer = !kPair || rank == 0;
-  const int bn_load = kPair ? p.bn / 2 : p.bn;            // token rows this CTA loads
-  const int64_t m_load = m0 + static_cast<int64_t>(rank) * bn_load;
   const int s_begin = blockIdx.z * p.stages_per_split;
   const int nst = min(p.stages_per_split, p.stages_total - s_begin);
 
@@ -148,8 +141,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      // one arrival per dequant warp of the stage's group (+ the peer's relay)
-      tc::mbar_init(dq_bar(s), kDqGroupThreads / 32 + ((kPair && rank == 0) ? 1 : 0));
+      tc::mbar_init(dq_bar(s), kDqGroupThreads / 32);   // one arrival per dequant warp
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
@@ -165,13 +157,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     tc::prefetch_tensormap(&tm_act);
     tc::prefetch_tensormap(&tm_codes);
   }
-  if (warp == 1) {
-    if (kPair) tc::tmem_alloc_pair(tc::smem_addr(tmem_slot), kTmemCols);
-    else tc::tmem_alloc(tc::smem_addr(tmem_slot), kTmemCols);
-  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
-  if (kPair) tc::cluster_barrier();   // both CTAs' barriers exist before any remote arrive
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
@@ -183,7 +171,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
-      const uint32_t tx = static_cast<uint32_t>(bn_load) * 128u + kCodesStageBytes;
+      const uint32_t tx = static_cast<uint32_t>(p.bn) * 128u + kCodesStageBytes;
       int issued = 0;
       for (int i = 0; i < nst && !*abort_flag; ++i) {
         const int slot = i % kStages;
@@ -193,7 +181,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::mbar_arrive_expect_tx(full_bar(slot), tx);
         const uint32_t act = tc::smem_addr(smem + kOffAct + slot * kActStageBytes);
         const uint32_t cod = tc::smem_addr(smem + kOffCodes + slot * kCodesStageBytes);
-        tc::tma_load_2d(act, &tm_act, s * 64, static_cast<int32_t>(m_load), full_bar(slot));
+        tc::tma_load_2d(act, &tm_act, s * 64, static_cast<int32_t>(m0), full_bar(slot));
         if (!kDx) {
           tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
         } else {
@@ -208,14 +196,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
-    if (lane == 0 && issuer) {
-      const uint32_t idesc =
-          tc::idesc_bf16_f32(kPair ? 2 * kTileRows : kTileRows, static_cast<uint32_t>(p.bn));
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, static_cast<uint32_t>(p.bn));
       for (int i = 0; i < nst && !*abort_flag; ++i) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        const bool ready = kPair ? tc::mbar_wait_cluster(dq_bar(slot), ph) : tc::mbar_wait(dq_bar(slot), ph);
-        if (!ready || !tc::mbar_wait(full_bar(slot), ph)) {
+        if (!tc::mbar_wait(dq_bar(slot), ph) || !tc::mbar_wait(full_bar(slot), ph)) {
           fail();
           break;
         }
@@ -224,35 +210,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const uint32_t b = tc::smem_addr(smem + kOffAct + slot * kActStageBytes);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (kPair)
-            tc::mma_bf16_tmem_a_pair(tmem, a + 8u * j, tc::sw128_kmajor_desc(b + 32u * j), idesc,
-                                     (i | j) != 0 ? 1u : 0u);
-          else
-            tc::mma_bf16_tmem_a(tmem, a + 8u * j, tc::sw128_kmajor_desc(b + 32u * j), idesc,
-                                (i | j) != 0 ? 1u : 0u);
+          tc::mma_bf16_tmem_a(tmem, a + 8u * j, tc::sw128_kmajor_desc(b + 32u * j), idesc,
+                              (i | j) != 0 ? 1u : 0u);
         }
-        if (kPair) tc::mma_commit_pair(empty_bar(slot));
-        else tc::mma_commit(empty_bar(slot));
+        tc::mma_commit(empty_bar(slot));
       }
-      if (kPair) tc::mma_commit_pair(accum_bar);
-      else tc::mma_commit(accum_bar);
-    } else if (kPair && lane == 0) {
-      // Peer CTA of a pair: relay "this CTA's stage is dequantized" to the
-      // issuing CTA with one cluster-scope arrive per stage, from a thread
-      // with no memory traffic of its own in flight.
-      const uint32_t remote0 = tc::map_to_cta(dq_bar(0), 0);
-      for (int i = 0; i < nst && !*abort_flag; ++i) {
-        const int slot = i % kStages;
-        if (!tc::mbar_wait(dq_bar(slot), (i / kStages) & 1)) {
-          fail();
-          break;
-        }
-        tc::fence_after_sync();
-        tc::fence_before_sync();
-        tc::mbar_arrive_cluster(remote0 + 8u * slot);
-      }
+      tc::mma_commit(accum_bar);
+      if (!tc::mbar_wait(accum_bar, 0)) fail();   // all MMAs done before teardown
     }
-    if (lane == 0 && !tc::mbar_wait(accum_bar, 0)) fail();   // all MMAs done before teardown
   } else {
     // ---------------------------------------------------- dequant + store --
     const int q = warp & 3;             // TMEM lane quarter of this warp
@@ -403,15 +368,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 
   tc::fence_before_sync();
   __syncthreads();
-  if (kPair) tc::cluster_barrier();   // the peer's MMAs and reads are over before either frees
   if (warp == 1) {
     tc::fence_after_sync();
-    if (kPair) tc::tmem_dealloc_pair(tmem, kTmemCols);
-    else tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <bool kDx, bool kPair>
+template <bool kDx>
 cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, const uint8_t* a8,
                       const float* s2, int64_t N, int64_t K, float* out, int num_sms, int* status,
                       cudaStream_t st) {
@@ -427,8 +390,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   a.bn = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
   const int64_t nd = kDx ? K : N;            // tile-row dimension
   const int64_t red = kDx ? N : K;           // reduction dimension
-  int64_t row_tiles = (nd + kTileRows - 1) / kTileRows;
-  if (kPair) row_tiles += row_tiles & 1;     // whole CTA pairs (a spare tile stores nothing)
+  const int64_t row_tiles = (nd + kTileRows - 1) / kTileRows;
   const int64_t m_tiles = (M + a.bn - 1) / a.bn;
   a.stages_total = static_cast<int>((red + 63) / 64);
   int splits = 1;
@@ -445,7 +407,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   // activations: [M, red] bf16, box 64 (reduction) x bn (tokens), 128-byte swizzle
   if (!encode_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, static_cast<uint64_t>(red),
                  static_cast<uint64_t>(M), static_cast<uint64_t>(red) * 2, 64,
-                 static_cast<uint32_t>(kPair ? a.bn / 2 : a.bn), CU_TENSOR_MAP_SWIZZLE_128B))
+                 static_cast<uint32_t>(a.bn), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // packed codes: [N, K/2] bytes; the forward takes 32 B x 128 rows, the input
   // gradient 64 B (128 columns) x 64 rows
@@ -456,44 +418,30 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
 
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(tc_gemm_kernel<kDx, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemBytes);
+    cudaFuncSetAttribute(tc_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (a.atomic_out) {
     cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(M) * nd * sizeof(float), st);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
-                     static_cast<unsigned>(splits));
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kPair ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kDx, kPair>, tm_act, tm_codes, a);
+  dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
+            static_cast<unsigned>(splits));
+  tc_gemm_kernel<kDx><<<grid, kTcThreads, kSmemBytes, st>>>(tm_act, tm_codes, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-// Token counts above 128 use 256-token tiles computed by CTA pairs.
 cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
                           const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
                           int* status, cudaStream_t st) {
-  if (M > 128) return launch_tc<false, true>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
-  return launch_tc<false, false>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
+  return launch_tc<false>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
 }
 
 cudaError_t launch_tc_dx(const uint16_t* dY, int64_t M, const uint8_t* codes, const uint8_t* a8,
                          const float* s2, int64_t N, int64_t K, float* dX, int num_sms,
                          int* status, cudaStream_t st) {
-  if (M > 128) return launch_tc<true, true>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
-  return launch_tc<true, false>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
+  return launch_tc<true>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
 }
 
 }  // namespace nf4
