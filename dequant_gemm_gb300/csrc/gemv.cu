@@ -119,15 +119,12 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-// Read a float of CTA `rank`'s shared memory at this CTA's address of `local`.
-// Volatile (kept between the cluster barriers) but without a memory clobber,
-// so several of these are issued back to back before their results are used.
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
+// Store a float into CTA `rank`'s shared memory at this CTA's address of
+// `local` (made visible to that CTA by the next cluster barrier).
+__device__ __forceinline__ void st_dsmem(float* local, uint32_t rank, float v) {
   uint32_t remote;
   asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 struct GemvArgs {
@@ -167,6 +164,10 @@ __host__ __device__ constexpr int gemv_off_bars(int ring, int max_nb) {
 __host__ __device__ constexpr int gemv_off_xs(int ring, int max_nb) {
   return gemv_off_bars(ring, max_nb) + (1 + 2 * kMaxRing) * 8 + 8;
 }
+// Inbox of the cluster reduction: [slices][8 NT tokens][128 / slices rows].
+__host__ __device__ constexpr int gemv_off_inbox(int ring, int max_nb, int nt) {
+  return (gemv_off_xs(ring, max_nb) + 8 * nt * (max_nb * 128 + 8) + 15) & ~15;
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kGemvThreads)
@@ -195,6 +196,46 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   const int nboxes = (nb + kBoxBlocks - 1) / kBoxBlocks;
   const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
   const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
+
+  // The prologue's own loads (activations, absmax codes, scales) are issued
+  // before the producer starts streaming the code tile, so that they do not
+  // queue behind it; the main loop then overlaps the stream.
+  const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
+  const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K +
+                                                      static_cast<int64_t>(kb0) * kBlock);
+  const int64_t xrow4 = p.K / 4;
+  uint2 xv[NT][4];
+  auto load_x = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      const int tk = warp + 8 * u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = c0 + lane + 32 * c;
+        xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
+      }
+    }
+  };
+  // dequantized absmax: thread t owns row t / 2 and every other block of it
+  constexpr int kAh = 4;
+  const int ah_r = tid >> 1, ah_par = tid & 1;
+  const bool ah_vrow = warp < kComputeWarps && row0 + ah_r < p.N;
+  const int64_t ah_bi0 = (row0 + ah_r) * p.nblk + kb0;
+  uint32_t av[kAh];
+  float sv[kAh];
+  auto load_ah = [&](int j0) {
+#pragma unroll
+    for (int u = 0; u < kAh; ++u) {
+      const int j = j0 + 2 * u;
+      const bool okj = ah_vrow && j < nb;
+      av[u] = okj ? static_cast<uint32_t>(__ldg(p.a8 + ah_bi0 + j)) : 0u;
+      sv[u] = okj ? __ldg(p.s2 + ((ah_bi0 + j) >> 8)) : 0.0f;
+    }
+  };
+  if (warp < kComputeWarps) {
+    load_x(0);
+    load_ah(ah_par);
+  }
 
   if (tid == 0) {
     tc::mbar_init(tab_bar, 1);
@@ -233,25 +274,11 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     issue_boxes(min(nboxes, nring));
   }
   if (warp < kComputeWarps) {
-    // Dequantized absmax of the CTA's rows over the slice: thread t owns row
-    // t / 2 and every other block of it; all loads of a batch come first.
+    // Dequantized absmax (batches of kAh blocks; the first one is in flight).
     {
-      const int r = tid >> 1, par = tid & 1;
-      const int64_t n = row0 + r;
-      const bool vrow = n < p.N;
-      const int64_t bi0 = n * p.nblk + kb0;
-      float* arow = ahat_s + r * p.max_nb;
-      constexpr int kAh = 4;
-      for (int j0 = par; j0 < nb; j0 += 2 * kAh) {
-        uint32_t av[kAh];
-        float sv[kAh];
-#pragma unroll
-        for (int u = 0; u < kAh; ++u) {
-          const int j = j0 + 2 * u;
-          const bool okj = vrow && j < nb;
-          av[u] = okj ? static_cast<uint32_t>(__ldg(p.a8 + bi0 + j)) : 0u;
-          sv[u] = okj ? __ldg(p.s2 + ((bi0 + j) >> 8)) : 0.0f;
-        }
+      float* arow = ahat_s + ah_r * p.max_nb;
+      for (int j0 = ah_par; j0 < nb; j0 += 2 * kAh) {
+        if (j0 != ah_par) load_ah(j0);
 #pragma unroll
         for (int u = 0; u < kAh; ++u) {
           const int j = j0 + 2 * u;
@@ -259,16 +286,12 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
         }
       }
     }
-    // Activations: warp w stages tokens w + 8u (u < NT). Per chunk of 128
-    // uint2 (8 blocks) every load of the warp is issued before any is used;
-    // per-token max |x| -> power-of-two scale into [2^14, 2^15) -> fp16. A
-    // slice of at most 8 blocks is converted straight from registers, longer
-    // slices are read a second time.
+
+    // Activations: warp w stages tokens w + 8u (u < NT) in chunks of 128 uint2
+    // (8 blocks; the first one is in flight): per-token max |x| -> power-of-two
+    // scale into [2^14, 2^15) -> fp16. A slice of at most 8 blocks is converted
+    // straight from registers, longer slices are read a second time.
     {
-      const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
-      const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K +
-                                                          static_cast<int64_t>(kb0) * kBlock);
-      const int64_t xrow4 = p.K / 4;
       auto absmax4 = [](uint2 v) {
         const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
         const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
@@ -281,20 +304,11 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
         const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
         return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
       };
-      uint2 xv[NT][4];
       float mx[NT];
 #pragma unroll
       for (int u = 0; u < NT; ++u) mx[u] = 0.0f;
       for (int c0 = 0; c0 < nkv4; c0 += 128) {
-#pragma unroll
-        for (int u = 0; u < NT; ++u) {
-          const int tk = warp + 8 * u;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int i = c0 + lane + 32 * c;
-            xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
-          }
-        }
+        if (c0 > 0) load_x(c0);
 #pragma unroll
         for (int u = 0; u < NT; ++u)
 #pragma unroll
@@ -315,17 +329,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
         if (lane == 0) xinv[warp + 8 * u] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
       }
       for (int c0 = 0; c0 < nkv4; c0 += 128) {
-        if (c0 > 0 || nkv4 > 128) {
-#pragma unroll
-          for (int u = 0; u < NT; ++u) {
-            const int tk = warp + 8 * u;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int i = c0 + lane + 32 * c;
-              xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
-            }
-          }
-        }
+        if (nkv4 > 128) load_x(c0);
 #pragma unroll
         for (int u = 0; u < NT; ++u) {
           const int tk = warp + 8 * u;
@@ -429,7 +433,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   }
   __syncthreads();
   float* out_s = reinterpret_cast<float*>(smem);
-  if (warp < kComputeWarps) {
+  if (p.slices == 1 && warp < kComputeWarps) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
@@ -449,27 +453,37 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
             *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4);
     }
   } else {
-    // Cluster reduction: CTA `rank` sums rows [rank*rpc, (rank+1)*rpc) of every
-    // slice's partial through distributed shared memory and stores them.
+    // Cluster reduction, push form: CTA `rank` owns rows [rank*rpc, (rank+1)*rpc)
+    // of the row tile. Every CTA stores its scaled partial of those rows into
+    // the owner's inbox slot for its slice, one cluster barrier makes the
+    // stores visible, and each owner sums its slots and writes Y once.
+    float* inbox = reinterpret_cast<float*>(smem + gemv_off_inbox(p.ring, p.max_nb, NT));
+    const int rpc = kGemvRows / p.slices;          // rows owned per CTA (a power of two)
+    const int rpc_shift = 31 - __clz(rpc);
+    if (warp < kComputeWarps) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int tk0 = nt * 8 + 2 * t;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tk = tk0 + (e & 1);
+          const int rg = warp * 16 + g + 8 * (e >> 1);
+          const float v = acc[nt][e] * ((e & 1) ? inv1[nt] : inv0[nt]);
+          const uint32_t owner = static_cast<uint32_t>(rg >> rpc_shift);
+          st_dsmem(inbox + ((slice * 8 * NT + tk) << rpc_shift) + (rg & (rpc - 1)), owner, v);
+        }
+      }
+    }
     cluster_sync();
-    const uint32_t rank = cluster_ctarank();
-    const int rpc = kGemvRows / p.slices;          // rows reduced by this CTA
-    const int rpc_shift = 31 - __clz(rpc);         // rpc is a power of two
+    const int rank = static_cast<int>(cluster_ctarank());
     for (int i = tid; i < 8 * NT * rpc; i += kGemvThreads) {
-      const int tk = i >> rpc_shift, r = static_cast<int>(rank) * rpc + (i & (rpc - 1));
+      const int tk = i >> rpc_shift, rl = i & (rpc - 1), r = rank * rpc + rl;
       if (tk < mt && row0 + r < p.N) {
-        const float* src = out_s + tk * kOutStride + r;
-        float part[kMaxCluster];
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)   // all remote loads in flight at once
-          part[c] = (c < p.slices) ? ld_dsmem(src, c) : 0.0f;
         float v = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c) v += part[c];
+        for (int c = 0; c < p.slices; ++c) v += inbox[((c * 8 * NT + tk) << rpc_shift) + rl];
         p.Y[(m0 + tk) * p.N + row0 + r] = v;
       }
     }
-    cluster_sync();   // no CTA leaves while its partial may still be read
   }
 }
 
@@ -551,8 +565,7 @@ simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __rest
 
 // Dynamic shared memory of one GEMV CTA (plus 1 KB to align the base).
 constexpr size_t gemv_smem_bytes(int nt, int ring, int max_nb) {
-  return static_cast<size_t>(gemv_off_xs(ring, max_nb)) +
-         8 * static_cast<size_t>(nt) * (static_cast<size_t>(max_nb) * 128 + 8) + 1024;
+  return static_cast<size_t>(gemv_off_inbox(ring, max_nb, nt)) + 8 * nt * kGemvRows * 4 + 1024;
 }
 constexpr size_t kGemvSmemLimit = 220 * 1024;
 
