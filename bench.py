@@ -180,33 +180,68 @@ class Step:
                 self.dx[(i, M)] = torch.empty(M, p.cols, dtype=torch.float32, device=device)
         self.quantize_in_step = rotate == 1
         self.calls = self._calls()
+        self.side = []
         self.graphs = None
 
     def _calls(self):
-        """List of (category, flop, bytes, launches, fn) in step order. With
-        rotating weight copies, one step walks every copy once."""
+        """List of (category, flop, bytes, launches, fn, group) in step order.
+        Calls with the same group are independent and may be issued together
+        (the projections of the layer that share an input); groups run in
+        order. With rotating weight copies, one step walks every copy once."""
         nf4 = self.nf4
         calls = []
         P = self.w.projections
+        groups = self.w.issue_groups()
         if self.quantize_in_step:
             for i, p in enumerate(P):
                 calls.append(("quantize", 0, quant_bytes(p), 1,
-                              lambda i=i: nf4.nf4_quantize(self.weights[i], out=self.q[0][i])))
+                              lambda i=i: nf4.nf4_quantize(self.weights[i], out=self.q[0][i]),
+                              ("quantize", 0)))
         for M in sorted(self.w.fwd_m, reverse=True):
             for r in range(self.rotate):
-                for i, p in enumerate(P):
-                    f, b = fwd_work(p, M)
-                    calls.append((f"fwd_M{M}", f, b, 1,
-                                  lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_fwd(
-                                      self.x[(p.cols, M)], self.q[r][i], out=self.y[(i, M)])))
+                for gi, g in enumerate(groups):
+                    for i in g:
+                        p = P[i]
+                        f, b = fwd_work(p, M)
+                        calls.append((f"fwd_M{M}", f, b, 1,
+                                      lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_fwd(
+                                          self.x[(p.cols, M)], self.q[r][i], out=self.y[(i, M)]),
+                                      (f"fwd_M{M}", r, gi)))
         for M in self.w.dx_m:
             for r in range(self.rotate):
-                for i, p in enumerate(P):
-                    f, b = dx_work(p, M)
-                    calls.append((f"dx_M{M}", f, b, 1,
-                                  lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_bwd_dx(
-                                      self.dy[(p.rows, M)], self.q[r][i], out=self.dx[(i, M)])))
+                for gi, g in enumerate(groups):
+                    for i in g:
+                        p = P[i]
+                        f, b = dx_work(p, M)
+                        calls.append((f"dx_M{M}", f, b, 1,
+                                      lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_bwd_dx(
+                                          self.dy[(p.rows, M)], self.q[r][i], out=self.dx[(i, M)]),
+                                      (f"dx_M{M}", r, gi)))
         return calls
+
+    def issue(self, idx):
+        """Launch calls idx in order; the members of a group go out on
+        parallel streams forked from and joined back to the current one, so
+        the tail wave of one can share the SMs with the next."""
+        main = torch.cuda.current_stream(self.dev)
+        runs = []
+        for k in idx:
+            if runs and runs[-1][0] == self.calls[k][5]:
+                runs[-1][1].append(k)
+            else:
+                runs.append((self.calls[k][5], [k]))
+        for _, ks in runs:
+            if len(ks) == 1:
+                self.calls[ks[0]][4]()
+                continue
+            while len(self.side) < len(ks):
+                self.side.append(torch.cuda.Stream(self.dev))
+            for s, k in zip(self.side, ks):
+                s.wait_stream(main)
+                with torch.cuda.stream(s):
+                    self.calls[k][4]()
+            for s in self.side[:len(ks)]:
+                main.wait_stream(s)
 
     def blocks(self):
         """Contiguous runs of one category: (category, [call indices])."""
@@ -231,8 +266,7 @@ class Step:
         for cat, idx in self.blocks():
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                for k in idx:
-                    self.calls[k][4]()
+                self.issue(idx)
             self.graphs.append((cat, idx, g))
         torch.cuda.synchronize(self.dev)
 
@@ -243,8 +277,7 @@ class Step:
         return sum(c[3] for c in self.calls)
 
     def run_eager(self):
-        for c in self.calls:
-            c[4]()
+        self.issue(range(len(self.calls)))
 
     def run(self, events=None):
         """Replay the captured step; events[j] brackets graph j."""
@@ -459,7 +492,7 @@ def main():
             e0, e1 = events[s * ngraphs + j]
             cat_ms[cat] = cat_ms.get(cat, 0.0) + e0.elapsed_time(e1)
             for k in idx:
-                _, f, b, n, _ = step.calls[k]
+                _, f, b, n, _, _ = step.calls[k]
                 cat_flop[cat] = cat_flop.get(cat, 0) + f
                 cat_bytes[cat] = cat_bytes.get(cat, 0) + b
                 cat_n[cat] = cat_n.get(cat, 0) + n

@@ -53,6 +53,39 @@ __host__ __device__ inline float bits_to_float(uint32_t b) {
 #endif
 }
 
+// fp32 -> fp16 round-to-nearest-even for the NF4 levels (all normal in fp16
+// or zero), evaluated at compile time.
+constexpr uint32_t level_to_f16(uint32_t b) {
+  const uint32_t sign = (b >> 16) & 0x8000u;
+  const uint32_t e = (b >> 23) & 0xffu;
+  if (e == 0) return sign;
+  const uint32_t m = b & 0x7fffffu;
+  uint32_t h = ((e - 127u + 15u) << 10) | (m >> 13);
+  const uint32_t rest = m & 0x1fffu;
+  if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;
+  return sign | h;
+}
+
+// Level pair table indexed by a code byte, in 32 lane-private copies so that
+// any 32 lookups of a warp hit 32 distinct banks: entry b of copy l is word
+// 32 b + l, whose low half is the fp16 level of the high nibble (the
+// lower-index element of the pair) and whose high half is the level of the
+// low nibble. Each kernel file instantiates its own copy in device memory and
+// brings it into shared memory with one bulk copy per CTA.
+constexpr int kHalfPairTableBytes = 256 * 32 * 4;
+struct HalfPairTable {
+  uint32_t w[256 * 32];
+};
+
+constexpr HalfPairTable make_half_pair_table() {
+  HalfPairTable t{};
+  for (int i = 0; i < 256 * 32; ++i) {
+    const int b = i >> 5;
+    t.w[i] = level_to_f16(kLevelBits[b >> 4]) | (level_to_f16(kLevelBits[b & 15]) << 16);
+  }
+  return t;
+}
+
 // Device status word values (the library's nf4_status codes).
 constexpr int kStatusTimeout = NF4_ERR_DEVICE_TIMEOUT;
 

@@ -42,40 +42,12 @@ namespace nf4 {
 namespace {
 
 constexpr int kGemvRows = 128;
-constexpr int kTabBytes = 256 * 32 * 4;
+constexpr int kTabBytes = kHalfPairTableBytes;
 constexpr int kMaxSliceBlocks = 48;
 constexpr int kMaxCluster = 8;
 constexpr int kOutStride = kGemvRows + 4;     // floats, keeps rows 16-byte aligned
 
-// fp32 -> fp16 round-to-nearest-even for the NF4 levels (all normal in fp16
-// or zero), evaluated at compile time.
-constexpr uint32_t level_to_f16(uint32_t b) {
-  const uint32_t sign = (b >> 16) & 0x8000u;
-  const uint32_t e = (b >> 23) & 0xffu;
-  if (e == 0) return sign;
-  const uint32_t m = b & 0x7fffffu;
-  uint32_t h = ((e - 127u + 15u) << 10) | (m >> 13);
-  const uint32_t rest = m & 0x1fffu;
-  if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;
-  return sign | h;
-}
-
-struct PairTable {
-  uint32_t w[256 * 32];
-};
-
-// Entry b of copy l at word 32 b + l: low half = fp16 level of the high
-// nibble (the even, lower-k element), high half = level of the low nibble.
-constexpr PairTable make_pair_table() {
-  PairTable t{};
-  for (int i = 0; i < 256 * 32; ++i) {
-    const int b = i >> 5;
-    t.w[i] = level_to_f16(kLevelBits[b >> 4]) | (level_to_f16(kLevelBits[b & 15]) << 16);
-  }
-  return t;
-}
-
-__device__ __align__(128) const PairTable kPairTable = make_pair_table();
+__device__ __align__(128) const HalfPairTable kPairTable = make_half_pair_table();
 
 // Not volatile: independent MMA chains of different blocks may interleave.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,

@@ -9,25 +9,35 @@
 // 256), looping over the reduction in stages of 64:
 //   * warp 0 (one thread) TMA-loads the stage's activation tile (bf16,
 //     128-byte swizzle, the K-major B operand) and its packed-code tile;
-//   * warps 2-9, in two groups of four that take alternate stages,
-//     dequantize the codes (level * dequantized absmax, rounded to bf16) and
-//     write them straight into tensor memory, where the MMA reads its A
-//     operand: the dequantized weight never touches shared memory. The
-//     forward looks up both levels of a code byte at once in a 256-entry pair
-//     table kept in 32 lane-private copies (every lookup of a warp hits 32
-//     distinct banks); the input gradient builds, per stage, a table of the 16
-//     levels pre-multiplied by each row's dequantized absmax;
+//   * the dequant warps, in groups of four (one per tensor-memory lane
+//     quarter) that take the stages in turn, dequantize the codes (level *
+//     dequantized absmax, rounded to bf16) and write them straight into
+//     tensor memory, where the MMA reads its A operand: the dequantized
+//     weight never touches shared memory;
 //   * warp 1 (one thread) issues tcgen05.mma (128 x BN x 16) into an fp32
 //     accumulator in tensor memory and commits each stage back to the
 //     producer;
-//   * warps 2-9 then read the accumulator with tcgen05.ld and store fp32
-//     outputs (coalesced: 32 consecutive outputs of one token per warp store).
-// The forward walks a tile of 128 weight rows along K, one row per dequant
-// thread; the input gradient walks a tile of 128 weight columns along N, one
-// column per dequant thread, reading its nibbles down the stage's 64 rows
-// (the transposed walk). When the output tiles alone
-// cannot fill the GPU the reduction is split across CTAs and summed with
-// atomics into a zeroed output.
+//   * the dequant warps then read the accumulator with tcgen05.ld and store
+//     fp32 outputs (32 consecutive outputs of one token per warp store).
+//
+// Forward: the tile is 128 weight rows, one row per dequant thread, walked
+// along K. Both levels of a code byte come from one lookup in a 256-entry
+// fp32 pair table kept in 32 lane-private copies (every lookup of a warp hits
+// 32 distinct banks); the row's absmax scale is a register.
+//
+// Input gradient: the tile is 128 weight columns walked along N (the
+// transposed walk), so a thread needs its column's nibbles down the stage's
+// 64 rows. Each warp reads its 32 columns' codes as 32-bit words (8 columns
+// of one row) and transposes 8 x 8 nibble blocks across lanes with three
+// shuffle rounds, after which a byte of a thread's word holds the codes of
+// two consecutive rows of its column: exactly one 32-bit tensor-memory word
+// of the A operand. That byte indexes a 256-entry fp16 level pair table (32
+// lane copies); the two levels are widened to fp32 and multiplied by their
+// rows' dequantized absmax, which the warp computes for its 64 rows and
+// broadcasts through shared memory.
+//
+// When the output tiles alone cannot fill the GPU the reduction is split
+// across CTAs and summed with atomics into a zeroed output.
 //
 // Every mbarrier wait is bounded; a CTA that gives up records a timeout in the
 // device status word, skips the remaining work and still releases its tensor
@@ -41,31 +51,34 @@
 namespace nf4 {
 namespace {
 
-constexpr int kTcThreads = 320;              // 10 warps
-constexpr int kDqGroupThreads = 128;         // warps 2-5 and 6-9, alternate stages
-constexpr int kStages = 4;
 constexpr int kTileRows = 128;               // MMA M
 constexpr int kMaxBN = 256;                  // MMA N
 constexpr int kActStageBytes = kMaxBN * 128; // 64 bf16 per token row
-constexpr int kCodesStageBytes = 4096;
+constexpr int kCodesStageBytes = 4096;       // 128 x 64 nibbles
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemA0 = 256;            // columns [256, 384): A-operand slots
+constexpr uint32_t kTmemA0 = 256;            // columns from 256 on: A-operand slots
+constexpr int kPairLutBytes = 256 * 32 * 8;  // forward: (c[hi], c[lo]) fp32 x 32 copies
 
-constexpr int kPairLutBytes = 256 * 32 * 8;           // forward: (c[hi], c[lo]) x 32 copies
-// dX: per stage 64 rows x 2 blocks of 16 scaled levels, each entry padded to
-// 20 floats so that the 16-byte stores of a warp land on distinct banks
-constexpr int kScaledEntry = 20;
-constexpr int kScaledLutBytes = kStages * 64 * 2 * kScaledEntry * 4;
-constexpr int kLutBytes = kPairLutBytes > kScaledLutBytes ? kPairLutBytes : kScaledLutBytes;
-
-constexpr int kOffAct = 0;
-constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
-constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
-constexpr int kOffLevels = kOffLut + kLutBytes;
-constexpr int kOffBars = kOffLevels + 64;
-constexpr int kNumBars = 3 * kStages + 2;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+// Per-direction configuration and shared-memory layout.
+template <bool kDx>
+struct Cfg {
+  static constexpr int kGroups = kDx ? 3 : 2;        // dequant warp groups
+  static constexpr int kDqWarps = 4 * kGroups;
+  static constexpr int kThreads = 64 + 32 * kDqWarps;
+  static constexpr int kStages = 4;
+  static constexpr int kLutBytes = kDx ? kHalfPairTableBytes : kPairLutBytes;
+  static constexpr int kAhatBytes = kDx ? kDqWarps * 64 * 4 : 0;   // per-warp row scales
+  static constexpr int kOffAct = 0;
+  static constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
+  static constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
+  static constexpr int kOffAhat = kOffLut + kLutBytes;
+  static constexpr int kOffBars = kOffAhat + kAhatBytes;
+  static constexpr int kNumBars = 3 * kStages + 2;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+  static_assert(kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 
 struct TcArgs {
   const uint8_t* a8;
@@ -100,6 +113,9 @@ constexpr PairLevels make_pair_levels() {
 __device__ __align__(128) const PairLevels kPairLevels = make_pair_levels();
 static_assert(sizeof(PairLevels) == kPairLutBytes, "pair table size");
 
+// Input-gradient pair table (fp16 levels, see common.cuh).
+__device__ __align__(128) const HalfPairTable kHalfPairs = make_half_pair_table();
+
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
   asm volatile(
@@ -114,22 +130,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+
 template <bool kDx>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(Cfg<kDx>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                const TcArgs p) {
+  using C = Cfg<kDx>;
+  constexpr int kStages = C::kStages;
+  constexpr int kGroups = C::kGroups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* levels = reinterpret_cast<float*>(smem + kOffLevels);
-  const uint32_t bars = tc::smem_addr(smem + kOffBars);
+  const uint32_t bars = tc::smem_addr(smem + C::kOffBars);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto dq_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto empty_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
   const uint32_t accum_bar = bars + 8u * (3 * kStages);
   const uint32_t lut_bar = bars + 8u * (3 * kStages + 1);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
@@ -137,21 +156,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   const int s_begin = blockIdx.z * p.stages_per_split;
   const int nst = min(p.stages_per_split, p.stages_total - s_begin);
 
-  if (threadIdx.x < 16) levels[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      tc::mbar_init(dq_bar(s), kDqGroupThreads / 32);   // one arrival per dequant warp
+      tc::mbar_init(dq_bar(s), 4);     // one arrival per warp of the stage's group
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
     tc::mbar_init(lut_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
-    if (!kDx) {
-      tc::mbar_arrive_expect_tx(lut_bar, kPairLutBytes);
-      bulk_copy_g2s(tc::smem_addr(smem + kOffLut), &kPairLevels, kPairLutBytes, lut_bar);
-    }
+    tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
+    if (kDx) bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), &kHalfPairs, C::kLutBytes, lut_bar);
+    else bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), &kPairLevels, C::kLutBytes, lut_bar);
   }
   if (warp == 0 && lane == 0) {
     tc::prefetch_tensormap(&tm_act);
@@ -179,13 +196,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         if (!tc::mbar_wait(empty_bar(slot), ph ^ 1)) { fail(); break; }
         const int s = s_begin + i;
         tc::mbar_arrive_expect_tx(full_bar(slot), tx);
-        const uint32_t act = tc::smem_addr(smem + kOffAct + slot * kActStageBytes);
-        const uint32_t cod = tc::smem_addr(smem + kOffCodes + slot * kCodesStageBytes);
+        const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
+        const uint32_t cod = tc::smem_addr(smem + C::kOffCodes + slot * kCodesStageBytes);
         tc::tma_load_2d(act, &tm_act, s * 64, static_cast<int32_t>(m0), full_bar(slot));
         if (!kDx) {
+          // 128 rows x 32 bytes
           tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
         } else {
-          tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(r0 / 2), s * 64, full_bar(slot));
+          // four 16-byte x 64-row boxes, one per lane quarter: quarter c's
+          // 32 columns land as a dense [64 rows][16 B] block at c * 1 KB
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tc::tma_load_2d(cod + 1024u * c, &tm_codes, static_cast<int32_t>(r0 / 2 + 16 * c),
+                            s * 64, full_bar(slot));
         }
         ++issued;
       }
@@ -207,7 +230,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
         tc::fence_after_sync();
         const uint32_t a = tmem + kTmemA0 + 32u * slot;
-        const uint32_t b = tc::smem_addr(smem + kOffAct + slot * kActStageBytes);
+        const uint32_t b = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           tc::mma_bf16_tmem_a(tmem, a + 8u * j, tc::sw128_kmajor_desc(b + 32u * j), idesc,
@@ -220,14 +243,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
   } else {
     // ---------------------------------------------------- dequant + store --
-    const int q = warp & 3;             // TMEM lane quarter of this warp
-    const int grp = (warp - 2) >> 2;    // dequant group: takes stages i % 2 == grp
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int grp = (warp - 2) >> 2;        // takes the stages i % kGroups == grp
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const int gt = 32 * q + lane;       // thread index within the group (= TMEM lane)
+    // tile row (forward: weight row; input gradient: weight column) held by
+    // this thread's accumulator lane
+    int tile_row = 32 * q + lane;
     if (!kDx) {
-      const int64_t n = r0 + gt;        // this thread's weight row
+      const int64_t n = r0 + tile_row;      // this thread's weight row
       const bool vrow = n < p.N;
-      const uint8_t* pair_b = smem + kOffLut + lane * 8;
+      const uint8_t* pair_b = smem + C::kOffLut + lane * 8;
       uint32_t a8v = 0;
       float s2v = 0.0f;
       auto load_scale = [&](int i) {
@@ -239,11 +264,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       };
       load_scale(grp);
       if (!tc::mbar_wait(lut_bar, 0)) fail();
-      for (int i = grp; i < nst; i += 2) {
+      for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
         const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
-        load_scale(i + 2);
+        load_scale(i + kGroups);
         // warp-uniform: the stage is done by all lanes or by none (the
         // arrival below follows a __syncwarp)
         bool go = !*abort_flag;
@@ -252,7 +277,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           go = false;
         }
         if (!__all_sync(0xffffffffu, go)) continue;
-        const uint8_t* crow = smem + kOffCodes + slot * kCodesStageBytes + gt * 32;
+        const uint8_t* crow = smem + C::kOffCodes + slot * kCodesStageBytes + tile_row * 32;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const uint4 c = *reinterpret_cast<const uint4*>(crow + 16 * hf);
@@ -275,62 +300,84 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         if (lane == 0) tc::mbar_arrive(dq_bar(slot));
       }
     } else {
-      const int kl = gt;                // weight column within the tile
-      const int kbl = kl >> 6;          // its absmax block within the tile
-      const int sh = (kl & 1) ? 0 : 4;  // even column: high nibble
-      // Per stage, thread gt owns row gt >> 1 of block gt & 1 of the scaled
-      // level table: 16 levels times that row-block's dequantized absmax.
-      const int e_row = gt >> 1, e_blk = gt & 1;
-      const int64_t e_kb = (r0 >> 6) + e_blk;
-      uint32_t a8v = 0;
-      float s2v = 0.0f;
-      bool e_valid = false;
-      auto load_entry = [&](int i) {
+      // After the transpose below, lane t holds column 8 (t & 3) + (t >> 2)
+      // of the warp's 32, and byte b of its word the codes of rows 2b (high
+      // nibble) and 2b + 1 (low nibble) of an 8-row group. The three rounds
+      // swap 4-bit, 8-bit and 16-bit blocks with the lanes 4, 8 and 16 away;
+      // which half a lane keeps follows bit s of its row index (t >> 2) ^ 1.
+      const int rho = lane >> 2;
+      tile_row = 32 * q + 8 * (lane & 3) + rho;
+      const bool h0 = ((rho & 1) ^ 1) != 0;
+      const uint32_t keep0 = h0 ? 0xf0f0f0f0u : 0x0f0f0f0fu;
+      const uint32_t rot0 = h0 ? 28u : 4u;
+      const uint32_t sel1 = ((rho >> 1) & 1) ? 0x3715u : 0x6240u;
+      const uint32_t sel2 = ((rho >> 2) & 1) ? 0x3276u : 0x5410u;
+      // the warp's 32 columns share one absmax block per weight row
+      const int64_t kb = (r0 >> 6) + (q >> 1);
+      const bool kb_ok = kb < p.nblk;
+      float* ah = reinterpret_cast<float*>(smem + C::kOffAhat) + (warp - 2) * 64;
+      const uint8_t* tab = smem + C::kOffLut + 4 * lane;
+      const uint8_t* cq = smem + C::kOffCodes + q * 1024 + rho * 16 + (lane & 3) * 4;
+      uint32_t a8v[2] = {0u, 0u};
+      float s2v[2] = {0.0f, 0.0f};
+      bool rok[2] = {false, false};
+      // this lane computes the dequantized absmax of rows lane and lane + 32
+      auto load_scales = [&](int i) {
         if (i >= nst) return;
-        const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + e_row;
-        e_valid = (n < p.N) && (e_kb < p.nblk);
-        if (e_valid) {
-          const int64_t bi = n * p.nblk + e_kb;
-          a8v = p.a8[bi];
-          s2v = p.s2[bi >> 8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + lane + 32 * h;
+          rok[h] = kb_ok && n < p.N;
+          if (rok[h]) {
+            const int64_t bi = n * p.nblk + kb;
+            a8v[h] = p.a8[bi];
+            s2v[h] = p.s2[bi >> 8];
+          }
         }
       };
-      load_entry(grp);
-      for (int i = grp; i < nst; i += 2) {
+      load_scales(grp);
+      if (!tc::mbar_wait(lut_bar, 0)) fail();
+      for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        float* tab = reinterpret_cast<float*>(smem + kOffLut) + slot * (64 * 2 * kScaledEntry);
-        {
-          const float ahat = e_valid ? dequant_absmax(a8v, s2v) : 0.0f;
-          float4* dst = reinterpret_cast<float4*>(tab + (e_row * 2 + e_blk) * kScaledEntry);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(__fmul_rn(levels[4 * j], ahat), __fmul_rn(levels[4 * j + 1], ahat),
-                                 __fmul_rn(levels[4 * j + 2], ahat), __fmul_rn(levels[4 * j + 3], ahat));
-          load_entry(i + 2);
-        }
-        // the group's 128 threads meet here (named barrier 1 + group)
-        if (grp == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
-        else asm volatile("bar.sync 2, 128;" ::: "memory");
-        // warp-uniform: the stage is done by all lanes or by none (the
-        // arrival below follows a __syncwarp)
+        const float ah0 = rok[0] ? dequant_absmax(a8v[0], s2v[0]) : 0.0f;
+        const float ah1 = rok[1] ? dequant_absmax(a8v[1], s2v[1]) : 0.0f;
+        load_scales(i + kGroups);
+        __syncwarp();                       // last stage's reads of ah are done
+        ah[lane] = ah0;
+        ah[lane + 32] = ah1;
+        __syncwarp();
         bool go = !*abort_flag;
         if (go && !tc::mbar_wait(full_bar(slot), ph)) {
           fail();
           go = false;
         }
         if (!__all_sync(0xffffffffu, go)) continue;
-        const uint8_t* cs = smem + kOffCodes + slot * kCodesStageBytes + (kl >> 1);
-        const float* tb = tab + kbl * kScaledEntry;
+        const uint8_t* cw = cq + slot * kCodesStageBytes;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t v[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int rr = 32 * hf + 2 * jj;
-            const uint32_t b0 = cs[rr * 64], b1 = cs[(rr + 1) * 64];
-            v[jj] = pack_bf16x2(tb[rr * (2 * kScaledEntry) + ((b0 >> sh) & 15u)],
-                                tb[(rr + 1) * (2 * kScaledEntry) + ((b1 >> sh) & 15u)]);
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const int i8 = 4 * hf + g8;     // rows 8 i8 .. 8 i8 + 7
+            uint32_t x = *reinterpret_cast<const uint32_t*>(cw + 128 * i8);
+            uint32_t y = __shfl_xor_sync(0xffffffffu, x, 4);
+            x = (x & keep0) | (__funnelshift_l(y, y, rot0) & ~keep0);
+            y = __shfl_xor_sync(0xffffffffu, x, 8);
+            x = __byte_perm(x, y, sel1);
+            y = __shfl_xor_sync(0xffffffffu, x, 16);
+            x = __byte_perm(x, y, sel2);
+            const float4 sa = *reinterpret_cast<const float4*>(ah + 8 * i8);
+            const float4 sb = *reinterpret_cast<const float4*>(ah + 8 * i8 + 4);
+            const float2 sc[4] = {make_float2(sa.x, sa.y), make_float2(sa.z, sa.w),
+                                  make_float2(sb.x, sb.y), make_float2(sb.z, sb.w)};
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const uint32_t byte = __byte_perm(x, 0u, 0x4440u + b);
+              const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
+              const float2 lv = __fmul2_rn(__half22float2(h2), sc[b]);
+              v[4 * g8 + b] = pack_bf16x2(lv.x, lv.y);
+            }
           }
           tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
         }
@@ -341,15 +388,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       }
     }
 
-    // epilogue: accumulator lanes are tile rows, columns are tokens
+    // epilogue: accumulator lanes are tile rows, columns are tokens; the
+    // groups share out the 16-column chunks
     if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail();
     tc::fence_after_sync();
     if (!*abort_flag) {
-      const int64_t rg = r0 + 32 * q + lane;
+      const int64_t rg = r0 + tile_row;
       const int64_t nd = kDx ? p.K : p.N;
       const bool vrow = rg < nd;
-      const int half = p.bn / 2;
-      for (int c = grp * half; c < (grp + 1) * half; c += 16) {
+      for (int c = 16 * grp; c < p.bn; c += 16 * kGroups) {
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
         tc::tmem_wait_ld();
@@ -378,6 +425,7 @@ template <bool kDx>
 cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, const uint8_t* a8,
                       const float* s2, int64_t N, int64_t K, float* out, int num_sms, int* status,
                       cudaStream_t st) {
+  using C = Cfg<kDx>;
   TcArgs a;
   a.a8 = a8;
   a.s2 = s2;
@@ -410,15 +458,16 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
                  static_cast<uint32_t>(a.bn), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // packed codes: [N, K/2] bytes; the forward takes 32 B x 128 rows, the input
-  // gradient 64 B (128 columns) x 64 rows
+  // gradient 16 B (32 columns) x 64 rows per box
   if (!encode_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
-                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), kDx ? 64 : 32,
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), kDx ? 16 : 32,
                  kDx ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
 
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(tc_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(tc_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         C::kSmemBytes);
   });
   if (a.atomic_out) {
     cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(M) * nd * sizeof(float), st);
@@ -426,7 +475,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   }
   dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
             static_cast<unsigned>(splits));
-  tc_gemm_kernel<kDx><<<grid, kTcThreads, kSmemBytes, st>>>(tm_act, tm_codes, a);
+  tc_gemm_kernel<kDx><<<grid, C::kThreads, C::kSmemBytes, st>>>(tm_act, tm_codes, a);
   return cudaGetLastError();
 }
 

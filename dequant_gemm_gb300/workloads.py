@@ -69,6 +69,22 @@ class Workload:
     dy_std: float = 0.01
     notes: str = ""
     extra: dict = field(default_factory=dict)
+    # Projections that read the same input and can be issued together, in
+    # layer order; projections not named run alone.
+    concurrent: tuple = ()
+
+    def issue_groups(self):
+        """Projection indices grouped for issue, in order: each group's
+        matmuls are independent of one another."""
+        named = {i for g in self.concurrent for i in g}
+        out, seen = [], set()
+        for i in range(len(self.projections)):
+            if i in seen:
+                continue
+            g = next((tuple(g) for g in self.concurrent if i in g), (i,)) if i in named else (i,)
+            out.append(g)
+            seen.update(g)
+        return out
 
 
 QWEN_LAYER = tuple(
@@ -92,5 +108,7 @@ WORKLOADS = {
                                     (Projection("down", 4096, 11008, SEED_W),), dx_m=(2048,),
                                     dy_std=0.01),
     # Qwen2.5-7B-shaped decoder layer, all seven linear weights
-    "qwen2.5_7b_layer": Workload("qwen2.5_7b_layer", QWEN_LAYER, fwd_m=(1, 64, 2048), dx_m=(2048,)),
+    # (q, k, v share the layer input; gate and up share the MLP input)
+    "qwen2.5_7b_layer": Workload("qwen2.5_7b_layer", QWEN_LAYER, fwd_m=(1, 64, 2048), dx_m=(2048,),
+                                 concurrent=((0, 1, 2), (4, 5))),
 }
