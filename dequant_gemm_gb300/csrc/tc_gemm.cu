@@ -22,8 +22,9 @@
 //
 // Forward: the tile is 128 weight rows, one row per dequant thread, walked
 // along K. Both levels of a code byte come from one lookup in a 256-entry
-// fp32 pair table kept in 32 lane-private copies (every lookup of a warp hits
-// 32 distinct banks); the row's absmax scale is a register.
+// fp16 level pair table kept in 32 lane-private copies (every lookup of a
+// warp hits 32 distinct banks), are widened to fp32 and multiplied by the
+// row's dequantized absmax, a register.
 //
 // Input gradient: the tile is 128 weight columns walked along N (the
 // transposed walk), so a thread needs its column's nibbles down the stage's
@@ -31,10 +32,9 @@
 // of one row) and transposes 8 x 8 nibble blocks across lanes with three
 // shuffle rounds, after which a byte of a thread's word holds the codes of
 // two consecutive rows of its column: exactly one 32-bit tensor-memory word
-// of the A operand. That byte indexes a 256-entry fp16 level pair table (32
-// lane copies); the two levels are widened to fp32 and multiplied by their
-// rows' dequantized absmax, which the warp computes for its 64 rows and
-// broadcasts through shared memory.
+// of the A operand. That byte indexes the same pair table; the two levels
+// are multiplied by their rows' dequantized absmax, which the warp computes
+// for its 64 rows and broadcasts through shared memory.
 //
 // When the output tiles alone cannot fill the GPU the reduction is split
 // across CTAs and summed with atomics into a zeroed output.
@@ -57,16 +57,15 @@ constexpr int kActStageBytes = kMaxBN * 128; // 64 bf16 per token row
 constexpr int kCodesStageBytes = 4096;       // 128 x 64 nibbles
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA0 = 256;            // columns from 256 on: A-operand slots
-constexpr int kPairLutBytes = 256 * 32 * 8;  // forward: (c[hi], c[lo]) fp32 x 32 copies
 
 // Per-direction configuration and shared-memory layout.
 template <bool kDx>
 struct Cfg {
-  static constexpr int kGroups = kDx ? 3 : 2;        // dequant warp groups
+  static constexpr int kGroups = 3;                  // dequant warp groups
   static constexpr int kDqWarps = 4 * kGroups;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
-  static constexpr int kStages = 4;
-  static constexpr int kLutBytes = kDx ? kHalfPairTableBytes : kPairLutBytes;
+  static constexpr int kStages = 5;
+  static constexpr int kLutBytes = kHalfPairTableBytes;
   static constexpr int kAhatBytes = kDx ? kDqWarps * 64 * 4 : 0;   // per-warp row scales
   static constexpr int kOffAct = 0;
   static constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
@@ -93,27 +92,7 @@ struct TcArgs {
   int* status;
 };
 
-// Forward pair table: entry b (a code byte), copy l at float2 index 32 b + l
-// holds (c[b >> 4], c[b & 15]); a compile-time constant brought into shared
-// memory by one bulk copy per CTA.
-struct PairLevels {
-  uint32_t w[256 * 32 * 2];
-};
-
-constexpr PairLevels make_pair_levels() {
-  PairLevels t{};
-  for (int i = 0; i < 256 * 32; ++i) {
-    const int b = i >> 5;
-    t.w[2 * i] = kLevelBits[b >> 4];
-    t.w[2 * i + 1] = kLevelBits[b & 15];
-  }
-  return t;
-}
-
-__device__ __align__(128) const PairLevels kPairLevels = make_pair_levels();
-static_assert(sizeof(PairLevels) == kPairLutBytes, "pair table size");
-
-// Input-gradient pair table (fp16 levels, see common.cuh).
+// Level pair table of both directions (fp16 levels, layout in common.cuh).
 __device__ __align__(128) const HalfPairTable kHalfPairs = make_half_pair_table();
 
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -167,8 +146,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     *abort_flag = 0;
     tc::fence_barrier_init();
     tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
-    if (kDx) bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), &kHalfPairs, C::kLutBytes, lut_bar);
-    else bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), &kPairLevels, C::kLutBytes, lut_bar);
+    bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), &kHalfPairs, C::kLutBytes, lut_bar);
   }
   if (warp == 0 && lane == 0) {
     tc::prefetch_tensormap(&tm_act);
@@ -252,7 +230,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     if (!kDx) {
       const int64_t n = r0 + tile_row;      // this thread's weight row
       const bool vrow = n < p.N;
-      const uint8_t* pair_b = smem + C::kOffLut + lane * 8;
+      const uint8_t* tab = smem + C::kOffLut + 4 * lane;
       uint32_t a8v = 0;
       float s2v = 0.0f;
       auto load_scale = [&](int i) {
@@ -268,6 +246,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
         const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
+        const float2 ahat2 = make_float2(ahat, ahat);
         load_scale(i + kGroups);
         // warp-uniform: the stage is done by all lanes or by none (the
         // arrival below follows a __syncwarp)
@@ -287,9 +266,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-              const uint32_t byte = (words[j] >> (8 * b)) & 0xffu;
-              const float2 lv = *reinterpret_cast<const float2*>(pair_b + (byte << 8));
-              v[4 * j + b] = pack_bf16x2(__fmul_rn(lv.x, ahat), __fmul_rn(lv.y, ahat));
+              const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
+              const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
+              const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
+              v[4 * j + b] = pack_bf16x2(lv.x, lv.y);
             }
           }
           tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
