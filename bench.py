@@ -44,25 +44,32 @@ def traffic_per_launch(workload, category):
     """Mean DRAM bytes (read + write) per launch of a kernel class, from the
     committed ncu capture for this workload, or None when there is none or the
     CUDA sources changed since it was taken."""
-    import glob
-    import hashlib
     path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.txt")
     if not os.path.exists(path):
         return None
-    srcs = sorted(glob.glob(os.path.join(ROOT, "dequant_gemm_gb300", "csrc", "*.cu")) +
-                  glob.glob(os.path.join(ROOT, "dequant_gemm_gb300", "csrc", "*.cuh")))
-    h = hashlib.sha256(b"".join(open(p, "rb").read() for p in srcs)).hexdigest()
-    vals, stamp = [], None
+    vals, stamp, files = [], None, []
     for line in open(path):
         if line.startswith("# sources_sha256"):
-            stamp = line.split()[-1]
+            # "# sources_sha256 <digest> <file> ...": the files that define
+            # the captured kernel, relative to the CUDA source folder
+            f = line.split()
+            stamp, files = f[2], f[3:]
         elif line.strip() and not line.startswith("#"):
             f = line.split()
             if f[0] == category:
                 vals.append(int(f[2]) + int(f[3]))
-    if stamp != h or not vals:
+    if stamp is None or not files or not vals:
+        return None
+    if stamp != sources_digest(files):
         return None
     return sum(vals) / len(vals)
+
+
+def sources_digest(files):
+    """sha256 over the named CUDA source files, in the order given."""
+    import hashlib
+    d = os.path.join(ROOT, "dequant_gemm_gb300", "csrc")
+    return hashlib.sha256(b"".join(open(os.path.join(d, f), "rb").read() for f in files)).hexdigest()
 
 
 def peaks():

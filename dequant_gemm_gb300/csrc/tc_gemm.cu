@@ -198,23 +198,50 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
     if (lane == 0) {
+      // The dequant warps arrive on dq_bar only after they have seen the
+      // stage's copies land on full_bar, so its completion orders both the
+      // tensor-memory A operand and the shared-memory B tile before the MMAs;
+      // a failure elsewhere surfaces here as a timeout. The forward takes the
+      // stages in pairs: both waits first, then the two stages' MMAs back to
+      // back, each followed by the commit that frees its slot, so the tensor
+      // pipe sees one loop turn per pair (its dequant runs well ahead). The
+      // input gradient, whose dequant is the slower side, takes them singly.
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, static_cast<uint32_t>(p.bn));
-      for (int i = 0; i < nst && !*abort_flag; ++i) {
-        const int slot = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!tc::mbar_wait(dq_bar(slot), ph) || !tc::mbar_wait(full_bar(slot), ph)) {
+      const uint64_t bdesc0 = tc::sw128_kmajor_desc(tc::smem_addr(smem + C::kOffAct));
+      int slot = 0;
+      uint32_t ph = 0;
+      auto next = [&](int s, uint32_t f, int& s2, uint32_t& f2) {
+        s2 = s + 1 == kStages ? 0 : s + 1;
+        f2 = s + 1 == kStages ? f ^ 1u : f;
+      };
+      auto issue = [&](int i, int sl) {
+        const uint32_t a = tmem + kTmemA0 + 32u * sl;
+        // the descriptor's start-address field counts 16-byte units
+        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tc::mma_bf16_tmem_a(tmem, a + 8u * j, bdesc + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
+        tc::mma_commit(empty_bar(sl));
+      };
+      constexpr int kStep = kDx ? 1 : 2;
+      for (int i = 0; i < nst; i += kStep) {
+        const bool two = kStep == 2 && i + 1 < nst;
+        int slot1;
+        uint32_t ph1;
+        next(slot, ph, slot1, ph1);
+        if (!tc::mbar_wait(dq_bar(slot), ph) || (two && !tc::mbar_wait(dq_bar(slot1), ph1))) {
           fail();
           break;
         }
         tc::fence_after_sync();
-        const uint32_t a = tmem + kTmemA0 + 32u * slot;
-        const uint32_t b = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tc::mma_bf16_tmem_a(tmem, a + 8u * j, tc::sw128_kmajor_desc(b + 32u * j), idesc,
-                              (i | j) != 0 ? 1u : 0u);
+        issue(i, slot);
+        if (two) {
+          issue(i + 1, slot1);
+          next(slot1, ph1, slot, ph);
+        } else {
+          slot = slot1;
+          ph = ph1;
         }
-        tc::mma_commit(empty_bar(slot));
       }
       tc::mma_commit(accum_bar);
       if (!tc::mbar_wait(accum_bar, 0)) fail();   // all MMAs done before teardown
