@@ -468,9 +468,9 @@ def main():
     step.capture()
     for i in range(args.warmup):
         step.run()
-    status = nf4.nf4_poll_device_status(dev)
+    status, site = nf4.nf4_poll_device_status_site(dev)
     if status != 0:
-        raise SystemExit(f"device status {status} after warm-up")
+        raise SystemExit(f"device status {status} after warm-up ({nf4.describe_site(site)})")
 
     ngraphs = len(step.graphs)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ngraphs * args.steps)]
@@ -488,9 +488,9 @@ def main():
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    status = nf4.nf4_poll_device_status(dev)
+    status, site = nf4.nf4_poll_device_status_site(dev)
     if status != 0:
-        raise SystemExit(f"device status {status} after the timed steps")
+        raise SystemExit(f"device status {status} after the timed steps ({nf4.describe_site(site)})")
 
     # per-category device time from the per-call events
     cat_ms, cat_flop, cat_bytes, cat_n = {}, {}, {}, {}

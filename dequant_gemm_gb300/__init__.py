@@ -30,7 +30,8 @@ STATUS = {
 
 # Every symbol the header declares, for load checks.
 EXPORTS = ("nf4_quantize", "nf4_dequantize", "nf4_matmul_fwd", "nf4_matmul_bwd_dx",
-           "nf4_poll_device_status", "nf4_codebook", "nf4_status_string")
+           "nf4_poll_device_status", "nf4_poll_device_status_site", "nf4_codebook",
+           "nf4_status_string")
 
 
 class NF4Error(RuntimeError):
@@ -68,6 +69,7 @@ def lib() -> ctypes.CDLL:
                 "nf4_matmul_fwd": [vp, i64, W, vp, vp],
                 "nf4_matmul_bwd_dx": [vp, i64, W, vp, vp],
                 "nf4_poll_device_status": [vp],
+                "nf4_poll_device_status_site": [vp, vp],
                 "nf4_codebook": [vp],
             }
             for name, args in sig.items():
@@ -196,6 +198,27 @@ def nf4_poll_device_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(lib().nf4_poll_device_status(_stream(dev)))
+
+
+def nf4_poll_device_status_site(device=None) -> tuple[int, int]:
+    """As nf4_poll_device_status, plus where the first timeout happened:
+    (status, site), site = kernel << 28 | role << 24 | CTA index (0 if none)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    site = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        st = int(lib().nf4_poll_device_status_site(_stream(dev), ctypes.byref(site)))
+    return st, int(site.value)
+
+
+def describe_site(site: int) -> str:
+    """Readable form of a timeout site."""
+    if site == 0:
+        return "none"
+    kernel = {1: "small-M forward", 2: "tensor-core forward", 3: "tensor-core input gradient"}
+    role = {1: "copy producer", 2: "MMA issuer", 3: "dequantizing warp", 4: "epilogue"}
+    u = site & 0xffffffff
+    return (f"{kernel.get(u >> 28, u >> 28)}, {role.get((u >> 24) & 15, (u >> 24) & 15)}, "
+            f"CTA {u & 0xffffff}")
 
 
 def nf4_codebook() -> torch.Tensor:

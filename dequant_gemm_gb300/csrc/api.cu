@@ -9,7 +9,7 @@ namespace {
 
 // Device status word: kernels whose bounded waits run out record
 // NF4_ERR_DEVICE_TIMEOUT here; nf4_poll_device_status reads and clears it.
-__device__ int g_device_status;
+__device__ int g_device_status[2];   // status, site of the first timeout
 
 struct DeviceInfo {
   bool checked = false;
@@ -155,7 +155,8 @@ nf4_status nf4_matmul_bwd_dx(const uint16_t* dY, int64_t M, const nf4_weight* w,
                                     w->cols, dX, d->num_sms, d->status, st));
 }
 
-nf4_status nf4_poll_device_status(void* stream) {
+nf4_status nf4_poll_device_status_site(void* stream, int32_t* site) {
+  if (site) *site = 0;
   DeviceInfo* d = nullptr;
   if (nf4_status s = current_device(&d)) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -163,15 +164,20 @@ nf4_status nf4_poll_device_status(void* stream) {
     cudaGetLastError();
     return NF4_ERR_LAUNCH;
   }
-  int value = 0;
-  const int zero = 0;
-  if (cudaMemcpyAsync(&value, d->status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaMemcpyAsync(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+  int value[2] = {0, 0};
+  const int zero[2] = {0, 0};
+  if (cudaMemcpyAsync(value, d->status, sizeof(value), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(d->status, zero, sizeof(zero), cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess) {
     cudaGetLastError();
     return NF4_ERR_LAUNCH;
   }
-  return value == 0 ? NF4_OK : static_cast<nf4_status>(value);
+  if (site) *site = value[1];
+  return value[0] == 0 ? NF4_OK : static_cast<nf4_status>(value[0]);
+}
+
+nf4_status nf4_poll_device_status(void* stream) {
+  return nf4_poll_device_status_site(stream, nullptr);
 }
 
 nf4_status nf4_codebook(float* out16) {

@@ -77,6 +77,19 @@ struct HalfPairTable {
   uint32_t w[256 * 32];
 };
 
+// The 256 distinct entries of that table (one copy), for kernels that lay the
+// copies out themselves.
+struct HalfPairs {
+  uint32_t w[256];
+};
+
+constexpr HalfPairs make_half_pairs() {
+  HalfPairs t{};
+  for (int b = 0; b < 256; ++b)
+    t.w[b] = level_to_f16(kLevelBits[b >> 4]) | (level_to_f16(kLevelBits[b & 15]) << 16);
+  return t;
+}
+
 constexpr HalfPairTable make_half_pair_table() {
   HalfPairTable t{};
   for (int i = 0; i < 256 * 32; ++i) {
@@ -90,9 +103,19 @@ constexpr HalfPairTable make_half_pair_table() {
 constexpr int kStatusTimeout = NF4_ERR_DEVICE_TIMEOUT;
 
 // Record a device-side failure without trapping.
-__device__ inline void report_status(int* status, int code) {
-  if (status) atomicCAS(status, 0, code);
+// status[0] is the status word, status[1] the site of the first report:
+// (kernel << 28) | (role << 24) | (linear CTA index & 0xffffff).
+__device__ inline void report_status(int* status, int code, uint32_t kernel, uint32_t role) {
+  if (!status) return;
+  if (atomicCAS(status, 0, code) == 0) {
+    const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    atomicExch(status + 1, static_cast<int>((kernel << 28) | (role << 24) | (cta & 0xffffffu)));
+  }
 }
+
+// Kernel and role numbers of report_status (see nf4_poll_device_status_site).
+constexpr uint32_t kSiteGemv = 1, kSiteTcFwd = 2, kSiteTcDx = 3;
+constexpr uint32_t kRoleProducer = 1, kRoleMma = 2, kRoleCompute = 3, kRoleEpilogue = 4;
 
 // Second-level dequant: ahat = fl32(fl32(a8 * s2) / 255), both IEEE RN.
 __device__ __forceinline__ float dequant_absmax(uint32_t a8, float s2) {

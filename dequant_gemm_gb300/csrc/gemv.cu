@@ -26,9 +26,11 @@
 //    bf16 values), and the scale is removed from the fp32 result.
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
-//    that every lookup of a warp hits 32 distinct banks. The table is a
-//    compile-time constant in device memory, brought into shared memory by
-//    one bulk asynchronous copy per CTA.
+//    that every lookup of a warp hits 32 distinct banks. Each CTA lays the
+//    copies out itself from a 1 KB constant array (no 32 KB copy from L2).
+//  * Launched with programmatic stream serialization: the CTAs of the next
+//    kernel in the stream can be resident and do their set-up while this one
+//    drains; no global memory is touched before griddepcontrol.wait.
 //  * Within a block the 4 threads of an MMA quad each own 16 contiguous k
 //    (8 code bytes); the reduction order over k is permuted consistently in A
 //    and B, which leaves the sum unchanged.
@@ -47,7 +49,9 @@ constexpr int kMaxSliceBlocks = 48;
 constexpr int kMaxCluster = 8;
 constexpr int kOutStride = kGemvRows + 4;     // floats, keeps rows 16-byte aligned
 
-__device__ __align__(128) const HalfPairTable kPairTable = make_half_pair_table();
+// The level pairs, read with warp-uniform addresses while each CTA lays out
+// its 32 lane copies in shared memory.
+__constant__ HalfPairs kPairConst = make_half_pairs();
 
 // Not volatile: independent MMA chains of different blocks may interleave.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -69,15 +73,6 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -151,7 +146,6 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   float* ahat_s = reinterpret_cast<float*>(smem + gemv_off_ahat(p.ring));   // [128][max_nb]
   float* xinv = reinterpret_cast<float*>(smem + gemv_off_xinv(p.ring, p.max_nb));  // [64]
   const uint32_t bars = tc::smem_addr(smem + gemv_off_bars(p.ring, p.max_nb));
-  const uint32_t tab_bar = bars;
   auto full_bar = [&](int s) { return bars + 8u * (1 + s); };
   auto empty_bar = [&](int s) { return bars + 8u * (1 + kMaxRing + s); };
   const int xstride_b = p.max_nb * 128 + 8;  // bytes per token row of the fp16 slice
@@ -204,13 +198,21 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       sv[u] = okj ? __ldg(p.s2 + ((ah_bi0 + j) >> 8)) : 0.0f;
     }
   };
+  // Programmatic dependent launch: the next kernel in the stream may start its
+  // own set-up now; this one touches no global memory before the previous
+  // kernel has completed (griddepcontrol.wait).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // level table: entry e, copy l at word 32 e + l (one conflict-free store per
+  // entry and warp)
+  for (int e = warp; e < 256; e += kComputeWarps + 1) tab[e * 32 + lane] = kPairConst.w[e];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   if (warp < kComputeWarps) {
     load_x(0);
     load_ah(ah_par);
   }
 
   if (tid == 0) {
-    tc::mbar_init(tab_bar, 1);
     for (int s = 0; s < kMaxRing; ++s) {
       tc::mbar_init(full_bar(s), 1);
       tc::mbar_init(empty_bar(s), kComputeWarps);
@@ -230,7 +232,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     for (int b = issued; b < upto; ++b) {
       const int slot = b % nring;
       if (b >= nring && !tc::mbar_wait(empty_bar(slot), ((b / nring) - 1) & 1)) {
-        report_status(p.status, kStatusTimeout);
+        report_status(p.status, kStatusTimeout, kSiteGemv, kRoleProducer);
         return;
       }
       tc::mbar_arrive_expect_tx(full_bar(slot), kBoxBytes);
@@ -241,8 +243,6 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   };
   if (producer) {
     tc::prefetch_tensormap(&tm_codes);
-    tc::mbar_arrive_expect_tx(tab_bar, kTabBytes);
-    bulk_copy_g2s(tc::smem_addr(tab), &kPairTable, kTabBytes, tab_bar);
     issue_boxes(min(nboxes, nring));
   }
   if (warp < kComputeWarps) {
@@ -330,7 +330,6 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
   if (warp < kComputeWarps) {
-    ok = tc::mbar_wait(tab_bar, 0);
     const uint32_t tab_b = tc::smem_addr(tab) + lane * 4;   // this lane's copy of the table
     const uint32_t xs_a = tc::smem_addr(xs) + g * xstride_b + t * 32;
     const float* ah_g = ahat_s + (warp * 16 + g) * p.max_nb;
@@ -391,7 +390,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty_bar(slot));   // slot free for the producer
     }
-    if (!ok) report_status(p.status, kStatusTimeout);
+    if (!ok) report_status(p.status, kStatusTimeout, kSiteGemv, kRoleCompute);
   }
 
   // Epilogue: undo the token scales and stage this slice's partial
@@ -594,13 +593,15 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = static_cast<unsigned>(slices);
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return nt == 1 ? launch_gemv_nt<1>(cfg, tm, a) : launch_gemv_nt<2>(cfg, tm, a);
 }
 

@@ -158,8 +158,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  auto fail = [&]() {
-    report_status(p.status, kStatusTimeout);
+  auto fail = [&](uint32_t role) {
+    report_status(p.status, kStatusTimeout, kDx ? kSiteTcDx : kSiteTcFwd, role);
     *abort_flag = 1;
   };
 
@@ -171,7 +171,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       for (int i = 0; i < nst && !*abort_flag; ++i) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!tc::mbar_wait(empty_bar(slot), ph ^ 1)) { fail(); break; }
+        if (!tc::mbar_wait(empty_bar(slot), ph ^ 1)) { fail(kRoleProducer); break; }
         const int s = s_begin + i;
         tc::mbar_arrive_expect_tx(full_bar(slot), tx);
         const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
@@ -230,7 +230,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         uint32_t ph1;
         next(slot, ph, slot1, ph1);
         if (!tc::mbar_wait(dq_bar(slot), ph) || (two && !tc::mbar_wait(dq_bar(slot1), ph1))) {
-          fail();
+          fail(kRoleMma);
           break;
         }
         tc::fence_after_sync();
@@ -244,7 +244,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
       }
       tc::mma_commit(accum_bar);
-      if (!tc::mbar_wait(accum_bar, 0)) fail();   // all MMAs done before teardown
+      if (!tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);   // all MMAs done before teardown
     }
   } else {
     // ---------------------------------------------------- dequant + store --
@@ -268,7 +268,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
       };
       load_scale(grp);
-      if (!tc::mbar_wait(lut_bar, 0)) fail();
+      if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
       for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
@@ -279,7 +279,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         // arrival below follows a __syncwarp)
         bool go = !*abort_flag;
         if (go && !tc::mbar_wait(full_bar(slot), ph)) {
-          fail();
+          fail(kRoleCompute);
           go = false;
         }
         if (!__all_sync(0xffffffffu, go)) continue;
@@ -343,7 +343,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
       };
       load_scales(grp);
-      if (!tc::mbar_wait(lut_bar, 0)) fail();
+      if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
       for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
@@ -356,7 +356,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         __syncwarp();
         bool go = !*abort_flag;
         if (go && !tc::mbar_wait(full_bar(slot), ph)) {
-          fail();
+          fail(kRoleCompute);
           go = false;
         }
         if (!__all_sync(0xffffffffu, go)) continue;
@@ -397,7 +397,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 
     // epilogue: accumulator lanes are tile rows, columns are tokens; the
     // groups share out the 16-column chunks
-    if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail();
+    if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail(kRoleEpilogue);
     tc::fence_after_sync();
     if (!*abort_flag) {
       const int64_t rg = r0 + tile_row;

@@ -125,6 +125,16 @@ nf4_status nf4_matmul_bwd_dx(const uint16_t* dY, int64_t M, const nf4_weight* w,
  * NF4_OK otherwise. */
 nf4_status nf4_poll_device_status(void* stream);
 
+/* As nf4_poll_device_status, and if `site` is not NULL it receives where the
+ * first timeout since the last poll happened (0 when there was none):
+ *   bits 28-31  kernel: 1 small-M forward, 2 tensor-core forward,
+ *               3 tensor-core input gradient
+ *   bits 24-27  role: 1 copy producer, 2 MMA issuer, 3 dequantizing /
+ *               computing warp, 4 epilogue
+ *   bits  0-23  linear index of the CTA within its grid (low 24 bits).
+ * Diagnostic only; the status value is the same. */
+nf4_status nf4_poll_device_status_site(void* stream, int32_t* site);
+
 /* Host-only: copies the 16 fp32 NF4 levels compiled into the library into
  * out16 (host memory). Needs no device. */
 nf4_status nf4_codebook(float* out16);

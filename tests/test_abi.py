@@ -99,3 +99,11 @@ def test_valid_call_without_device_reports_device_error():
     w = _weight(codes=P, a8=P, s2=P)
     assert L.nf4_quantize(P, 8, 64, 64, P, P, P, None) == 5
     assert L.nf4_matmul_fwd(P, 4, ctypes.byref(w), P, None) == 5
+
+
+def test_timeout_site_description():
+    # kernel << 28 | role << 24 | CTA index, as the device records it
+    assert nf4.describe_site(0) == "none"
+    assert nf4.describe_site((3 << 28) | (2 << 24) | 77) == "tensor-core input gradient, MMA issuer, CTA 77"
+    assert nf4.describe_site((1 << 28) | (1 << 24)) == "small-M forward, copy producer, CTA 0"
+    assert nf4.describe_site(-((1 << 32) - ((2 << 28) | (4 << 24) | 5))) == "tensor-core forward, epilogue, CTA 5"

@@ -268,7 +268,7 @@ def test_fwd_output_guard_bytes():
         torch.cuda.synchronize()
         assert torch.all(buf[:32] == 123.0) and torch.all(buf[32 + n:] == 123.0)
         assert torch.all(dbuf[:32] == 321.0) and torch.all(dbuf[32 + M * 256:] == 321.0)
-    assert nf4.nf4_poll_device_status() == 0
+    assert nf4.nf4_poll_device_status_site() == (0, 0)
 
 
 def test_non_default_stream():
