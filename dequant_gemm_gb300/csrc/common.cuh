@@ -77,19 +77,6 @@ struct HalfPairTable {
   uint32_t w[256 * 32];
 };
 
-// The 256 distinct entries of that table (one copy), for kernels that lay the
-// copies out themselves.
-struct HalfPairs {
-  uint32_t w[256];
-};
-
-constexpr HalfPairs make_half_pairs() {
-  HalfPairs t{};
-  for (int b = 0; b < 256; ++b)
-    t.w[b] = level_to_f16(kLevelBits[b >> 4]) | (level_to_f16(kLevelBits[b & 15]) << 16);
-  return t;
-}
-
 constexpr HalfPairTable make_half_pair_table() {
   HalfPairTable t{};
   for (int i = 0; i < 256 * 32; ++i) {

@@ -4,15 +4,18 @@
 // dequantized on chip; the full-precision weight never reaches HBM).
 //
 // Forward design (HBM-bound: 0.516 B of weight per 2*M flops):
-//  * CTA = 8 warps = 128 weight rows (16 per warp) x one K-slice. The S
-//    K-slices of the same rows form a thread-block cluster and reduce their
-//    partial sums through distributed shared memory, so every output is
-//    written once with a plain store (no zeroing pass, no atomics).
-//  * A producer warp streams the CTA's packed codes with 2-D TMA boxes of
-//    128 rows x 128 bytes (four absmax blocks), 128-byte swizzled, through a
-//    ring of four shared-memory slots; the eight compute warps read them
-//    bank-conflict free. The absmax codes, scales and activations of the
-//    prologue are loaded with all requests issued before any is used.
+//  * CTA = 16 warps = 8 row groups of 16 weight rows (128 rows) x 2 halves of
+//    one K-slice. The two warps of a row group reduce through shared memory;
+//    the S K-slices of the same rows form a thread-block cluster and reduce
+//    through distributed shared memory, so every output is written once with
+//    a plain store (no zeroing pass, no atomics). The number of slices keeps
+//    the grid within one wave of two CTAs per SM.
+//  * Every warp streams its own codes: lane 0 issues 2-D TMA boxes of 16 rows
+//    x 128 bytes (four 64-weight blocks, 128-byte swizzled) into two private
+//    shared-memory slots with one mbarrier each, so warps never wait for one
+//    another in the main loop, and the copies travel apart from the ordinary
+//    loads of the prologue (activations, absmax codes, scales), which thus do
+//    not queue behind the weight stream.
 //  * The weight is the A operand of mma.sync.m16n8k16 (16 rows per warp), the
 //    tokens are the N operand (8 per n-tile, one or two n-tiles): the "swap AB"
 //    shape for skinny products. Each weight is dequantized once per CTA for
@@ -27,13 +30,13 @@
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
 //    that every lookup of a warp hits 32 distinct banks. Each CTA lays the
-//    copies out itself from a 1 KB constant array (no 32 KB copy from L2).
-//  * Launched with programmatic stream serialization: the CTAs of the next
-//    kernel in the stream can be resident and do their set-up while this one
-//    drains; no global memory is touched before griddepcontrol.wait.
+//    copies out itself, by shuffles from levels held in registers.
 //  * Within a block the 4 threads of an MMA quad each own 16 contiguous k
 //    (8 code bytes); the reduction order over k is permuted consistently in A
 //    and B, which leaves the sum unchanged.
+//  * Launched with programmatic stream serialization: the CTAs of the next
+//    kernel in the stream can be resident and do their set-up while this one
+//    drains; no global memory is touched before griddepcontrol.wait.
 #include <algorithm>
 #include <mutex>
 
@@ -43,15 +46,29 @@
 namespace nf4 {
 namespace {
 
-constexpr int kGemvRows = 128;
+constexpr int kGemvRows = 128;                  // weight rows per CTA
+constexpr int kRowGroups = 8;                   // 16 rows each
+constexpr int kGemvWarps = 2 * kRowGroups;      // two K-halves per row group
+constexpr int kGemvThreads = 32 * kGemvWarps;
+constexpr int kBoxBlocks = 4;                   // 64-weight blocks per code box
+constexpr int kBoxBytes = 16 * 128;             // 16 rows x 128 bytes
+constexpr int kWarpSlots = 2;                   // code boxes in flight per warp
 constexpr int kTabBytes = kHalfPairTableBytes;
-constexpr int kMaxSliceBlocks = 48;
+constexpr int kMaxSliceBlocks = 96;
 constexpr int kMaxCluster = 8;
-constexpr int kOutStride = kGemvRows + 4;     // floats, keeps rows 16-byte aligned
+constexpr int kOutStride = kGemvRows + 4;       // floats, keeps rows 16-byte aligned
 
-// The level pairs, read with warp-uniform addresses while each CTA lays out
-// its 32 lane copies in shared memory.
-__constant__ HalfPairs kPairConst = make_half_pairs();
+// fp16 bits of level i (0 <= i < 16) as a select tree over immediates: no
+// memory access, so the table set-up does not wait on a constant-cache miss.
+template <int kLo, int kN>
+__device__ __forceinline__ uint32_t level_f16(int i) {
+  if constexpr (kN == 1) {
+    return level_to_f16(kLevelBits[kLo]);
+  } else {
+    const uint32_t lo = level_f16<kLo, kN / 2>(i), hi = level_f16<kLo + kN / 2, kN / 2>(i);
+    return (i & (kN / 2)) ? hi : lo;
+  }
+}
 
 // Not volatile: independent MMA chains of different blocks may interleave.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -61,18 +78,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -103,7 +108,6 @@ struct GemvArgs {
   int nblk;              // K / 64
   int slices;            // K-slices = cluster size along y
   int max_nb;            // largest slice, in blocks
-  int ring;              // code-box slots (1..kMaxRing)
   int* status;
 };
 
@@ -112,49 +116,37 @@ __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
   return (nblk * s) / slices;
 }
 
-constexpr int kComputeWarps = 8;
-constexpr int kGemvThreads = 32 * (kComputeWarps + 1);   // + one TMA producer warp
-constexpr int kMaxRing = 4;                 // code boxes in flight, at most
-constexpr int kBoxBlocks = 4;               // absmax blocks per box (128 B of codes per row)
-constexpr int kBoxBytes = kGemvRows * 128;  // 16 KB: 128 rows x 128 B
-
 // Shared memory (offsets from a 1024-byte aligned base): level table, code
-// ring, absmax table, token scales, mbarriers, fp16 activation slice.
-constexpr int kOffRing = kTabBytes;
-__host__ __device__ constexpr int gemv_off_ahat(int ring) { return kOffRing + ring * kBoxBytes; }
-__host__ __device__ constexpr int gemv_off_xinv(int ring, int max_nb) {
-  return gemv_off_ahat(ring) + kGemvRows * max_nb * 4;
-}
-__host__ __device__ constexpr int gemv_off_bars(int ring, int max_nb) {
-  return gemv_off_xinv(ring, max_nb) + 64 * 4;
-}
-__host__ __device__ constexpr int gemv_off_xs(int ring, int max_nb) {
-  return gemv_off_bars(ring, max_nb) + (1 + 2 * kMaxRing) * 8 + 8;
-}
-// Inbox of the cluster reduction: [slices][8 NT tokens][128 / slices rows].
-__host__ __device__ constexpr int gemv_off_inbox(int ring, int max_nb, int nt) {
-  return (gemv_off_xs(ring, max_nb) + 8 * nt * (max_nb * 128 + 8) + 15) & ~15;
-}
+// slots (per warp, 1024-byte aligned for the swizzle), mbarriers, the
+// dequantized absmax of each slot's row pairs (g, g + 8), token scales, the
+// K-half reduction buffer, the cluster reduction inbox and the fp16
+// activation slice (rows of max_nb * 128 + 8 bytes: the 8 keeps the B
+// fragment loads of 8 token rows on distinct banks).
+constexpr int kOffSlots = kTabBytes;
+constexpr int kOffBars = kOffSlots + kGemvWarps * kWarpSlots * kBoxBytes;
+constexpr int kOffAhw = kOffBars + kGemvWarps * kWarpSlots * 8;
+constexpr int kOffXinv = kOffAhw + kGemvWarps * kWarpSlots * 32 * 8;
+constexpr int kOffRed = kOffXinv + 16 * 4;
+__host__ __device__ constexpr int gemv_off_inbox(int nt) { return kOffRed + kRowGroups * 32 * 4 * nt * 4; }
+__host__ __device__ constexpr int gemv_off_xs(int nt) { return gemv_off_inbox(nt) + 8 * nt * kGemvRows * 4; }
+__host__ __device__ constexpr int gemv_xstride(int max_nb) { return max_nb * 128 + 8; }
 
 template <int NT>
-__global__ void __launch_bounds__(kGemvThreads)
+__global__ void __launch_bounds__(kGemvThreads, 2)
 gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
-  float* ahat_s = reinterpret_cast<float*>(smem + gemv_off_ahat(p.ring));   // [128][max_nb]
-  float* xinv = reinterpret_cast<float*>(smem + gemv_off_xinv(p.ring, p.max_nb));  // [64]
-  const uint32_t bars = tc::smem_addr(smem + gemv_off_bars(p.ring, p.max_nb));
-  auto full_bar = [&](int s) { return bars + 8u * (1 + s); };
-  auto empty_bar = [&](int s) { return bars + 8u * (1 + kMaxRing + s); };
-  const int xstride_b = p.max_nb * 128 + 8;  // bytes per token row of the fp16 slice
-  uint8_t* xs = smem + gemv_off_xs(p.ring, p.max_nb);
-  const int nring = p.ring;
-  const uint32_t ring = tc::smem_addr(smem + kOffRing);
+  float* xinv = reinterpret_cast<float*>(smem + kOffXinv);    // [16]
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* inbox = reinterpret_cast<float*>(smem + gemv_off_inbox(NT));
+  uint8_t* xs = smem + gemv_off_xs(NT);
+  const int xstride = gemv_xstride(p.max_nb);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
+  const int rgp = warp & (kRowGroups - 1), kh = warp / kRowGroups;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kGemvRows;
   const int slice = blockIdx.y;
   const int kb0 = slice_begin(p.nblk, p.slices, slice);
@@ -162,239 +154,217 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   const int nboxes = (nb + kBoxBlocks - 1) / kBoxBlocks;
   const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
   const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
+  // this warp's code slots and their mbarriers; it takes boxes kh, kh + 2, ...
+  const uint32_t slots = tc::smem_addr(smem + kOffSlots) + warp * kWarpSlots * kBoxBytes;
+  const uint32_t bars = tc::smem_addr(smem + kOffBars) + warp * kWarpSlots * 8;
+  float2* ahw = reinterpret_cast<float2*>(smem + kOffAhw) + warp * kWarpSlots * 32;
 
-  // The prologue's own loads (activations, absmax codes, scales) are issued
-  // before the producer starts streaming the code tile, so that they do not
-  // queue behind it; the main loop then overlaps the stream.
-  const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
-  const uint2* xbase = reinterpret_cast<const uint2*>(p.X + m0 * p.K +
-                                                      static_cast<int64_t>(kb0) * kBlock);
-  const int64_t xrow4 = p.K / 4;
-  uint2 xv[NT][4];
-  auto load_x = [&](int c0) {
-#pragma unroll
-    for (int u = 0; u < NT; ++u) {
-      const int tk = warp + 8 * u;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = c0 + lane + 32 * c;
-        xv[u][c] = (tk < mt && i < nkv4) ? __ldg(xbase + tk * xrow4 + i) : make_uint2(0u, 0u);
-      }
-    }
-  };
-  // dequantized absmax: thread t owns row t / 2 and every other block of it
-  constexpr int kAh = 4;
-  const int ah_r = tid >> 1, ah_par = tid & 1;
-  const bool ah_vrow = warp < kComputeWarps && row0 + ah_r < p.N;
-  const int64_t ah_bi0 = (row0 + ah_r) * p.nblk + kb0;
-  uint32_t av[kAh];
-  float sv[kAh];
-  auto load_ah = [&](int j0) {
-#pragma unroll
-    for (int u = 0; u < kAh; ++u) {
-      const int j = j0 + 2 * u;
-      const bool okj = ah_vrow && j < nb;
-      av[u] = okj ? static_cast<uint32_t>(__ldg(p.a8 + ah_bi0 + j)) : 0u;
-      sv[u] = okj ? __ldg(p.s2 + ((ah_bi0 + j) >> 8)) : 0.0f;
-    }
-  };
   // Programmatic dependent launch: the next kernel in the stream may start its
   // own set-up now; this one touches no global memory before the previous
   // kernel has completed (griddepcontrol.wait).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // level table: entry e, copy l at word 32 e + l (one conflict-free store per
-  // entry and warp)
-  for (int e = warp; e < 256; e += kComputeWarps + 1) tab[e * 32 + lane] = kPairConst.w[e];
+  // entry and warp); lane l holds level l & 15, entries come by shuffles
+  {
+    const uint32_t lev = level_f16<0, 16>(lane & 15);
+    for (int e = warp; e < 256; e += kGemvWarps) {
+      const uint32_t hi = __shfl_sync(0xffffffffu, lev, e >> 4);
+      const uint32_t lo = __shfl_sync(0xffffffffu, lev, e & 15);
+      tab[e * 32 + lane] = hi | (lo << 16);
+    }
+  }
+  if (lane == 0) {
+    for (int s = 0; s < kWarpSlots; ++s) tc::mbar_init(bars + 8u * s, 1);
+    tc::fence_barrier_init();
+    tc::prefetch_tensormap(&tm_codes);
+  }
+  __syncwarp();
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  if (warp < kComputeWarps) {
-    load_x(0);
-    load_ah(ah_par);
-  }
-
-  if (tid == 0) {
-    for (int s = 0; s < kMaxRing; ++s) {
-      tc::mbar_init(full_bar(s), 1);
-      tc::mbar_init(empty_bar(s), kComputeWarps);
+  // Activations first, ahead of the code stream: warp w copies token w of
+  // the tile, as bf16, into its staging row and takes its max |x| on the way
+  // (one global round trip); the conversion to fp16 happens in place below.
+  auto to_f2 = [](uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  };
+  auto amax4 = [&](uint2 v) {
+    const float2 f0 = to_f2(v.x), f1 = to_f2(v.y);
+    return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+  };
+  const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
+  uint2* xo = reinterpret_cast<uint2*>(xs + warp * xstride);
+  float xmax = 0.0f;
+  if (warp < mt) {
+    const uint2* xrow = reinterpret_cast<const uint2*>(p.X + (m0 + warp) * p.K +
+                                                       static_cast<int64_t>(kb0) * kBlock);
+#pragma unroll 8
+    for (int i = lane; i < nkv4; i += 32) {
+      const uint2 v = __ldg(xrow + i);
+      xo[i] = v;
+      xmax = fmaxf(xmax, amax4(v));
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
 
-  bool ok = true;
-  // Producer (lane 0 of the last warp): level table and code boxes (128 rows
-  // x 4 blocks each, 128-byte swizzled) through a ring of `nring` slots. The
-  // first ring-full goes out before the prologue barrier; the rest, which
-  // waits for slots to free, after it.
-  const bool producer = warp == kComputeWarps && lane == 0;
-  int issued = 0;
-  auto issue_boxes = [&](int upto) {
-    for (int b = issued; b < upto; ++b) {
-      const int slot = b % nring;
-      if (b >= nring && !tc::mbar_wait(empty_bar(slot), ((b / nring) - 1) & 1)) {
-        report_status(p.status, kStatusTimeout, kSiteGemv, kRoleProducer);
-        return;
-      }
-      tc::mbar_arrive_expect_tx(full_bar(slot), kBoxBytes);
-      tc::tma_load_2d(ring + slot * kBoxBytes, &tm_codes, (kb0 + kBoxBlocks * b) * 32,
-                      static_cast<int32_t>(row0), full_bar(slot));
-      issued = b + 1;
+  // Box i of this warp (the slice's box kh + 2 i) goes into slot i % 2, by
+  // TMA; its absmax codes and scales travel alongside: lane e loads those of
+  // row pair (e & 7, (e & 7) + 8) of block e >> 3 of the box.
+  const int nmine = (nboxes - kh + 1) / 2;   // boxes of this warp
+  const int64_t ar = row0 + rgp * 16 + (lane & 7);
+  const bool ar_ok = ar < p.N, br_ok = ar + 8 < p.N;
+  auto issue_box = [&](int i) {
+    if (lane == 0) {
+      const int b = kh + 2 * i;
+      const uint32_t bar = bars + 8u * (i % kWarpSlots);
+      tc::mbar_arrive_expect_tx(bar, kBoxBytes);
+      tc::tma_load_2d(slots + (i % kWarpSlots) * kBoxBytes, &tm_codes,
+                      (kb0 + kBoxBlocks * b) * 32, static_cast<int32_t>(row0 + rgp * 16), bar);
     }
   };
-  if (producer) {
-    tc::prefetch_tensormap(&tm_codes);
-    issue_boxes(min(nboxes, nring));
-  }
-  if (warp < kComputeWarps) {
-    // Dequantized absmax (batches of kAh blocks; the first one is in flight).
-    {
-      float* arow = ahat_s + ah_r * p.max_nb;
-      for (int j0 = ah_par; j0 < nb; j0 += 2 * kAh) {
-        if (j0 != ah_par) load_ah(j0);
-#pragma unroll
-        for (int u = 0; u < kAh; ++u) {
-          const int j = j0 + 2 * u;
-          if (j < nb) arow[j] = dequant_absmax(av[u], sv[u]);
-        }
-      }
-    }
+  auto load_scales = [&](int i, uint32_t& qa, uint32_t& qb, float& sa, float& sb) {
+    const int j = (kh + 2 * i) * kBoxBlocks + (lane >> 3);
+    const bool in = i < nmine && j < nb;
+    const int64_t ia = ar * p.nblk + kb0 + j, ib = ia + 8 * p.nblk;
+    qa = (in && ar_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ia)) : 0u;
+    qb = (in && br_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ib)) : 0u;
+    sa = (in && ar_ok) ? __ldg(p.s2 + (ia >> 8)) : 0.0f;
+    sb = (in && br_ok) ? __ldg(p.s2 + (ib >> 8)) : 0.0f;
+  };
+  uint32_t qa0, qb0, qa1, qb1;
+  float sa0, sb0, sa1, sb1;
+  load_scales(0, qa0, qb0, sa0, sb0);
+  load_scales(1, qa1, qb1, sa1, sb1);
+  if (nmine > 0) issue_box(0);
+  if (nmine > 1) issue_box(1);
 
-    // Activations: warp w stages tokens w + 8u (u < NT) in chunks of 128 uint2
-    // (8 blocks; the first one is in flight): per-token max |x| -> power-of-two
-    // scale into [2^14, 2^15) -> fp16. A slice of at most 8 blocks is converted
-    // straight from registers, longer slices are read a second time.
-    {
-      auto absmax4 = [](uint2 v) {
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-        return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-      };
-      auto convert = [](uint2 v, float scale) {
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-        const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
-        const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
-        return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-      };
-      float mx[NT];
+  // max |x| over the slice -> power-of-two scale into [2^14, 2^15) -> fp16
+  // (exact for bf16 inputs)
+  if (warp < mt) {
+    float mx = xmax;
 #pragma unroll
-      for (int u = 0; u < NT; ++u) mx[u] = 0.0f;
-      for (int c0 = 0; c0 < nkv4; c0 += 128) {
-        if (c0 > 0) load_x(c0);
-#pragma unroll
-        for (int u = 0; u < NT; ++u)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) mx[u] = fmaxf(mx[u], absmax4(xv[u][c]));
-      }
-      float scale[NT];
-#pragma unroll
-      for (int u = 0; u < NT; ++u) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-          mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], off));
-        int e = 0;
-        if (mx[u] > 0.0f) {
-          const int E = max(1, static_cast<int>((__float_as_uint(mx[u]) >> 23) & 0xffu));
-          e = min(141 - E, 126);
-        }
-        scale[u] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-        if (lane == 0) xinv[warp + 8 * u] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-      }
-      for (int c0 = 0; c0 < nkv4; c0 += 128) {
-        if (nkv4 > 128) load_x(c0);
-#pragma unroll
-        for (int u = 0; u < NT; ++u) {
-          const int tk = warp + 8 * u;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int i = c0 + lane + 32 * c;
-            if (tk < mt && i < nkv4)
-              reinterpret_cast<uint2*>(xs + tk * xstride_b)[i] = convert(xv[u][c], scale[u]);
-          }
-        }
-      }
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    int e = 0;
+    if (mx > 0.0f) {
+      const int E = max(1, static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu));
+      e = min(141 - E, 126);
     }
+    const float scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    if (lane == 0) xinv[warp] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    auto convert = [&](uint2 v) {
+      const float2 f0 = to_f2(v.x), f1 = to_f2(v.y);
+      const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
+      const __half2 h1 = __floats2half2_rn(f1.x * scale, f1.y * scale);
+      return make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                        *reinterpret_cast<const uint32_t*>(&h1));
+    };
+    for (int i = lane; i < nkv4; i += 32) xo[i] = convert(xo[i]);   // each lane its own entries
   }
   __syncthreads();
-  if (producer) {
-    issue_boxes(nboxes);
-    // copies still in flight land before the CTA may exit
-    for (int b = max(0, issued - nring); b < issued; ++b)
-      tc::mbar_wait(full_bar(b % nring), (b / nring) & 1);
-  }
 
+  // Main loop: per block, 16 lookups and 4 MMA k-steps per n-tile, then the
+  // block's partial sums scaled by the rows' dequantized absmax.
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-
-  if (warp < kComputeWarps) {
-    const uint32_t tab_b = tc::smem_addr(tab) + lane * 4;   // this lane's copy of the table
-    const uint32_t xs_a = tc::smem_addr(xs) + g * xstride_b + t * 32;
-    const float* ah_g = ahat_s + (warp * 16 + g) * p.max_nb;
-    const float* ah_g8 = ah_g + 8 * p.max_nb;
-    // swizzled offsets of this lane's 8 code bytes in rows g and g + 8 of the
-    // warp: 16-byte chunk c of a box row r sits at chunk c ^ (r & 7)
-    const uint32_t row_a = ring + (warp * 16 + g) * 128 + (t & 1) * 8;
-    const uint32_t row_b = row_a + 8 * 128;
-    bool tok_ok[NT];
+  const uint8_t* tabl = smem + lane * 4;                 // this lane's table copy
+  const uint8_t* xsl = xs + g * xstride + t * 32;        // token g, this lane's 16 k
+  bool tok_ok[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < mt;
-
-    for (int b = 0; b < nboxes && ok; ++b) {
-      const int slot = b % nring;
-      if (!tc::mbar_wait(full_bar(slot), (b / nring) & 1)) {
-        ok = false;
-        break;
-      }
+  for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < mt;
+  auto lut = [&](uint32_t w, int b) {
+    return *reinterpret_cast<const uint32_t*>(tabl + (__byte_perm(w, 0u, 0x4440u + b) << 7));
+  };
+  // rows g and g + 8 of the box; 16-byte chunk c of row r sits at c ^ (r & 7)
+  const uint8_t* slot_g = smem + kOffSlots + warp * kWarpSlots * kBoxBytes + g * 128 + (t & 1) * 8;
+  bool ok = true;
+  int waited = 0;
+  // one box: its scales into the warp's slot buffer, then its four blocks
+  auto do_box = [&](int i, uint32_t qa, uint32_t qb, float sa, float sb) {
+    const int sl = i % kWarpSlots;
+    ahw[sl * 32 + lane] = make_float2(dequant_absmax(qa, sa), dequant_absmax(qb, sb));
+    // warp-uniform outcome: the lanes leave together or go on together
+    const bool got = tc::mbar_wait(bars + 8u * sl, (i / kWarpSlots) & 1);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, got)) return false;
+    const int b = kh + 2 * i;
+    const uint8_t* sg = slot_g + sl * kBoxBytes;
 #pragma unroll
-      for (int jj = 0; jj < kBoxBlocks; ++jj) {
-        const int j = b * kBoxBlocks + jj;
-        if (j < nb) {
-          const uint32_t chunk = static_cast<uint32_t>((2 * jj + (t >> 1)) ^ g) << 4;
-          const uint2 cg = lds64(row_a + slot * kBoxBytes + chunk);
-          const uint2 cg8 = lds64(row_b + slot * kBoxBytes + chunk);
-          float part[NT][4];
+    for (int jj = 0; jj < kBoxBlocks; ++jj) {
+      const int j = b * kBoxBlocks + jj;
+      if (j < nb) {
+        const int chunk = ((2 * jj + (t >> 1)) ^ g) << 4;
+        const uint2 wa = *reinterpret_cast<const uint2*>(sg + chunk);
+        const uint2 wb = *reinterpret_cast<const uint2*>(sg + 8 * 128 + chunk);
+        float part[NT][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) part[nt][i] = 0.0f;
+          for (int q = 0; q < 4; ++q) part[nt][q] = 0.0f;
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint32_t wg = (s < 2) ? cg.x : cg.y;
-            const uint32_t wg8 = (s < 2) ? cg8.x : cg8.y;
-            const int sh = 16 * (s & 1);
-            // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
-            const uint32_t a0 = lds32(tab_b + (((wg >> sh) & 0xffu) << 7));
-            const uint32_t a2 = lds32(tab_b + (((wg >> (sh + 8)) & 0xffu) << 7));
-            const uint32_t a1 = lds32(tab_b + (((wg8 >> sh) & 0xffu) << 7));
-            const uint32_t a3 = lds32(tab_b + (((wg8 >> (sh + 8)) & 0xffu) << 7));
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              uint2 bx = make_uint2(0u, 0u);
-              if (tok_ok[nt]) bx = lds64(xs_a + nt * 8 * xstride_b + j * 128 + 8 * s);
-              mma_f16(part[nt], a0, a1, a2, a3, bx.x, bx.y);
-            }
-          }
-          const float ag = ah_g[j], ag8 = ah_g8[j];
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t xa = s < 2 ? wa.x : wa.y, xb = s < 2 ? wb.x : wb.y;
+          const int bs = 2 * (s & 1);
+          // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
+          const uint32_t a0 = lut(xa, bs), a2 = lut(xa, bs + 1);
+          const uint32_t a1 = lut(xb, bs), a3 = lut(xb, bs + 1);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            acc[nt][0] = fmaf(ag, part[nt][0], acc[nt][0]);
-            acc[nt][1] = fmaf(ag, part[nt][1], acc[nt][1]);
-            acc[nt][2] = fmaf(ag8, part[nt][2], acc[nt][2]);
-            acc[nt][3] = fmaf(ag8, part[nt][3], acc[nt][3]);
+            uint2 bx = make_uint2(0u, 0u);
+            if (tok_ok[nt])
+              bx = *reinterpret_cast<const uint2*>(xsl + nt * 8 * xstride + j * 128 + 8 * s);
+            mma_f16(part[nt], a0, a1, a2, a3, bx.x, bx.y);
           }
         }
+        const float2 ah = ahw[sl * 32 + jj * 8 + g];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[nt][0] = fmaf(ah.x, part[nt][0], acc[nt][0]);
+          acc[nt][1] = fmaf(ah.x, part[nt][1], acc[nt][1]);
+          acc[nt][2] = fmaf(ah.y, part[nt][2], acc[nt][2]);
+          acc[nt][3] = fmaf(ah.y, part[nt][3], acc[nt][3]);
+        }
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(empty_bar(slot));   // slot free for the producer
     }
-    if (!ok) report_status(p.status, kStatusTimeout, kSiteGemv, kRoleCompute);
+    // every lane is done with the slot: refill it with this warp's box i + 2
+    __syncwarp();
+    if (i + kWarpSlots < nmine) {
+      if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue_box(i + kWarpSlots);
+    }
+    return true;
+  };
+  for (int i = 0; i < nmine && ok; i += 2) {
+    // the registers of box i (slot 0) are refilled for box i + 2 right after use
+    uint32_t qa = qa0, qb = qb0;
+    float sa = sa0, sb = sb0;
+    load_scales(i + 2, qa0, qb0, sa0, sb0);
+    if (!do_box(i, qa, qb, sa, sb)) { ok = false; break; }
+    waited = i + 1;
+    if (i + 1 < nmine) {
+      qa = qa1; qb = qb1; sa = sa1; sb = sb1;
+      load_scales(i + 3, qa1, qb1, sa1, sb1);
+      if (!do_box(i + 1, qa, qb, sa, sb)) { ok = false; break; }
+      waited = i + 2;
+    }
+  }
+  if (!ok) {
+    report_status(p.status, kStatusTimeout, kSiteGemv, kRoleCompute);
+    // copies still in flight land before the CTA may exit
+    if (lane == 0)
+      for (int i = waited; i < min(nmine, waited + kWarpSlots); ++i)
+        tc::mbar_wait(bars + 8u * (i % kWarpSlots), (i / kWarpSlots) & 1);
   }
 
-  // Epilogue: undo the token scales and stage this slice's partial
-  // [8 NT tokens x 128 rows] in shared memory (over the level table).
+  // The second K-half of each row group hands its sums to the first.
+  if (kh == 1) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      *reinterpret_cast<float4*>(red + ((rgp * 32 + lane) * NT + nt) * 4) =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+  }
+  __syncthreads();
+  // Undo the token scales; the first K-half holds the row group's sums.
   float inv0[NT], inv1[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -402,20 +372,30 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     inv0[nt] = tk0 < mt ? xinv[tk0] : 0.0f;
     inv1[nt] = tk0 + 1 < mt ? xinv[tk0 + 1] : 0.0f;
   }
-  __syncthreads();
-  float* out_s = reinterpret_cast<float*>(smem);
-  if (p.slices == 1 && warp < kComputeWarps) {
+  if (kh == 0) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
-      const int rg = warp * 16 + g;
-      out_s[tk0 * kOutStride + rg] = acc[nt][0] * inv0[nt];
-      out_s[tk1 * kOutStride + rg] = acc[nt][1] * inv1[nt];
-      out_s[tk0 * kOutStride + rg + 8] = acc[nt][2] * inv0[nt];
-      out_s[tk1 * kOutStride + rg + 8] = acc[nt][3] * inv1[nt];
+      const float4 o = *reinterpret_cast<const float4*>(red + ((rgp * 32 + lane) * NT + nt) * 4);
+      acc[nt][0] = (acc[nt][0] + o.x) * inv0[nt];
+      acc[nt][1] = (acc[nt][1] + o.y) * inv1[nt];
+      acc[nt][2] = (acc[nt][2] + o.z) * inv0[nt];
+      acc[nt][3] = (acc[nt][3] + o.w) * inv1[nt];
     }
   }
   if (p.slices == 1) {
+    // stage [8 NT tokens x 128 rows] over the level table, then float4 stores
+    float* out_s = reinterpret_cast<float*>(smem);
+    if (kh == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
+        const int rg = rgp * 16 + g;
+        out_s[tk0 * kOutStride + rg] = acc[nt][0];
+        out_s[tk1 * kOutStride + rg] = acc[nt][1];
+        out_s[tk0 * kOutStride + rg + 8] = acc[nt][2];
+        out_s[tk1 * kOutStride + rg + 8] = acc[nt][3];
+      }
+    }
     __syncthreads();
     for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
       const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
@@ -425,23 +405,22 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     }
   } else {
     // Cluster reduction, push form: CTA `rank` owns rows [rank*rpc, (rank+1)*rpc)
-    // of the row tile. Every CTA stores its scaled partial of those rows into
-    // the owner's inbox slot for its slice, one cluster barrier makes the
-    // stores visible, and each owner sums its slots and writes Y once.
-    float* inbox = reinterpret_cast<float*>(smem + gemv_off_inbox(p.ring, p.max_nb, NT));
+    // of the row tile. Every CTA stores its partial of those rows into the
+    // owner's inbox slot for its slice, one cluster barrier makes the stores
+    // visible, and each owner sums its slots and writes Y once.
     const int rpc = kGemvRows / p.slices;          // rows owned per CTA (a power of two)
     const int rpc_shift = 31 - __clz(rpc);
-    if (warp < kComputeWarps) {
+    if (kh == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int tk0 = nt * 8 + 2 * t;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tk = tk0 + (e & 1);
-          const int rg = warp * 16 + g + 8 * (e >> 1);
-          const float v = acc[nt][e] * ((e & 1) ? inv1[nt] : inv0[nt]);
+          const int rg = rgp * 16 + g + 8 * (e >> 1);
           const uint32_t owner = static_cast<uint32_t>(rg >> rpc_shift);
-          st_dsmem(inbox + ((slice * 8 * NT + tk) << rpc_shift) + (rg & (rpc - 1)), owner, v);
+          st_dsmem(inbox + ((slice * 8 * NT + tk) << rpc_shift) + (rg & (rpc - 1)), owner,
+                   acc[nt][e]);
         }
       }
     }
@@ -535,9 +514,11 @@ simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __rest
 }  // namespace
 
 // Dynamic shared memory of one GEMV CTA (plus 1 KB to align the base).
-constexpr size_t gemv_smem_bytes(int nt, int ring, int max_nb) {
-  return static_cast<size_t>(gemv_off_inbox(ring, max_nb, nt)) + 8 * nt * kGemvRows * 4 + 1024;
+constexpr size_t gemv_smem_bytes(int nt, int max_nb, int xrows) {
+  return static_cast<size_t>(gemv_off_xs(nt)) +
+         static_cast<size_t>(xrows) * gemv_xstride(max_nb) + 1024;
 }
+constexpr size_t kGemvSmemTwoPerSm = 112 * 1024;   // two CTAs per SM
 constexpr size_t kGemvSmemLimit = 220 * 1024;
 
 template <int NT>
@@ -558,27 +539,46 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
   a.status = status;
-  // K-slices (cluster size): aim for about two CTAs per SM, at most 8, each
-  // slice at least one block and at most kMaxSliceBlocks blocks.
+  // Launch shape: K-slices (cluster size, a power of two <= 8) and n-tiles
+  // per CTA, chosen for the fewest waves (two CTAs per SM when they fit in
+  // shared memory, else one), then the most busy SMs, then two n-tiles.
   const int64_t row_ctas = (N + kGemvRows - 1) / kGemvRows;
-  int slices = 1;
-  while (slices < kMaxCluster && row_ctas * slices < 2 * static_cast<int64_t>(num_sms) &&
-         slices * 2 <= a.nblk)
-    slices *= 2;
-  while (slices < kMaxCluster && (a.nblk + slices - 1) / slices > kMaxSliceBlocks) slices *= 2;
-  if ((a.nblk + slices - 1) / slices > kMaxSliceBlocks) return cudaErrorInvalidValue;
-  a.slices = slices;
-  a.max_nb = (a.nblk + slices - 1) / slices;
-  a.ring = std::min(kMaxRing, (a.max_nb + kBoxBlocks - 1) / kBoxBlocks);
-  int nt = M <= 8 ? 1 : 2;
-  while (nt > 1 && gemv_smem_bytes(nt, a.ring, a.max_nb) > kGemvSmemLimit) nt /= 2;
+  const int nt_max = M <= 8 ? 1 : 2;
+  int best_s = 0, best_nt = 0;
+  int64_t best_waves = 0, best_busy = 0;
+  size_t best_smem = 0;
+  for (int sl = kMaxCluster; sl >= 1; sl /= 2) {
+    if (sl > a.nblk) continue;
+    const int nb = (a.nblk + sl - 1) / sl;
+    if (nb > kMaxSliceBlocks) continue;
+    for (int n = nt_max; n >= 1; --n) {
+      const size_t b = gemv_smem_bytes(n, nb, static_cast<int>(std::min<int64_t>(M, 8 * n)));
+      if (b > kGemvSmemLimit) continue;
+      const int64_t ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
+      const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
+      const int64_t waves = (ctas + cap - 1) / cap, busy = std::min(ctas, cap);
+      const bool better = best_s == 0 || waves < best_waves ||
+                          (waves == best_waves && busy > best_busy) ||
+                          (waves == best_waves && busy == best_busy && n > best_nt);
+      if (better) {
+        best_s = sl;
+        best_nt = n;
+        best_waves = waves;
+        best_busy = busy;
+        best_smem = b;
+      }
+    }
+  }
+  if (best_s == 0) return cudaErrorInvalidValue;
+  a.slices = best_s;
+  a.max_nb = (a.nblk + best_s - 1) / best_s;
+  const int nt = best_nt;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
-  const size_t smem = gemv_smem_bytes(nt, a.ring, a.max_nb);
-  if (smem > kGemvSmemLimit) return cudaErrorInvalidValue;
-  // packed codes [N, K/2] bytes, box 128 B (4 absmax blocks) x 128 rows, 128-byte swizzle
+  const size_t smem = best_smem;
+  // packed codes [N, K/2] bytes, box 128 B (4 absmax blocks) x 16 rows, 128-byte swizzle
   CUtensorMap tm;
   if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
-                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), 128, kGemvRows,
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), 128, 16,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static std::once_flag once;
@@ -588,7 +588,7 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
     cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   });
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(slices),
+  cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(a.slices),
                      static_cast<unsigned>(mtiles));
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -596,7 +596,7 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = static_cast<unsigned>(slices);
+  attr[0].val.clusterDim.y = static_cast<unsigned>(a.slices);
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
