@@ -191,7 +191,8 @@ class Step:
         self.graphs = None
 
     def _calls(self):
-        """List of (category, flop, bytes, launches, fn, group) in step order.
+        """List of (category, flop, bytes, launches, fn, group, projection) in
+        step order.
         Calls with the same group are independent and may be issued together
         (the projections of the layer that share an input); groups run in
         order. With rotating weight copies, one step walks every copy once."""
@@ -203,7 +204,7 @@ class Step:
             for i, p in enumerate(P):
                 calls.append(("quantize", 0, quant_bytes(p), 1,
                               lambda i=i: nf4.nf4_quantize(self.weights[i], out=self.q[0][i]),
-                              ("quantize", 0)))
+                              ("quantize", 0), i))
         for M in sorted(self.w.fwd_m, reverse=True):
             for r in range(self.rotate):
                 for gi, g in enumerate(groups):
@@ -213,7 +214,7 @@ class Step:
                         calls.append((f"fwd_M{M}", f, b, 1,
                                       lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_fwd(
                                           self.x[(p.cols, M)], self.q[r][i], out=self.y[(i, M)]),
-                                      (f"fwd_M{M}", r, gi)))
+                                      (f"fwd_M{M}", r, gi), i))
         for M in self.w.dx_m:
             for r in range(self.rotate):
                 for gi, g in enumerate(groups):
@@ -223,7 +224,7 @@ class Step:
                         calls.append((f"dx_M{M}", f, b, 1,
                                       lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_bwd_dx(
                                           self.dy[(p.rows, M)], self.q[r][i], out=self.dx[(i, M)]),
-                                      (f"dx_M{M}", r, gi)))
+                                      (f"dx_M{M}", r, gi), i))
         return calls
 
     def issue(self, idx):
@@ -310,17 +311,51 @@ class Step:
         return h2d, d2h
 
     def run_e2e(self):
-        for W, hW in zip(self.weights, self.h_w):
-            W.copy_(hW, non_blocking=True)
-        for k, v in self.x.items():
-            v.copy_(self.h_x[k], non_blocking=True)
-        for k, v in self.dy.items():
-            v.copy_(self.h_dy[k], non_blocking=True)
-        self.run_eager()
-        for k, v in self.y.items():
-            self.h_y[k].copy_(v, non_blocking=True)
-        for k, v in self.dx.items():
-            self.h_dx[k].copy_(v, non_blocking=True)
+        """One step from host inputs to host outputs, streamed by projection:
+        the activations and then each weight go in on a copy stream; a
+        projection's quantize, forwards and input gradient run as soon as its
+        weight has landed, and its outputs go back on a second copy stream
+        while later weights are still arriving. The largest weights go first,
+        so that what is left after the last copy-in is small. Same work as
+        run(); only the order (by projection) and the overlap differ."""
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "cin"):
+            self.cin, self.cout = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        cin, cout = self.cin, self.cout
+        cin.wait_stream(main)        # the previous step's kernels have read their inputs
+        P = self.w.projections
+        order = sorted(range(len(P)), key=lambda i: -P[i].rows * P[i].cols)
+        with torch.cuda.stream(cin):
+            for k, v in self.x.items():
+                v.copy_(self.h_x[k], non_blocking=True)
+            for k, v in self.dy.items():
+                v.copy_(self.h_dy[k], non_blocking=True)
+            ev_act = torch.cuda.Event()
+            ev_act.record(cin)
+            ev_w = {}
+            if self.h_w:
+                for i in order:
+                    self.weights[i].copy_(self.h_w[i], non_blocking=True)
+                    ev_w[i] = torch.cuda.Event()
+                    ev_w[i].record(cin)
+        main.wait_event(ev_act)
+        for i in order:
+            if ev_w:
+                main.wait_event(ev_w[i])
+            for c in self.calls:
+                if c[6] == i:
+                    c[4]()
+            done = torch.cuda.Event()
+            done.record(main)
+            cout.wait_event(done)
+            with torch.cuda.stream(cout):
+                for (j, M), v in self.y.items():
+                    if j == i:
+                        self.h_y[(j, M)].copy_(v, non_blocking=True)
+                for (j, M), v in self.dx.items():
+                    if j == i:
+                        self.h_dx[(j, M)].copy_(v, non_blocking=True)
+        main.wait_stream(cout)
 
 
 # ------------------------------------------------------------ oracle sample --
@@ -499,7 +534,7 @@ def main():
             e0, e1 = events[s * ngraphs + j]
             cat_ms[cat] = cat_ms.get(cat, 0.0) + e0.elapsed_time(e1)
             for k in idx:
-                _, f, b, n, _, _ = step.calls[k]
+                _, f, b, n, _, _, _ = step.calls[k]
                 cat_flop[cat] = cat_flop.get(cat, 0) + f
                 cat_bytes[cat] = cat_bytes.get(cat, 0) + b
                 cat_n[cat] = cat_n.get(cat, 0) + n

@@ -117,17 +117,16 @@ __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
 }
 
 // Shared memory (offsets from a 1024-byte aligned base): level table, code
-// slots (per warp, 1024-byte aligned for the swizzle), mbarriers, the
-// dequantized absmax of each slot's row pairs (g, g + 8), token scales, the
-// K-half reduction buffer, the cluster reduction inbox and the fp16
+// slots (per warp, 1024-byte aligned for the swizzle; after the main loop a
+// second-K-half warp's first slot carries its sums to the first K-half),
+// mbarriers, token scales, the cluster reduction inbox and the fp16
 // activation slice (rows of max_nb * 128 + 8 bytes: the 8 keeps the B
 // fragment loads of 8 token rows on distinct banks).
 constexpr int kOffSlots = kTabBytes;
 constexpr int kOffBars = kOffSlots + kGemvWarps * kWarpSlots * kBoxBytes;
-constexpr int kOffAhw = kOffBars + kGemvWarps * kWarpSlots * 8;
-constexpr int kOffXinv = kOffAhw + kGemvWarps * kWarpSlots * 32 * 8;
-constexpr int kOffRed = kOffXinv + 16 * 4;
-__host__ __device__ constexpr int gemv_off_inbox(int nt) { return kOffRed + kRowGroups * 32 * 4 * nt * 4; }
+constexpr int kOffXinv = kOffBars + kGemvWarps * kWarpSlots * 8;
+constexpr int kOffInbox = kOffXinv + 16 * 4;
+__host__ __device__ constexpr int gemv_off_inbox(int) { return kOffInbox; }
 __host__ __device__ constexpr int gemv_off_xs(int nt) { return gemv_off_inbox(nt) + 8 * nt * kGemvRows * 4; }
 __host__ __device__ constexpr int gemv_xstride(int max_nb) { return max_nb * 128 + 8; }
 
@@ -139,7 +138,6 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
   float* xinv = reinterpret_cast<float*>(smem + kOffXinv);    // [16]
-  float* red = reinterpret_cast<float*>(smem + kOffRed);
   float* inbox = reinterpret_cast<float*>(smem + gemv_off_inbox(NT));
   uint8_t* xs = smem + gemv_off_xs(NT);
   const int xstride = gemv_xstride(p.max_nb);
@@ -147,6 +145,9 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int rgp = warp & (kRowGroups - 1), kh = warp / kRowGroups;
+  // K-half hand-off of row group rgp: the first slot of warp rgp + 8, free
+  // once that warp has consumed its last box
+  float* red = reinterpret_cast<float*>(smem + kOffSlots + (rgp + kRowGroups) * kWarpSlots * kBoxBytes);
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kGemvRows;
   const int slice = blockIdx.y;
   const int kb0 = slice_begin(p.nblk, p.slices, slice);
@@ -157,7 +158,6 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   // this warp's code slots and their mbarriers; it takes boxes kh, kh + 2, ...
   const uint32_t slots = tc::smem_addr(smem + kOffSlots) + warp * kWarpSlots * kBoxBytes;
   const uint32_t bars = tc::smem_addr(smem + kOffBars) + warp * kWarpSlots * 8;
-  float2* ahw = reinterpret_cast<float2*>(smem + kOffAhw) + warp * kWarpSlots * 32;
 
   // Programmatic dependent launch: the next kernel in the stream may start its
   // own set-up now; this one touches no global memory before the previous
@@ -279,13 +279,13 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   const uint8_t* slot_g = smem + kOffSlots + warp * kWarpSlots * kBoxBytes + g * 128 + (t & 1) * 8;
   bool ok = true;
   int waited = 0;
-  // one box: its scales into the warp's slot buffer, then its four blocks
+  // one box: lane e's row-pair scales (block e >> 3, rows (e & 7, + 8)),
+  // then its four blocks, each taking its scales from lane 8 jj + g
   auto do_box = [&](int i, uint32_t qa, uint32_t qb, float sa, float sb) {
     const int sl = i % kWarpSlots;
-    ahw[sl * 32 + lane] = make_float2(dequant_absmax(qa, sa), dequant_absmax(qb, sb));
+    const float aha = dequant_absmax(qa, sa), ahb = dequant_absmax(qb, sb);
     // warp-uniform outcome: the lanes leave together or go on together
     const bool got = tc::mbar_wait(bars + 8u * sl, (i / kWarpSlots) & 1);
-    __syncwarp();
     if (!__all_sync(0xffffffffu, got)) return false;
     const int b = kh + 2 * i;
     const uint8_t* sg = slot_g + sl * kBoxBytes;
@@ -316,7 +316,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
             mma_f16(part[nt], a0, a1, a2, a3, bx.x, bx.y);
           }
         }
-        const float2 ah = ahw[sl * 32 + jj * 8 + g];
+        const float2 ah = make_float2(__shfl_sync(0xffffffffu, aha, jj * 8 + g),
+                                      __shfl_sync(0xffffffffu, ahb, jj * 8 + g));
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           acc[nt][0] = fmaf(ah.x, part[nt][0], acc[nt][0]);
@@ -360,7 +361,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   if (kh == 1) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-      *reinterpret_cast<float4*>(red + ((rgp * 32 + lane) * NT + nt) * 4) =
+      *reinterpret_cast<float4*>(red + (lane * NT + nt) * 4) =
           make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   }
   __syncthreads();
@@ -375,7 +376,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   if (kh == 0) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float4 o = *reinterpret_cast<const float4*>(red + ((rgp * 32 + lane) * NT + nt) * 4);
+      const float4 o = *reinterpret_cast<const float4*>(red + (lane * NT + nt) * 4);
       acc[nt][0] = (acc[nt][0] + o.x) * inv0[nt];
       acc[nt][1] = (acc[nt][1] + o.y) * inv1[nt];
       acc[nt][2] = (acc[nt][2] + o.z) * inv0[nt];
@@ -540,13 +541,24 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   a.nblk = static_cast<int>(K / kBlock);
   a.status = status;
   // Launch shape: K-slices (cluster size, a power of two <= 8) and n-tiles
-  // per CTA, chosen for the fewest waves (two CTAs per SM when they fit in
-  // shared memory, else one), then the most busy SMs, then two n-tiles.
+  // per CTA. Fewest waves (two CTAs per SM when they fit in shared memory,
+  // else one); among those, the fewest CTAs that still keep 70% of the SMs
+  // busy (bigger CTAs pay the prologue and the cluster barrier less often;
+  // measured faster than filling every SM with smaller ones), else the most
+  // busy SMs; then two n-tiles over one.
   const int64_t row_ctas = (N + kGemvRows - 1) / kGemvRows;
   const int nt_max = M <= 8 ? 1 : 2;
-  int best_s = 0, best_nt = 0;
-  int64_t best_waves = 0, best_busy = 0;
-  size_t best_smem = 0;
+  struct Shape { int s, nt; int64_t ctas, waves, busy; size_t smem; };
+  Shape best{0, 0, 0, 0, 0, 0};
+  const int64_t enough = (7 * static_cast<int64_t>(num_sms)) / 10;
+  auto better = [&](const Shape& c) {
+    if (best.s == 0 || c.waves != best.waves) return best.s == 0 || c.waves < best.waves;
+    const bool ce = c.busy >= enough, be = best.busy >= enough;
+    if (ce != be) return ce;
+    if (ce && c.ctas != best.ctas) return c.ctas < best.ctas;
+    if (!ce && c.busy != best.busy) return c.busy > best.busy;
+    return c.nt > best.nt;
+  };
   for (int sl = kMaxCluster; sl >= 1; sl /= 2) {
     if (sl > a.nblk) continue;
     const int nb = (a.nblk + sl - 1) / sl;
@@ -554,27 +566,29 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
     for (int n = nt_max; n >= 1; --n) {
       const size_t b = gemv_smem_bytes(n, nb, static_cast<int>(std::min<int64_t>(M, 8 * n)));
       if (b > kGemvSmemLimit) continue;
-      const int64_t ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
+      Shape c;
+      c.s = sl;
+      c.nt = n;
+      c.smem = b;
+      c.ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
       const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
-      const int64_t waves = (ctas + cap - 1) / cap, busy = std::min(ctas, cap);
-      const bool better = best_s == 0 || waves < best_waves ||
-                          (waves == best_waves && busy > best_busy) ||
-                          (waves == best_waves && busy == best_busy && n > best_nt);
-      if (better) {
-        best_s = sl;
-        best_nt = n;
-        best_waves = waves;
-        best_busy = busy;
-        best_smem = b;
-      }
+      c.waves = (c.ctas + cap - 1) / cap;
+      c.busy = std::min(c.ctas, static_cast<int64_t>(num_sms));
+      if (better(c)) best = c;
     }
   }
+  const int best_s = best.s, best_nt = best.nt;
+  const size_t best_smem = best.smem;
   if (best_s == 0) return cudaErrorInvalidValue;
   a.slices = best_s;
   a.max_nb = (a.nblk + best_s - 1) / best_s;
   const int nt = best_nt;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
-  const size_t smem = best_smem;
+  // A grid of at most one CTA per SM asks for more shared memory than two
+  // CTAs can share, so that the early-launched CTAs of the next kernel in the
+  // stream (programmatic dependent launch) cannot pile up two on one SM while
+  // others stay idle.
+  const size_t smem = best.ctas <= num_sms ? std::max(best_smem, kGemvSmemTwoPerSm + 4096) : best_smem;
   // packed codes [N, K/2] bytes, box 128 B (4 absmax blocks) x 16 rows, 128-byte swizzle
   CUtensorMap tm;
   if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),

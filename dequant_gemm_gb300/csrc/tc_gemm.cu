@@ -52,19 +52,26 @@ namespace nf4 {
 namespace {
 
 constexpr int kTileRows = 128;               // MMA M
-constexpr int kMaxBN = 256;                  // MMA N
-constexpr int kActStageBytes = kMaxBN * 128; // 64 bf16 per token row
 constexpr int kCodesStageBytes = 4096;       // 128 x 64 nibbles
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemA0 = 256;            // columns from 256 on: A-operand slots
 
-// Per-direction configuration and shared-memory layout.
-template <bool kDx>
+// Per-direction and per-token-tile configuration and shared-memory layout.
+// The token tile BN (MMA N) sets the stage size; smaller tiles get deeper
+// rings, so that enough code bytes are in flight per SM to cover the memory
+// latency. Tensor memory holds the BN fp32 accumulator columns, then one
+// 32-column A-operand slot per stage.
+template <bool kDx, int kBN>
 struct Cfg {
   static constexpr int kGroups = 3;                  // dequant warp groups
   static constexpr int kDqWarps = 4 * kGroups;
-  static constexpr int kThreads = 64 + 32 * kDqWarps;
-  static constexpr int kStages = 5;
+  // With small token tiles one MMA takes too little time to hide the cost of
+  // issuing it, so the forward then issues from two threads on different
+  // schedulers, alternate stage pairs into two accumulators.
+  static constexpr int kMmaThreads = (!kDx && kBN <= 128) ? 2 : 1;
+  static constexpr int kThreads = 64 + 32 * kDqWarps + (kMmaThreads == 2 ? 32 : 0);
+  static constexpr int kStages = kBN == 64 ? 12 : (kBN == 128 ? 8 : 5);
+  static constexpr int kActStageBytes = kBN * 128;   // 64 bf16 per token row
+  static constexpr uint32_t kTmemA0 = kMmaThreads * kBN;
   static constexpr int kLutBytes = kHalfPairTableBytes;
   static constexpr int kAhatBytes = kDx ? kDqWarps * 64 * 4 : 0;   // per-warp row scales
   static constexpr int kOffAct = 0;
@@ -76,6 +83,7 @@ struct Cfg {
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   static_assert(kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
+  static_assert(kBN == 64 || kBN == 128 || kBN == 256, "token tile");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -110,13 +118,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 
-template <bool kDx>
-__global__ void __launch_bounds__(Cfg<kDx>::kThreads, 1)
+template <bool kDx, int kBN>
+__global__ void __launch_bounds__(Cfg<kDx, kBN>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                const TcArgs p) {
-  using C = Cfg<kDx>;
+  using C = Cfg<kDx, kBN>;
   constexpr int kStages = C::kStages;
   constexpr int kGroups = C::kGroups;
+  constexpr int kActStageBytes = C::kActStageBytes;
+  constexpr uint32_t kTmemA0 = C::kTmemA0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -141,7 +151,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       tc::mbar_init(dq_bar(s), 4);     // one arrival per warp of the stage's group
       tc::mbar_init(empty_bar(s), 1);
     }
-    tc::mbar_init(accum_bar, 1);
+    tc::mbar_init(accum_bar, C::kMmaThreads);
     tc::mbar_init(lut_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -195,9 +205,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           tc::mbar_wait(full_bar(i % kStages), (i / kStages) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (C::kMmaThreads == 2 && warp == 2 + C::kDqWarps)) {
     // ---------------------------------------------------------------- MMA --
     if (lane == 0) {
+      const int mth = warp == 1 ? 0 : 1;     // MMA thread: its accumulator and stage pairs
       // The dequant warps arrive on dq_bar only after they have seen the
       // stage's copies land on full_bar, so its completion orders both the
       // tensor-memory A operand and the shared-memory B tile before the MMAs;
@@ -208,40 +219,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       // input gradient, whose dequant is the slower side, takes them singly.
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, static_cast<uint32_t>(p.bn));
       const uint64_t bdesc0 = tc::sw128_kmajor_desc(tc::smem_addr(smem + C::kOffAct));
-      int slot = 0;
-      uint32_t ph = 0;
-      auto next = [&](int s, uint32_t f, int& s2, uint32_t& f2) {
-        s2 = s + 1 == kStages ? 0 : s + 1;
-        f2 = s + 1 == kStages ? f ^ 1u : f;
-      };
-      auto issue = [&](int i, int sl) {
+      const uint32_t dacc = tmem + static_cast<uint32_t>(mth * kBN);
+      bool first = true;
+      auto issue = [&](int sl) {
         const uint32_t a = tmem + kTmemA0 + 32u * sl;
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          tc::mma_bf16_tmem_a(tmem, a + 8u * j, bdesc + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
+          tc::mma_bf16_tmem_a(dacc, a + 8u * j, bdesc + 2u * j, idesc, (first && j == 0) ? 0u : 1u);
+        first = false;
         tc::mma_commit(empty_bar(sl));
       };
       constexpr int kStep = kDx ? 1 : 2;
-      for (int i = 0; i < nst; i += kStep) {
+      for (int i = mth * kStep; i < nst; i += kStep * C::kMmaThreads) {
         const bool two = kStep == 2 && i + 1 < nst;
-        int slot1;
-        uint32_t ph1;
-        next(slot, ph, slot1, ph1);
+        const int slot = i % kStages, slot1 = (i + 1) % kStages;
+        const uint32_t ph = (i / kStages) & 1, ph1 = ((i + 1) / kStages) & 1;
         if (!tc::mbar_wait(dq_bar(slot), ph) || (two && !tc::mbar_wait(dq_bar(slot1), ph1))) {
           fail(kRoleMma);
           break;
         }
         tc::fence_after_sync();
-        issue(i, slot);
-        if (two) {
-          issue(i + 1, slot1);
-          next(slot1, ph1, slot, ph);
-        } else {
-          slot = slot1;
-          ph = ph1;
-        }
+        issue(slot);
+        if (two) issue(slot1);
       }
       tc::mma_commit(accum_bar);
       if (!tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);   // all MMAs done before teardown
@@ -396,7 +397,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
 
     // epilogue: accumulator lanes are tile rows, columns are tokens; the
-    // groups share out the 16-column chunks
+    // groups share out the 16-column chunks (with two MMA threads, the sum of
+    // both accumulators; the second is unwritten when it had no stage pair)
     if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail(kRoleEpilogue);
     tc::fence_after_sync();
     if (!*abort_flag) {
@@ -406,6 +408,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       for (int c = 16 * grp; c < p.bn; c += 16 * kGroups) {
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
+        if (C::kMmaThreads == 2 && nst > 2) {
+          uint32_t v2[16];
+          tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(kBN + c), v2);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
+        }
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -428,11 +438,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   }
 }
 
-template <bool kDx>
+template <bool kDx, int kBN>
 cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, const uint8_t* a8,
                       const float* s2, int64_t N, int64_t K, float* out, int num_sms, int* status,
                       cudaStream_t st) {
-  using C = Cfg<kDx>;
+  using C = Cfg<kDx, kBN>;
   TcArgs a;
   a.a8 = a8;
   a.s2 = s2;
@@ -442,7 +452,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
   a.status = status;
-  a.bn = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  a.bn = kBN;
   const int64_t nd = kDx ? K : N;            // tile-row dimension
   const int64_t red = kDx ? N : K;           // reduction dimension
   const int64_t row_tiles = (nd + kTileRows - 1) / kTileRows;
@@ -450,9 +460,9 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   a.stages_total = static_cast<int>((red + 63) / 64);
   int splits = 1;
   const int64_t ctas = row_tiles * m_tiles;
-  if (ctas < num_sms) {
-    splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms / ctas,
-                                                                      a.stages_total / 2)));
+  if (ctas < num_sms) {   // each split fills the ring at least once
+    splits = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(num_sms / ctas, a.stages_total / C::kStages)));
   }
   a.stages_per_split = (a.stages_total + splits - 1) / splits;
   splits = (a.stages_total + a.stages_per_split - 1) / a.stages_per_split;
@@ -473,7 +483,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
 
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(tc_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(tc_gemm_kernel<kDx, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          C::kSmemBytes);
   });
   if (a.atomic_out) {
@@ -482,7 +492,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   }
   dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
             static_cast<unsigned>(splits));
-  tc_gemm_kernel<kDx><<<grid, C::kThreads, C::kSmemBytes, st>>>(tm_act, tm_codes, a);
+  tc_gemm_kernel<kDx, kBN><<<grid, C::kThreads, C::kSmemBytes, st>>>(tm_act, tm_codes, a);
   return cudaGetLastError();
 }
 
@@ -491,13 +501,17 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
 cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
                           const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
                           int* status, cudaStream_t st) {
-  return launch_tc<false>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
+  if (M <= 64) return launch_tc<false, 64>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
+  if (M <= 128) return launch_tc<false, 128>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
+  return launch_tc<false, 256>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
 }
 
 cudaError_t launch_tc_dx(const uint16_t* dY, int64_t M, const uint8_t* codes, const uint8_t* a8,
                          const float* s2, int64_t N, int64_t K, float* dX, int num_sms,
                          int* status, cudaStream_t st) {
-  return launch_tc<true>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
+  if (M <= 64) return launch_tc<true, 64>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
+  if (M <= 128) return launch_tc<true, 128>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
+  return launch_tc<true, 256>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
 }
 
 }  // namespace nf4
