@@ -80,7 +80,7 @@ constexpr int kQThreads = 256;   // one thread per block of the group
 // per block per load), so a lane's 8 weights share one absmax (3 shuffle
 // steps) and one reciprocal. All 16 loads of a lane are issued before any is
 // used (64 KB in flight per CTA).
-__global__ void __launch_bounds__(kQThreads)
+__global__ void __launch_bounds__(kQThreads, 3)
 quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restrict__ codes,
                 uint8_t* __restrict__ a8_out, float* __restrict__ s2_out) {
   __shared__ float s_absmax[kGroup];

@@ -107,3 +107,13 @@ def test_timeout_site_description():
     assert nf4.describe_site((3 << 28) | (2 << 24) | 77) == "tensor-core input gradient, MMA issuer, CTA 77"
     assert nf4.describe_site((1 << 28) | (1 << 24)) == "small-M forward, copy producer, CTA 0"
     assert nf4.describe_site(-((1 << 32) - ((2 << 28) | (4 << 24) | 5))) == "tensor-core forward, epilogue, CTA 5"
+
+
+def test_autograd_wrapper_imports_and_validates_without_a_device():
+    from dequant_gemm_gb300.autograd import NF4LinearFunction, nf4_linear  # noqa: F401
+    q = nf4.NF4Weight(torch.empty(0, dtype=torch.uint8), torch.empty(0, dtype=torch.uint8),
+                      torch.empty(0), 8, 64)
+    with pytest.raises(ValueError):
+        nf4_linear(torch.zeros(2, 64, dtype=torch.float32), q)      # not bf16
+    with pytest.raises(ValueError):
+        nf4_linear(torch.zeros(2, 32, dtype=torch.bfloat16), q)     # wrong width
