@@ -54,6 +54,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Non-blocking probe of a phase. Unlike try_wait, it never suspends the thread,
+// and on the tcgen05 issuing thread it does not hold back the MMAs already
+// queued (a try_wait there was measured to let the tensor pipe drain).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded spin on mbar_test_wait, for a thread with nothing else to do.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
+                                               long long limit = (1ll << 31)) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint32_t bar) {

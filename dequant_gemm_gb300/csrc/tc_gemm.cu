@@ -64,14 +64,10 @@ template <bool kDx, int kBN>
 struct Cfg {
   static constexpr int kGroups = 3;                  // dequant warp groups
   static constexpr int kDqWarps = 4 * kGroups;
-  // With small token tiles one MMA takes too little time to hide the cost of
-  // issuing it, so the forward then issues from two threads on different
-  // schedulers, alternate stage pairs into two accumulators.
-  static constexpr int kMmaThreads = (!kDx && kBN <= 128) ? 2 : 1;
-  static constexpr int kThreads = 64 + 32 * kDqWarps + (kMmaThreads == 2 ? 32 : 0);
+  static constexpr int kThreads = 64 + 32 * kDqWarps;
   static constexpr int kStages = kBN == 64 ? 12 : (kBN == 128 ? 8 : 5);
   static constexpr int kActStageBytes = kBN * 128;   // 64 bf16 per token row
-  static constexpr uint32_t kTmemA0 = kMmaThreads * kBN;
+  static constexpr uint32_t kTmemA0 = kBN;
   static constexpr int kLutBytes = kHalfPairTableBytes;
   static constexpr int kAhatBytes = kDx ? kDqWarps * 64 * 4 : 0;   // per-warp row scales
   static constexpr int kOffAct = 0;
@@ -151,7 +147,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       tc::mbar_init(dq_bar(s), 4);     // one arrival per warp of the stage's group
       tc::mbar_init(empty_bar(s), 1);
     }
-    tc::mbar_init(accum_bar, C::kMmaThreads);
+    tc::mbar_init(accum_bar, 1);
     tc::mbar_init(lut_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -205,44 +201,32 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           tc::mbar_wait(full_bar(i % kStages), (i / kStages) & 1);
       }
     }
-  } else if (warp == 1 || (C::kMmaThreads == 2 && warp == 2 + C::kDqWarps)) {
+  } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
     if (lane == 0) {
-      const int mth = warp == 1 ? 0 : 1;     // MMA thread: its accumulator and stage pairs
       // The dequant warps arrive on dq_bar only after they have seen the
       // stage's copies land on full_bar, so its completion orders both the
       // tensor-memory A operand and the shared-memory B tile before the MMAs;
-      // a failure elsewhere surfaces here as a timeout. The forward takes the
-      // stages in pairs: both waits first, then the two stages' MMAs back to
-      // back, each followed by the commit that frees its slot, so the tensor
-      // pipe sees one loop turn per pair (its dequant runs well ahead). The
-      // input gradient, whose dequant is the slower side, takes them singly.
+      // a failure elsewhere surfaces here as a timeout. The wait is a spin on
+      // the non-blocking test: a suspending try_wait on this thread lets the
+      // MMAs already queued drain (about 380 idle tensor cycles per wait, as
+      // measured), while back-to-back issue keeps the pipe at its full rate.
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, static_cast<uint32_t>(p.bn));
       const uint64_t bdesc0 = tc::sw128_kmajor_desc(tc::smem_addr(smem + C::kOffAct));
-      const uint32_t dacc = tmem + static_cast<uint32_t>(mth * kBN);
-      bool first = true;
-      auto issue = [&](int sl) {
+      for (int i = 0; i < nst; ++i) {
+        const int sl = i % kStages;
+        if (!tc::mbar_wait_spin(dq_bar(sl), (i / kStages) & 1)) {
+          fail(kRoleMma);
+          break;
+        }
+        tc::fence_after_sync();
         const uint32_t a = tmem + kTmemA0 + 32u * sl;
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          tc::mma_bf16_tmem_a(dacc, a + 8u * j, bdesc + 2u * j, idesc, (first && j == 0) ? 0u : 1u);
-        first = false;
+          tc::mma_bf16_tmem_a(tmem, a + 8u * j, bdesc + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
         tc::mma_commit(empty_bar(sl));
-      };
-      constexpr int kStep = kDx ? 1 : 2;
-      for (int i = mth * kStep; i < nst; i += kStep * C::kMmaThreads) {
-        const bool two = kStep == 2 && i + 1 < nst;
-        const int slot = i % kStages, slot1 = (i + 1) % kStages;
-        const uint32_t ph = (i / kStages) & 1, ph1 = ((i + 1) / kStages) & 1;
-        if (!tc::mbar_wait(dq_bar(slot), ph) || (two && !tc::mbar_wait(dq_bar(slot1), ph1))) {
-          fail(kRoleMma);
-          break;
-        }
-        tc::fence_after_sync();
-        issue(slot);
-        if (two) issue(slot1);
       }
       tc::mma_commit(accum_bar);
       if (!tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);   // all MMAs done before teardown
@@ -397,8 +381,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
 
     // epilogue: accumulator lanes are tile rows, columns are tokens; the
-    // groups share out the 16-column chunks (with two MMA threads, the sum of
-    // both accumulators; the second is unwritten when it had no stage pair)
+    // groups share out the 16-column chunks
     if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail(kRoleEpilogue);
     tc::fence_after_sync();
     if (!*abort_flag) {
@@ -408,14 +391,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       for (int c = 16 * grp; c < p.bn; c += 16 * kGroups) {
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
-        if (C::kMmaThreads == 2 && nst > 2) {
-          uint32_t v2[16];
-          tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(kBN + c), v2);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
-        }
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
