@@ -80,22 +80,10 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
 // Store a float into CTA `rank`'s shared memory at this CTA's address of
 // `local` (made visible to that CTA by the next cluster barrier).
 __device__ __forceinline__ void st_dsmem(float* local, uint32_t rank, float v) {
-  uint32_t remote;
-  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(local)), "r"(rank));
+  const uint32_t remote = tc::mapa(tc::smem_addr(local), rank);
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
@@ -425,8 +413,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
         }
       }
     }
-    cluster_sync();
-    const int rank = static_cast<int>(cluster_ctarank());
+    tc::cluster_sync();
+    const int rank = static_cast<int>(tc::cluster_ctarank());
     for (int i = tid; i < 8 * NT * rpc; i += kGemvThreads) {
       const int tk = i >> rpc_shift, rl = i & (rpc - 1), r = rank * rpc + rl;
       if (tk < mt && row0 + r < p.N) {

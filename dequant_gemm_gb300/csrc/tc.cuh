@@ -69,15 +69,80 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Bounded spin on mbar_test_wait, for a thread with nothing else to do.
+// The same probe with acquire semantics at cluster scope, for a barrier that
+// threads of the peer CTA arrive on.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded spin on mbar_test_wait, for a thread with nothing else to do;
+// kCluster selects the cluster-scope acquire.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
                                                long long limit = (1ll << 31)) {
-  if (mbar_test_wait(bar, parity)) return true;
+  auto probe = [&] {
+    return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+  };
+  if (probe()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_test_wait(bar, parity)) return true;
+    if (probe()) return true;
     if (clock64() - t0 > limit) return false;
   }
+}
+
+// One lane of the (converged) warp gets true. A loop that the whole warp runs
+// on warp-uniform operands, issuing its tcgen05 instructions from the elected
+// lane, was measured to issue an MMA in ~70 cycles against ~116 from a loop
+// inside a one-thread branch.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "elect.sync _|P1, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "+r"(pred));
+  return pred != 0;
+}
+
+// ----------------------------------------------------------------- cluster --
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory writes before
+// it (release) against reads after it (acquire) across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Shared::cluster address of the variable at the same offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in
+// another CTA of the cluster), with the instruction's default semantics
+// (release at CTA scope). Measured on a busy SM, a release at cluster scope
+// instead waits for the thread's (or, cumulatively, the SM's) memory traffic
+// in flight: 1-2.5K cycles.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // --------------------------------------------------------------------- TMA --
@@ -96,16 +161,34 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 
 // ------------------------------------------------------------------ tcgen05 --
 // Allocation is warp-wide; the base address is written to shared memory.
+// With kCg = 2 one warp of each CTA of the pair allocates collectively, the
+// same columns in both tensor memories.
+template <int kCg = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (kCg == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
 }
 
+template <int kCg = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (kCg == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  }
 }
 
 __device__ __forceinline__ void fence_before_sync() {
@@ -116,22 +199,46 @@ __device__ __forceinline__ void fence_after_sync() {
 }
 
 // D[tmem] (+)= A[tmem] * B[smem descriptor]^T, bf16 inputs, fp32 accumulate.
+// With kCg = 2 the instruction is issued by one thread of the even CTA of a
+// pair and spans both SMs: each CTA holds half of the M rows of A and D in its
+// own tensor memory and half of the N rows of B at the same shared-memory
+// offset, and each SM's accumulator receives all N columns.
+template <int kCg = 1>
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (kCg == 1) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this
-// thread has completed.
+// thread has completed. With kCg = 2 the arrival goes to the barrier at the
+// same offset in both CTAs of the pair.
+template <int kCg = 1>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+  if constexpr (kCg == 1) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  } else {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(0x3))
+        : "memory");
+  }
 }
 
 // Thread i of the warp writes / reads lane (taddr.lane + i), 16 consecutive

@@ -6,7 +6,8 @@
 //
 // One CTA computes a 128 x BN tile of D = A * B^T with the weight as the
 // 128-row A operand and the tokens as the BN-column B operand (BN = 64, 128 or
-// 256), looping over the reduction in stages of 64:
+// 256; 256 on CTA pairs that share one 256 x 256 MMA), looping over the
+// reduction in stages of 64:
 //   * warp 0 (one thread) TMA-loads the stage's activation tile (bf16,
 //     128-byte swizzle, the K-major B operand) and its packed-code tile;
 //   * the dequant warps, in groups of four (one per tensor-memory lane
@@ -14,8 +15,8 @@
 //     dequantized absmax, rounded to bf16) and write them straight into
 //     tensor memory, where the MMA reads its A operand: the dequantized
 //     weight never touches shared memory;
-//   * warp 1 (one thread) issues tcgen05.mma (128 x BN x 16) into an fp32
-//     accumulator in tensor memory and commits each stage back to the
+//   * warp 1 issues tcgen05.mma (128 x BN x 16) from one elected lane into
+//     an fp32 accumulator in tensor memory and commits each stage back to the
 //     producer;
 //   * the dequant warps then read the accumulator with tcgen05.ld and store
 //     fp32 outputs (32 consecutive outputs of one token per warp store).
@@ -60,13 +61,30 @@ constexpr uint32_t kTmemCols = 512;
 // rings, so that enough code bytes are in flight per SM to cover the memory
 // latency. Tensor memory holds the BN fp32 accumulator columns, then one
 // 32-column A-operand slot per stage.
+//
+// The forward with BN = 256 runs on CTA pairs (cta_group::2): the two CTAs of
+// a cluster hold 128 weight rows each, and half of the token tile each; the
+// MMA warp of the even CTA issues 256 x 256 x 16 MMAs over both SMs. Each SM
+// then stages and reads only half of the activation tile, which is most of
+// the shared-memory traffic of a stage. The dequant warps of
+// both CTAs arrive on the issuing CTA's stage barrier. The arrival takes the
+// instruction's default (CTA-scope) release: by then the warp's tensor-memory
+// stores have retired (tcgen05.wait::st) and the stage's copies have been seen
+// complete, and a cluster-scope release was measured to stall the arriving
+// thread for 1-2.5K cycles on a busy SM, enough to halve the MMA rate.
 template <bool kDx, int kBN>
 struct Cfg {
-  static constexpr int kGroups = 3;                  // dequant warp groups
+  static constexpr bool kPair = kBN == 256 && !kDx;
+  static constexpr int kCg = kPair ? 2 : 1;          // tcgen05 cta_group
+  // dequant warp groups: a group needs several MMA stage times per stage;
+  // four for the forward (72 registers a thread), three for the input
+  // gradient, whose transposed walk runs best with ~120 registers a thread
+  static constexpr int kGroups = kDx ? 3 : 4;
   static constexpr int kDqWarps = 4 * kGroups;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
-  static constexpr int kStages = kBN == 64 ? 12 : (kBN == 128 ? 8 : 5);
-  static constexpr int kActStageBytes = kBN * 128;   // 64 bf16 per token row
+  static constexpr int kStages = kBN == 64 ? 12 : (kBN == 128 || kPair ? 8 : 5);
+  static constexpr int kBRows = kPair ? kBN / 2 : kBN;   // tokens staged per CTA
+  static constexpr int kActStageBytes = kBRows * 128;    // 64 bf16 per token row
   static constexpr uint32_t kTmemA0 = kBN;
   static constexpr int kLutBytes = kHalfPairTableBytes;
   static constexpr int kAhatBytes = kDx ? kDqWarps * 64 * 4 : 0;   // per-warp row scales
@@ -119,6 +137,8 @@ __global__ void __launch_bounds__(Cfg<kDx, kBN>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                const TcArgs p) {
   using C = Cfg<kDx, kBN>;
+  constexpr bool kPair = C::kPair;
+  constexpr int kCg = C::kCg;
   constexpr int kStages = C::kStages;
   constexpr int kGroups = C::kGroups;
   constexpr int kActStageBytes = C::kActStageBytes;
@@ -136,6 +156,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A pair is the cluster (2, 1, 1): CTA 2p + rank holds rows 128 (2p + rank),
+  // the token half rank of the tile, and rank 0 issues the pair's MMAs.
+  const uint32_t rank = kPair ? tc::cluster_ctarank() : 0u;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * p.bn;
   const int s_begin = blockIdx.z * p.stages_per_split;
@@ -144,7 +167,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      tc::mbar_init(dq_bar(s), 4);     // one arrival per warp of the stage's group
+      // one arrival per warp of the stage's group, in both CTAs of a pair
+      tc::mbar_init(dq_bar(s), 4 * kCg);
       tc::mbar_init(empty_bar(s), 1);
     }
     tc::mbar_init(accum_bar, 1);
@@ -158,9 +182,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     tc::prefetch_tensormap(&tm_act);
     tc::prefetch_tensormap(&tm_codes);
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), kTmemCols);
+  if (warp == 1) tc::tmem_alloc<kCg>(tc::smem_addr(tmem_slot), kTmemCols);
   tc::fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair) tc::cluster_sync();   // the peer's barriers exist before any arrival
+  else __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
@@ -172,7 +197,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
-      const uint32_t tx = static_cast<uint32_t>(p.bn) * 128u + kCodesStageBytes;
+      const uint32_t tx = static_cast<uint32_t>(kActStageBytes + kCodesStageBytes);
+      const int32_t m_load = static_cast<int32_t>(m0) + static_cast<int32_t>(rank) * C::kBRows;
       int issued = 0;
       for (int i = 0; i < nst && !*abort_flag; ++i) {
         const int slot = i % kStages;
@@ -182,7 +208,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::mbar_arrive_expect_tx(full_bar(slot), tx);
         const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
         const uint32_t cod = tc::smem_addr(smem + C::kOffCodes + slot * kCodesStageBytes);
-        tc::tma_load_2d(act, &tm_act, s * 64, static_cast<int32_t>(m0), full_bar(slot));
+        tc::tma_load_2d(act, &tm_act, s * 64, m_load, full_bar(slot));
         if (!kDx) {
           // 128 rows x 32 bytes
           tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
@@ -203,36 +229,52 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
-    if (lane == 0) {
-      // The dequant warps arrive on dq_bar only after they have seen the
-      // stage's copies land on full_bar, so its completion orders both the
-      // tensor-memory A operand and the shared-memory B tile before the MMAs;
-      // a failure elsewhere surfaces here as a timeout. The wait is a spin on
-      // the non-blocking test: a suspending try_wait on this thread lets the
-      // MMAs already queued drain (about 380 idle tensor cycles per wait, as
-      // measured), while back-to-back issue keeps the pipe at its full rate.
-      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, static_cast<uint32_t>(p.bn));
+    // The whole warp runs the loop on warp-uniform values and one elected
+    // lane issues, which lets the MMA operands stay uniform (a loop inside a
+    // one-thread branch issued ~60% slower). The dequant warps arrive on
+    // dq_bar only after they have seen the stage's copies land on full_bar,
+    // so its completion orders both the tensor-memory A operand and the
+    // shared-memory B tile before the MMAs; a failure elsewhere surfaces here
+    // as a timeout. The wait is a spin on the non-blocking test: a suspending
+    // try_wait on the issuing warp lets the MMAs already queued drain (about
+    // 380 idle tensor cycles per wait, as measured). On a pair the peer's
+    // dequant warps arrive here too, once they have stored the stage and
+    // seen their own copies land.
+    if (rank == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows * kCg, static_cast<uint32_t>(p.bn));
       const uint64_t bdesc0 = tc::sw128_kmajor_desc(tc::smem_addr(smem + C::kOffAct));
       for (int i = 0; i < nst; ++i) {
         const int sl = i % kStages;
-        if (!tc::mbar_wait_spin(dq_bar(sl), (i / kStages) & 1)) {
-          fail(kRoleMma);
+        const bool ok = tc::mbar_wait_spin<kPair>(dq_bar(sl), (i / kStages) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) fail(kRoleMma);
           break;
         }
         tc::fence_after_sync();
         const uint32_t a = tmem + kTmemA0 + 32u * sl;
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tc::mma_bf16_tmem_a(tmem, a + 8u * j, bdesc + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
-        tc::mma_commit(empty_bar(sl));
+          for (int j = 0; j < 4; ++j)
+            tc::mma_bf16_tmem_a<kCg>(tmem, a + 8u * j, bdesc + 2u * j, idesc,
+                                     (i | j) != 0 ? 1u : 0u);
+          tc::mma_commit<kCg>(empty_bar(sl));
+        }
+        __syncwarp();
       }
-      tc::mma_commit(accum_bar);
-      if (!tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);   // all MMAs done before teardown
+      if (tc::elect_one()) tc::mma_commit<kCg>(accum_bar);
+      __syncwarp();
+      // all MMAs done before teardown
+      if (lane == 0 && !tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);
     }
   } else {
     // ---------------------------------------------------- dequant + store --
+    // the stage's A slot is written: tell the pair's MMA thread
+    auto arrive_dq = [&](int slot) {
+      if constexpr (kPair) tc::mbar_arrive_remote(tc::mapa(dq_bar(slot), 0));
+      else tc::mbar_arrive(dq_bar(slot));
+    };
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int grp = (warp - 2) >> 2;        // takes the stages i % kGroups == grp
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -289,7 +331,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(dq_bar(slot));
+        if (lane == 0) arrive_dq(slot);
       }
     } else {
       // After the transpose below, lane t holds column 8 (t & 3) + (t >> 2)
@@ -376,7 +418,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(dq_bar(slot));
+        if (lane == 0) arrive_dq(slot);
       }
     }
 
@@ -405,11 +447,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
   }
 
+  // On a pair, neither CTA frees its tensor memory or leaves (its barriers
+  // take the peer's arrivals) before both are done.
   tc::fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair) tc::cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc<kCg>(tmem, kTmemCols);
   }
 }
 
@@ -430,7 +475,9 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   a.bn = kBN;
   const int64_t nd = kDx ? K : N;            // tile-row dimension
   const int64_t red = kDx ? N : K;           // reduction dimension
-  const int64_t row_tiles = (nd + kTileRows - 1) / kTileRows;
+  // a pair's two CTAs take consecutive 128-row tiles
+  const int64_t tile_rows = kTileRows * C::kCg;
+  const int64_t row_tiles = (nd + tile_rows - 1) / tile_rows * C::kCg;
   const int64_t m_tiles = (M + a.bn - 1) / a.bn;
   a.stages_total = static_cast<int>((red + 63) / 64);
   int splits = 1;
@@ -444,10 +491,11 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   a.atomic_out = splits > 1 ? 1 : 0;
 
   CUtensorMap tm_act, tm_codes;
-  // activations: [M, red] bf16, box 64 (reduction) x bn (tokens), 128-byte swizzle
+  // activations: [M, red] bf16, box 64 (reduction) x the tokens one CTA
+  // stages, 128-byte swizzle
   if (!encode_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, static_cast<uint64_t>(red),
                  static_cast<uint64_t>(M), static_cast<uint64_t>(red) * 2, 64,
-                 static_cast<uint32_t>(a.bn), CU_TENSOR_MAP_SWIZZLE_128B))
+                 static_cast<uint32_t>(C::kBRows), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // packed codes: [N, K/2] bytes; the forward takes 32 B x 128 rows, the input
   // gradient 16 B (32 columns) x 64 rows per box
@@ -467,8 +515,24 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   }
   dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
             static_cast<unsigned>(splits));
-  tc_gemm_kernel<kDx, kBN><<<grid, C::kThreads, C::kSmemBytes, st>>>(tm_act, tm_codes, a);
-  return cudaGetLastError();
+  if constexpr (C::kPair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kDx, kBN>, tm_act, tm_codes, a);
+  } else {
+    tc_gemm_kernel<kDx, kBN><<<grid, C::kThreads, C::kSmemBytes, st>>>(tm_act, tm_codes, a);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace

@@ -316,10 +316,11 @@ def test_quantize_quotients_on_decision_edges():
 
 
 @pytest.mark.parametrize("rows,cols", [(8, 64), (24, 128), (136, 64), (8, 4096)])
-@pytest.mark.parametrize("M", [1, 16, 40])
+@pytest.mark.parametrize("M", [1, 16, 40, 300])
 def test_fwd_small_shapes(rows, cols, M):
     """Shortest reductions and fewest rows the format allows, on the decode
-    and tensor-memory paths (the code tile is wider than the weight)."""
+    and tensor-memory paths (the code tile is wider than the weight; at
+    M = 300 one CTA pair whose second CTA holds no weight row)."""
     W = weight_np(rows, cols, 21)
     X = wl.activations(M, cols, seed=rows + M)
     _, Y = run_fwd(W, X)
@@ -328,7 +329,7 @@ def test_fwd_small_shapes(rows, cols, M):
 
 
 @pytest.mark.parametrize("rows,cols", [(8, 64), (24, 128), (136, 64)])
-@pytest.mark.parametrize("M", [3, 40])
+@pytest.mark.parametrize("M", [3, 40, 200])
 def test_dx_small_shapes(rows, cols, M):
     W = weight_np(rows, cols, 22)
     dY = wl.activations(M, rows, std=0.01, seed=rows + M)
