@@ -223,6 +223,34 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
   }
 }
 
+// D[tmem] (+)= A[smem descriptor] * B[smem descriptor]^T, bf16 inputs, fp32
+// accumulate; kCg as for mma_bf16_tmem_a.
+template <int kCg = 1>
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kCg == 1) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Makes this thread's generic-proxy shared-memory stores visible to the async
+// proxy (TMA, tensor cores) before a later synchronisation.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this
 // thread has completed. With kCg = 2 the arrival goes to the barrier at the
 // same offset in both CTAs of the pair.
@@ -287,13 +315,31 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_byte_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand in 128-byte-swizzled
+// atoms: an atom is 8 rows of K, each 128 bytes holding 64 consecutive bf16
+// along M (N), 1024-byte aligned, 16-byte chunks XOR-permuted by the row.
+// `lbo` is the byte distance between atoms adjacent along M, `sbo` between
+// atoms adjacent along K.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_byte_addr, uint32_t lbo,
+                                                       uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_byte_addr >> 4) & 0x3fffu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;            // version
+  d |= static_cast<uint64_t>(2u) << 61;            // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 D, both
 // operands K-major, shape M x N:
 //   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)
 //   bits 10-12 B format (1 = bf16) bit 15/16 A/B major (0 = K)
 //   bits 17-22 N >> 3              bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n,
+                                                      bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) |
+         ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 }  // namespace tc

@@ -10,32 +10,33 @@
 // reduction in stages of 64:
 //   * warp 0 (one thread) TMA-loads the stage's activation tile (bf16,
 //     128-byte swizzle, the K-major B operand) and its packed-code tile;
-//   * the dequant warps, in groups of four (one per tensor-memory lane
-//     quarter) that take the stages in turn, dequantize the codes (level *
-//     dequantized absmax, rounded to bf16) and write them straight into
-//     tensor memory, where the MMA reads its A operand: the dequantized
-//     weight never touches shared memory;
+//   * the dequant warps, in four groups of four that take the stages in
+//     turn, dequantize the codes (level * dequantized absmax, rounded to
+//     bf16) into the stage's A operand;
 //   * warp 1 issues tcgen05.mma (128 x BN x 16) from one elected lane into
 //     an fp32 accumulator in tensor memory and commits each stage back to the
 //     producer;
 //   * the dequant warps then read the accumulator with tcgen05.ld and store
 //     fp32 outputs (32 consecutive outputs of one token per warp store).
 //
-// Forward: the tile is 128 weight rows, one row per dequant thread, walked
-// along K. Both levels of a code byte come from one lookup in a 256-entry
-// fp16 level pair table kept in 32 lane-private copies (every lookup of a
-// warp hits 32 distinct banks), are widened to fp32 and multiplied by the
-// row's dequantized absmax, a register.
+// Both directions walk the weight along its rows, one thread per (row, 64
+// columns) run, which is one absmax block: both levels of a code byte come
+// from one lookup in a 256-entry fp16 level pair table kept in 32
+// lane-private copies (every lookup of a warp hits 32 distinct banks), are
+// widened to fp32 and multiplied by the block's dequantized absmax, a
+// register.
 //
-// Input gradient: the tile is 128 weight columns walked along N (the
-// transposed walk), so a thread needs its column's nibbles down the stage's
-// 64 rows. Each warp reads its 32 columns' codes as 32-bit words (8 columns
-// of one row) and transposes 8 x 8 nibble blocks across lanes with three
-// shuffle rounds, after which a byte of a thread's word holds the codes of
-// two consecutive rows of its column: exactly one 32-bit tensor-memory word
-// of the A operand. That byte indexes the same pair table; the two levels
-// are multiplied by their rows' dequantized absmax, which the warp computes
-// for its 64 rows and broadcasts through shared memory.
+// Forward: the tile is 128 weight rows, the reduction runs along a row, so a
+// thread's run is K-contiguous and goes straight into tensor memory (one
+// lane per weight row), where the MMA reads its A operand: the dequantized
+// weight never touches shared memory.
+//
+// Input gradient: the tile is 128 weight columns and the reduction runs down
+// the columns. A = w^T is then M-major in the weight's own row order, so a
+// thread's run is one 128-byte row of a 128-byte-swizzled MN-major atom (64
+// columns x 8 rows) of an A tile in shared memory, read by the MMA through
+// an MN-major descriptor: no transposition and no per-row scale exchange
+// between lanes.
 //
 // When the output tiles alone cannot fill the GPU the reduction is split
 // across CTAs and summed with atomics into a zeroed output.
@@ -74,29 +75,32 @@ constexpr uint32_t kTmemCols = 512;
 // thread for 1-2.5K cycles on a busy SM, enough to halve the MMA rate.
 template <bool kDx, int kBN>
 struct Cfg {
-  static constexpr bool kPair = kBN == 256 && !kDx;
+  static constexpr bool kPair = kBN == 256;
   static constexpr int kCg = kPair ? 2 : 1;          // tcgen05 cta_group
-  // dequant warp groups: a group needs several MMA stage times per stage;
-  // four for the forward (72 registers a thread), three for the input
-  // gradient, whose transposed walk runs best with ~120 registers a thread
-  static constexpr int kGroups = kDx ? 3 : 4;
+  // dequant warp groups: a group needs several MMA stage times per stage
+  static constexpr int kGroups = 4;
   static constexpr int kDqWarps = 4 * kGroups;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
-  static constexpr int kStages = kBN == 64 ? 12 : (kBN == 128 || kPair ? 8 : 5);
+  // the input gradient stages its A tile in shared memory as well
+  static constexpr int kAStageBytes = kDx ? kTileRows * 64 * 2 : 0;
+  static constexpr int kStages = kDx ? (kBN == 64 ? 6 : 5) : (kBN == 64 ? 12 : 8);
   static constexpr int kBRows = kPair ? kBN / 2 : kBN;   // tokens staged per CTA
   static constexpr int kActStageBytes = kBRows * 128;    // 64 bf16 per token row
   static constexpr uint32_t kTmemA0 = kBN;
+  // the forward's A slots follow the accumulator; the input gradient holds
+  // only the accumulator (BN columns, a power of two >= 32)
+  static constexpr uint32_t kTmemAlloc = kDx ? static_cast<uint32_t>(kBN) : kTmemCols;
   static constexpr int kLutBytes = kHalfPairTableBytes;
-  static constexpr int kAhatBytes = kDx ? kDqWarps * 64 * 4 : 0;   // per-warp row scales
   static constexpr int kOffAct = 0;
-  static constexpr int kOffCodes = kOffAct + kStages * kActStageBytes;
+  static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
+  static constexpr int kOffCodes = kOffA + kStages * kAStageBytes;
   static constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
-  static constexpr int kOffAhat = kOffLut + kLutBytes;
-  static constexpr int kOffBars = kOffAhat + kAhatBytes;
+  static constexpr int kOffBars = kOffLut + kLutBytes;
   static constexpr int kNumBars = 3 * kStages + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
-  static_assert(kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
+  static_assert(kDx || kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
+  static_assert(kOffA % 1024 == 0 && kOffCodes % 1024 == 0, "swizzled tiles");
   static_assert(kBN == 64 || kBN == 128 || kBN == 256, "token tile");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -182,7 +186,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     tc::prefetch_tensormap(&tm_act);
     tc::prefetch_tensormap(&tm_codes);
   }
-  if (warp == 1) tc::tmem_alloc<kCg>(tc::smem_addr(tmem_slot), kTmemCols);
+  if (warp == 1) tc::tmem_alloc<kCg>(tc::smem_addr(tmem_slot), C::kTmemAlloc);
   tc::fence_before_sync();
   if constexpr (kPair) tc::cluster_sync();   // the peer's barriers exist before any arrival
   else __syncthreads();
@@ -213,12 +217,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           // 128 rows x 32 bytes
           tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
         } else {
-          // four 16-byte x 64-row boxes, one per lane quarter: quarter c's
-          // 32 columns land as a dense [64 rows][16 B] block at c * 1 KB
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tc::tma_load_2d(cod + 1024u * c, &tm_codes, static_cast<int32_t>(r0 / 2 + 16 * c),
-                            s * 64, full_bar(slot));
+          // one 64-byte (128 columns) x 64-row box with the 64-byte swizzle:
+          // row r's 16-byte chunk c lands at r * 64 + 16 * (c ^ ((r >> 1) & 3)).
+          // One box issues a quarter of the row requests of four 16-byte-wide
+          // ones (measured: the narrow boxes held the stage rate back).
+          tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(r0 / 2), s * 64, full_bar(slot));
         }
         ++issued;
       }
@@ -241,8 +244,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     // dequant warps arrive here too, once they have stored the stage and
     // seen their own copies land.
     if (rank == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows * kCg, static_cast<uint32_t>(p.bn));
+      const uint32_t idesc =
+          tc::idesc_bf16_f32(kTileRows * kCg, static_cast<uint32_t>(p.bn), kDx);
       const uint64_t bdesc0 = tc::sw128_kmajor_desc(tc::smem_addr(smem + C::kOffAct));
+      // input gradient: A tile atoms (column half h, row group g) at
+      // (2 g + h) KB, i.e. 1 KB apart along M and 2 KB along K
+      const uint64_t adesc0 = tc::sw128_mnmajor_desc(tc::smem_addr(smem + C::kOffA), 1024, 2048);
       for (int i = 0; i < nst; ++i) {
         const int sl = i % kStages;
         const bool ok = tc::mbar_wait_spin<kPair>(dq_bar(sl), (i / kStages) & 1);
@@ -254,11 +261,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const uint32_t a = tmem + kTmemA0 + 32u * sl;
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
+        const uint64_t adesc = adesc0 + static_cast<uint64_t>(sl * (C::kAStageBytes >> 4));
         if (tc::elect_one()) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc::mma_bf16_tmem_a<kCg>(tmem, a + 8u * j, bdesc + 2u * j, idesc,
-                                     (i | j) != 0 ? 1u : 0u);
+          for (int j = 0; j < 4; ++j) {
+            if constexpr (kDx)   // K rows 16 j .. 16 j + 15: row groups 2 j, 2 j + 1
+              tc::mma_bf16_ss<kCg>(tmem, adesc + 256u * j, bdesc + 2u * j, idesc,
+                                   (i | j) != 0 ? 1u : 0u);
+            else
+              tc::mma_bf16_tmem_a<kCg>(tmem, a + 8u * j, bdesc + 2u * j, idesc,
+                                       (i | j) != 0 ? 1u : 0u);
+          }
           tc::mma_commit<kCg>(empty_bar(sl));
         }
         __syncwarp();
@@ -334,89 +347,73 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         if (lane == 0) arrive_dq(slot);
       }
     } else {
-      // After the transpose below, lane t holds column 8 (t & 3) + (t >> 2)
-      // of the warp's 32, and byte b of its word the codes of rows 2b (high
-      // nibble) and 2b + 1 (low nibble) of an 8-row group. The three rounds
-      // swap 4-bit, 8-bit and 16-bit blocks with the lanes 4, 8 and 16 away;
-      // which half a lane keeps follows bit s of its row index (t >> 2) ^ 1.
-      const int rho = lane >> 2;
-      tile_row = 32 * q + 8 * (lane & 3) + rho;
-      const bool h0 = ((rho & 1) ^ 1) != 0;
-      const uint32_t keep0 = h0 ? 0xf0f0f0f0u : 0x0f0f0f0fu;
-      const uint32_t rot0 = h0 ? 28u : 4u;
-      const uint32_t sel1 = ((rho >> 1) & 1) ? 0x3715u : 0x6240u;
-      const uint32_t sel2 = ((rho >> 2) & 1) ? 0x3276u : 0x5410u;
-      // the warp's 32 columns share one absmax block per weight row
-      const int64_t kb = (r0 >> 6) + (q >> 1);
+      // Thread t of the group dequantizes weight row t % 64 of the stage over
+      // the tile's columns 64 (t / 64) .. + 63, one absmax block, as the
+      // forward walks a row. The 64 bf16 results are one 128-byte row of a
+      // 128-byte-swizzled MN-major atom of the A tile (64 weight columns along
+      // M x 8 weight rows along K per 1 KB atom; atom (column half h, row
+      // group g) at (2 g + h) KB).
+      const int t = ((warp - 2) & 3) * 32 + lane;
+      const int rr = t & 63, h = t >> 6;
+      const int64_t kb = (r0 >> 6) + h;
       const bool kb_ok = kb < p.nblk;
-      float* ah = reinterpret_cast<float*>(smem + C::kOffAhat) + (warp - 2) * 64;
       const uint8_t* tab = smem + C::kOffLut + 4 * lane;
-      const uint8_t* cq = smem + C::kOffCodes + q * 1024 + rho * 16 + (lane & 3) * 4;
-      uint32_t a8v[2] = {0u, 0u};
-      float s2v[2] = {0.0f, 0.0f};
-      bool rok[2] = {false, false};
-      // this lane computes the dequantized absmax of rows lane and lane + 32
-      auto load_scales = [&](int i) {
+      // 16-byte code chunks 2 h and 2 h + 1 of row rr (64-byte swizzle)
+      const int csw = (rr >> 1) & 3;
+      const int co0 = rr * 64 + 16 * ((2 * h) ^ csw), co1 = rr * 64 + 16 * ((2 * h + 1) ^ csw);
+      const int ao = (2 * (rr >> 3) + h) * 1024 + (rr & 7) * 128;
+      const int asw = rr & 7;
+      uint32_t a8v = 0;
+      float s2v = 0.0f;
+      bool rok = false;
+      auto load_scale = [&](int i) {
         if (i >= nst) return;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + lane + 32 * h;
-          rok[h] = kb_ok && n < p.N;
-          if (rok[h]) {
-            const int64_t bi = n * p.nblk + kb;
-            a8v[h] = p.a8[bi];
-            s2v[h] = p.s2[bi >> 8];
-          }
+        const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + rr;
+        rok = kb_ok && n < p.N;
+        if (rok) {
+          const int64_t bi = n * p.nblk + kb;
+          a8v = p.a8[bi];
+          s2v = p.s2[bi >> 8];
         }
       };
-      load_scales(grp);
+      load_scale(grp);
       if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
       for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        const float ah0 = rok[0] ? dequant_absmax(a8v[0], s2v[0]) : 0.0f;
-        const float ah1 = rok[1] ? dequant_absmax(a8v[1], s2v[1]) : 0.0f;
-        load_scales(i + kGroups);
-        __syncwarp();                       // last stage's reads of ah are done
-        ah[lane] = ah0;
-        ah[lane + 32] = ah1;
-        __syncwarp();
+        const float ahat = rok ? dequant_absmax(a8v, s2v) : 0.0f;
+        const float2 ahat2 = make_float2(ahat, ahat);
+        load_scale(i + kGroups);
         bool go = !*abort_flag;
         if (go && !tc::mbar_wait(full_bar(slot), ph)) {
           fail(kRoleCompute);
           go = false;
         }
         if (!__all_sync(0xffffffffu, go)) continue;
-        const uint8_t* cw = cq + slot * kCodesStageBytes;
+        const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
+        uint8_t* arow = smem + C::kOffA + slot * C::kAStageBytes + ao;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
+          const uint4 c = *reinterpret_cast<const uint4*>(cst + (hf ? co1 : co0));
+          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
           uint32_t v[16];
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            const int i8 = 4 * hf + g8;     // rows 8 i8 .. 8 i8 + 7
-            uint32_t x = *reinterpret_cast<const uint32_t*>(cw + 128 * i8);
-            uint32_t y = __shfl_xor_sync(0xffffffffu, x, 4);
-            x = (x & keep0) | (__funnelshift_l(y, y, rot0) & ~keep0);
-            y = __shfl_xor_sync(0xffffffffu, x, 8);
-            x = __byte_perm(x, y, sel1);
-            y = __shfl_xor_sync(0xffffffffu, x, 16);
-            x = __byte_perm(x, y, sel2);
-            const float4 sa = *reinterpret_cast<const float4*>(ah + 8 * i8);
-            const float4 sb = *reinterpret_cast<const float4*>(ah + 8 * i8 + 4);
-            const float2 sc[4] = {make_float2(sa.x, sa.y), make_float2(sa.z, sa.w),
-                                  make_float2(sb.x, sb.y), make_float2(sb.z, sb.w)};
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-              const uint32_t byte = __byte_perm(x, 0u, 0x4440u + b);
+              const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
               const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
-              const float2 lv = __fmul2_rn(__half22float2(h2), sc[b]);
-              v[4 * g8 + b] = pack_bf16x2(lv.x, lv.y);
+              const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
+              v[4 * j + b] = pack_bf16x2(lv.x, lv.y);
             }
           }
-          tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
+          // columns 32 hf + 8 j .. + 7 form chunk 4 hf + j of the atom row
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(arow + 16 * ((4 * hf + j) ^ asw)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
-        tc::tmem_wait_st();
-        tc::fence_before_sync();
+        tc::fence_proxy_async();   // the MMA reads the tile through the async proxy
         __syncwarp();
         if (lane == 0) arrive_dq(slot);
       }
@@ -454,7 +451,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   else __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc<kCg>(tmem, kTmemCols);
+    tc::tmem_dealloc<kCg>(tmem, C::kTmemAlloc);
   }
 }
 
@@ -498,10 +495,10 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
                  static_cast<uint32_t>(C::kBRows), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // packed codes: [N, K/2] bytes; the forward takes 32 B x 128 rows, the input
-  // gradient 16 B (32 columns) x 64 rows per box
+  // gradient 64 B (128 columns) x 64 rows, 64-byte swizzled
   if (!encode_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
-                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), kDx ? 16 : 32,
-                 kDx ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), kDx ? 64 : 32,
+                 kDx ? 64 : 128, kDx ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
 
   static std::once_flag once;
