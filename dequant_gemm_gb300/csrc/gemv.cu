@@ -81,6 +81,18 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Prefetch a tile of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // Store a float into CTA `rank`'s shared memory at this CTA's address of
 // `local` (made visible to that CTA by the next cluster barrier).
 __device__ __forceinline__ void st_dsmem(float* local, uint32_t rank, float v) {
@@ -164,14 +176,14 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     const int nmine_pf = (nboxes - kh + 1) / 2;
     if (lane == 0 && nmine_pf <= kWarpSlots && row0 + rgp * 16 < p.N)   // boxes inside the weight
       for (int i = 0; i < nmine_pf; ++i)
-        tc::tma_prefetch_2d(&tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * 32,
+        tma_prefetch_2d(&tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * 32,
                             static_cast<int32_t>(row0 + rgp * 16));
     const int64_t pr = row0 + rgp * 16 + lane;
     if (kh == 0 && lane < 16 && pr < p.N && nb > 0 && nmine_pf <= kWarpSlots) {
       const int64_t ia = pr * p.nblk + kb0;
-      tc::prefetch_l2(p.a8 + ia);
-      tc::prefetch_l2(p.a8 + ia + nb - 1);
-      tc::prefetch_l2(p.s2 + (ia >> 8));
+      prefetch_l2(p.a8 + ia);
+      prefetch_l2(p.a8 + ia + nb - 1);
+      prefetch_l2(p.s2 + (ia >> 8));
     }
   }
   // level table: entry e, copy l at word 32 e + l (one conflict-free store per
