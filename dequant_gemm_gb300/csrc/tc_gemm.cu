@@ -81,9 +81,13 @@ struct Cfg {
   static constexpr int kGroups = 4;
   static constexpr int kDqWarps = 4 * kGroups;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
-  // the input gradient stages its A tile in shared memory as well
+  // The input gradient stages its A tile in shared memory as well, in a ring
+  // of its own: one slot per dequant group, freed by the stage's MMAs, while
+  // the copies run further ahead (a shared 5-deep ring left the MMA waiting
+  // on copy latency plus dequant every stage).
   static constexpr int kAStageBytes = kDx ? kTileRows * 64 * 2 : 0;
-  static constexpr int kStages = kDx ? (kBN == 64 ? 6 : 5) : (kBN == 64 ? 12 : 8);
+  static constexpr int kStages = kDx ? (kBN == 64 ? 8 : 6) : (kBN == 64 ? 12 : 8);
+  static constexpr int kASlots = kDx ? 4 : kStages;   // forward: the TMEM slot of the stage
   static constexpr int kBRows = kPair ? kBN / 2 : kBN;   // tokens staged per CTA
   static constexpr int kActStageBytes = kBRows * 128;    // 64 bf16 per token row
   static constexpr uint32_t kTmemA0 = kBN;
@@ -93,10 +97,10 @@ struct Cfg {
   static constexpr int kLutBytes = kHalfPairTableBytes;
   static constexpr int kOffAct = 0;
   static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
-  static constexpr int kOffCodes = kOffA + kStages * kAStageBytes;
+  static constexpr int kOffCodes = kOffA + kASlots * kAStageBytes;
   static constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
   static constexpr int kOffBars = kOffLut + kLutBytes;
-  static constexpr int kNumBars = 3 * kStages + 2;
+  static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   static_assert(kDx || kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
@@ -151,11 +155,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t bars = tc::smem_addr(smem + C::kOffBars);
+  constexpr int kASlots = C::kASlots;
+  // copy ring: full / empty per stage slot; A ring: dq (written) / afree
+  // (read by the MMAs; input gradient only) per A slot
   auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto dq_bar = [&](int s) { return bars + 8u * (kStages + s); };
-  auto empty_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
-  const uint32_t accum_bar = bars + 8u * (3 * kStages);
-  const uint32_t lut_bar = bars + 8u * (3 * kStages + 1);
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  auto dq_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
+  auto afree_bar = [&](int a) { return bars + 8u * (2 * kStages + kASlots + a); };
+  const uint32_t accum_bar = bars + 8u * (2 * kStages + 2 * kASlots);
+  const uint32_t lut_bar = accum_bar + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -171,9 +179,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full_bar(s), 1);
-      // one arrival per warp of the stage's group, in both CTAs of a pair
-      tc::mbar_init(dq_bar(s), 4 * kCg);
       tc::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kASlots; ++a) {
+      // one arrival per warp of the stage's group, in both CTAs of a pair
+      tc::mbar_init(dq_bar(a), 4 * kCg);
+      tc::mbar_init(afree_bar(a), 1);
     }
     tc::mbar_init(accum_bar, 1);
     tc::mbar_init(lut_bar, 1);
@@ -252,7 +263,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       const uint64_t adesc0 = tc::sw128_mnmajor_desc(tc::smem_addr(smem + C::kOffA), 1024, 2048);
       for (int i = 0; i < nst; ++i) {
         const int sl = i % kStages;
-        const bool ok = tc::mbar_wait_spin<kPair>(dq_bar(sl), (i / kStages) & 1);
+        const int as = i % kASlots;
+        const bool ok = tc::mbar_wait_spin<kPair>(dq_bar(as), (i / kASlots) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) fail(kRoleMma);
           break;
@@ -261,7 +273,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const uint32_t a = tmem + kTmemA0 + 32u * sl;
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
-        const uint64_t adesc = adesc0 + static_cast<uint64_t>(sl * (C::kAStageBytes >> 4));
+        const uint64_t adesc = adesc0 + static_cast<uint64_t>(as * (C::kAStageBytes >> 4));
         if (tc::elect_one()) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -273,6 +285,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
                                        (i | j) != 0 ? 1u : 0u);
           }
           tc::mma_commit<kCg>(empty_bar(sl));
+          if constexpr (kDx) tc::mma_commit<kCg>(afree_bar(as));
         }
         __syncwarp();
       }
@@ -284,9 +297,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   } else {
     // ---------------------------------------------------- dequant + store --
     // the stage's A slot is written: tell the pair's MMA thread
-    auto arrive_dq = [&](int slot) {
-      if constexpr (kPair) tc::mbar_arrive_remote(tc::mapa(dq_bar(slot), 0));
-      else tc::mbar_arrive(dq_bar(slot));
+    auto arrive_dq = [&](int a) {
+      if constexpr (kPair) tc::mbar_arrive_remote(tc::mapa(dq_bar(a), 0));
+      else tc::mbar_arrive(dq_bar(a));
     };
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int grp = (warp - 2) >> 2;        // takes the stages i % kGroups == grp
@@ -389,9 +402,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           fail(kRoleCompute);
           go = false;
         }
+        // the A slot's previous tile (stage i - kASlots) has been read by its MMAs
+        const int as = i % kASlots;
+        if (go && i >= kASlots && !tc::mbar_wait(afree_bar(as), ((i / kASlots) - 1) & 1)) {
+          fail(kRoleCompute);
+          go = false;
+        }
         if (!__all_sync(0xffffffffu, go)) continue;
         const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
-        uint8_t* arow = smem + C::kOffA + slot * C::kAStageBytes + ao;
+        uint8_t* arow = smem + C::kOffA + as * C::kAStageBytes + ao;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const uint4 c = *reinterpret_cast<const uint4*>(cst + (hf ? co1 : co0));
@@ -415,7 +434,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
         tc::fence_proxy_async();   // the MMA reads the tile through the async proxy
         __syncwarp();
-        if (lane == 0) arrive_dq(slot);
+        if (lane == 0) arrive_dq(as);
       }
     }
 
