@@ -211,35 +211,44 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      const uint32_t tx = static_cast<uint32_t>(kActStageBytes + kCodesStageBytes);
-      const int32_t m_load = static_cast<int32_t>(m0) + static_cast<int32_t>(rank) * C::kBRows;
-      int issued = 0;
-      for (int i = 0; i < nst && !*abort_flag; ++i) {
-        const int slot = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!tc::mbar_wait(empty_bar(slot), ph ^ 1)) { fail(kRoleProducer); break; }
-        const int s = s_begin + i;
+    // Like the MMA loop, the whole warp runs it on warp-uniform values and
+    // one elected lane issues the copies: from a one-thread branch a stage's
+    // expect_tx and two tensor copies took ~500 cycles, which paced the whole
+    // pipeline.
+    const uint32_t tx = static_cast<uint32_t>(kActStageBytes + kCodesStageBytes);
+    const int32_t m_load = static_cast<int32_t>(m0) + static_cast<int32_t>(rank) * C::kBRows;
+    int issued = 0;
+    for (int i = 0; i < nst; ++i) {
+      // one vote, so that the lanes leave together (a lane-wise read of the
+      // flag could split the warp ahead of the vote below)
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int slot = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(empty_bar(slot), ph ^ 1))) {
+        if (lane == 0) fail(kRoleProducer);
+        break;
+      }
+      const int s = s_begin + i;
+      const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
+      const uint32_t cod = tc::smem_addr(smem + C::kOffCodes + slot * kCodesStageBytes);
+      if (tc::elect_one()) {
         tc::mbar_arrive_expect_tx(full_bar(slot), tx);
-        const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
-        const uint32_t cod = tc::smem_addr(smem + C::kOffCodes + slot * kCodesStageBytes);
         tc::tma_load_2d(act, &tm_act, s * 64, m_load, full_bar(slot));
         if (!kDx) {
           // 128 rows x 32 bytes
           tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
         } else {
           // one 64-byte (128 columns) x 64-row box with the 64-byte swizzle:
-          // row r's 16-byte chunk c lands at r * 64 + 16 * (c ^ ((r >> 1) & 3)).
-          // One box issues a quarter of the row requests of four 16-byte-wide
-          // ones (measured: the narrow boxes held the stage rate back).
+          // row r's 16-byte chunk c lands at r * 64 + 16 * (c ^ ((r >> 1) & 3))
           tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(r0 / 2), s * 64, full_bar(slot));
         }
-        ++issued;
       }
-      if (*abort_flag) {  // let copies in flight land before the CTA exits
-        for (int i = max(0, issued - kStages); i < issued; ++i)
-          tc::mbar_wait(full_bar(i % kStages), (i / kStages) & 1);
-      }
+      __syncwarp();
+      ++issued;
+    }
+    if (*abort_flag && lane == 0) {  // let copies in flight land before the CTA exits
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        tc::mbar_wait(full_bar(i % kStages), (i / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
