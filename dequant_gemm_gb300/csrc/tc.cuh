@@ -199,7 +199,7 @@ __device__ __forceinline__ void fence_after_sync() {
 }
 
 // D[tmem] (+)= A[tmem] * B[smem descriptor]^T, bf16 inputs, fp32 accumulate.
-// With kCg = 2 the instruction is issued by one thread of the even CTA of a
+// With kCg = 2 the instruction is issued by one lane of the even CTA of a
 // pair and spans both SMs: each CTA holds half of the M rows of A and D in its
 // own tensor memory and half of the N rows of B at the same shared-memory
 // offset, and each SM's accumulator receives all N columns.

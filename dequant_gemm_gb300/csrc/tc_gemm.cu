@@ -8,8 +8,8 @@
 // 128-row A operand and the tokens as the BN-column B operand (BN = 64, 128 or
 // 256; 256 on CTA pairs that share one 256 x 256 MMA), looping over the
 // reduction in stages of 64:
-//   * warp 0 (one thread) TMA-loads the stage's activation tile (bf16,
-//     128-byte swizzle, the K-major B operand) and its packed-code tile;
+//   * warp 0 TMA-loads the stage's activation tile (bf16, 128-byte swizzle,
+//     the K-major B operand) and its packed-code tile from one elected lane;
 //   * the dequant warps, in four groups of four that take the stages in
 //     turn, dequantize the codes (level * dequantized absmax, rounded to
 //     bf16) into the stage's A operand;
