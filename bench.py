@@ -102,7 +102,71 @@ def quant_bytes(p):
 
 
 # --------------------------------------------------------------------- clocks --
+class NvmlClockSampler:
+    """SM clock and clock-event reasons, read through NVML (the driver's
+    libnvidia-ml, read-only queries) every ~1 ms from a thread, so that a timed
+    region of a few tens of milliseconds still gets samples of its own."""
+
+    # clock-event (throttle) reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML handle")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self.window = None
+        self.stop_flag = False
+        self.thread = None
+
+    def _poll(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag:
+            t = time.perf_counter()
+            if (self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ct.byref(clk)) == 0
+                    and self.reason_fn(self.handle, ct.byref(rs)) == 0):
+                self.samples.append((t, float(clk.value), int(rs.value)))
+            time.sleep(0.001)
+
+    def start(self):
+        import threading
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        time.sleep(0.01)   # polling before the timed region begins
+
+    def mark(self, t0, t1):
+        """The host-side bounds of the timed region."""
+        self.window = (t0, t1)
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        t0, t1 = self.window if self.window else (-1e30, 1e30)
+        inside = [(c, r) for (t, c, r) in self.samples if t0 <= t <= t1]
+        if not inside:
+            return None
+        reasons = sorted({name for _, r in inside for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside), "source": "nvml, ~1 ms"}
+
+
 class ClockSampler:
+    """nvidia-smi sampling every 200 ms (fallback when NVML cannot be loaded)."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -120,6 +184,9 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def mark(self, t0, t1):
+        pass
 
     def stop(self):
         if self.proc is None:
@@ -150,7 +217,14 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms"}
+
+
+def clock_sampler(index):
+    try:
+        return NvmlClockSampler(index)
+    except (OSError, AttributeError):
+        return ClockSampler(index)
 
 
 # -------------------------------------------------------------- our workload --
@@ -511,15 +585,17 @@ def main():
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ngraphs * args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index)
+    clocks = clock_sampler(dev.index)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
     t_start.record(stream)
     for s in range(args.steps):
         step.run(events[s * ngraphs:(s + 1) * ngraphs])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark(h0, time.perf_counter())
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
