@@ -1,0 +1,72 @@
+"""Host-side pieces of bench.py that need no GPU: the clock record keeps only
+samples taken inside the timed region and decodes the clock-event reason bits,
+and the sampler falls back to nvidia-smi when NVML cannot be loaded."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+class _FakeLib:
+    def __init__(self):
+        self.shutdown = 0
+
+    def nvmlShutdown(self):
+        self.shutdown += 1
+        return 0
+
+
+class _FakeThread:
+    def join(self, timeout=None):
+        pass
+
+
+def _sampler(samples, window):
+    s = object.__new__(bench.NvmlClockSampler)
+    s.lib = _FakeLib()
+    s.thread = _FakeThread()
+    s.stop_flag = False
+    s.max_mhz = 2070.0
+    s.samples = samples
+    s.window = window
+    return s
+
+
+def test_clock_record_keeps_only_the_timed_window_and_decodes_reasons():
+    samples = [
+        (0.5, 900.0, 0x1),          # before the window (idle): dropped
+        (1.0, 2070.0, 0x0),
+        (1.1, 1800.0, 0x4),         # sw_power_cap
+        (1.2, 1500.0, 0x4 | 0x8),   # + hw_slowdown
+        (2.5, 300.0, 0x40),         # after the window: dropped
+    ]
+    s = _sampler(samples, (1.0, 1.2))
+    rec = s.stop()
+    assert rec["samples"] == 3
+    assert rec["sm_mhz"] == 1800.0
+    assert rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert s.stop_flag and s.lib.shutdown == 1
+
+
+def test_clock_record_is_none_without_samples_in_the_window():
+    s = _sampler([(0.1, 2070.0, 0), (9.0, 2070.0, 0)], (1.0, 2.0))
+    assert s.stop() is None
+
+
+def test_thermal_reasons_are_named():
+    s = _sampler([(1.0, 1200.0, 0x20 | 0x40)], (0.0, 2.0))
+    assert s.stop()["reasons"] == ["hw_thermal_slowdown", "sw_thermal_slowdown"]
+
+
+def test_sampler_falls_back_to_nvidia_smi(monkeypatch):
+    class _NoNvml:
+        def __init__(self, index):
+            raise OSError("no libnvidia-ml")
+    monkeypatch.setattr(bench, "NvmlClockSampler", _NoNvml)
+    s = bench.clock_sampler(0)
+    assert isinstance(s, bench.ClockSampler)
+    s.mark(0.0, 1.0)   # accepted and ignored: nvidia-smi samples are not timestamped here
