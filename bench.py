@@ -545,6 +545,49 @@ METRIC = ("fused NF4 matmul TFLOP/s and HBM GB/s vs roofline; nf4_quantize GB/s 
           "(value: matmul FLOP of one layer step / device time of the step, quantization included)")
 
 
+def run_naive(args, dev):
+    """The fused NF4 forward against the naive path that the pages' speed claim
+    compares with: dequantize the whole weight to fp32 in HBM, cast it to bf16,
+    then a cuBLAS bf16 matmul (torch.matmul) widened to fp32. Same inputs, same
+    output shape and dtype. Both timed with CUDA events on the current stream
+    after 3 warm-ups, without an L2 flush (a weight smaller than L2 stays warm
+    for both). One JSON line for the workload."""
+    import dequant_gemm_gb300 as nf4
+    work = wl.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(dev)
+
+    def time_ms(fn, reps):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    rows = []
+    for p in work.projections:
+        W = p.make_weight().to(dev)
+        q = nf4.nf4_quantize(W)
+        del W
+        for M in work.fwd_m:
+            X = wl.activations(M, p.cols, std=work.x_std, seed=1 + M).to(dev)
+            t_fused = time_ms(lambda: nf4.nf4_matmul_fwd(X, q), args.steps)
+            t_naive = time_ms(
+                lambda: torch.matmul(X, nf4.nf4_dequantize(q).to(torch.bfloat16).t()).float(),
+                args.steps)
+            rows.append({"projection": f"{p.name} {p.rows}x{p.cols}", "M": M,
+                         "fused_ms": t_fused, "naive_ms": t_naive, "speedup": t_naive / t_fused})
+    status = nf4.nf4_poll_device_status(dev)
+    if status != 0:
+        raise SystemExit(f"device status {status}")
+    print(json.dumps({"metric": "fused NF4 forward vs dequantize-to-HBM + cuBLAS bf16 matmul",
+                      "config": {"workload": args.workload}, "steps": args.steps, "rows": rows}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -554,6 +597,8 @@ def main():
     ap.add_argument("--workload", default="qwen2.5_7b_layer", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--naive", action="store_true",
+                    help="time the fused forward against dequantize + cuBLAS instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
@@ -566,6 +611,8 @@ def main():
     torch.cuda.set_device(dev)
     import dequant_gemm_gb300 as nf4
     nf4.lib()
+    if args.naive:
+        return run_naive(args, dev)
 
     work = wl.WORKLOADS[args.workload]
     ws_bytes = sum(4 * p.rows * p.cols for p in work.projections)
