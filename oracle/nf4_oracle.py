@@ -37,7 +37,13 @@ docstring of the function that takes it.
 Parity status per function:
   nf4_levels        pinned (second inverse-CDF routine, forward CDF, invariants)
   nearest_code      pinned (exact rational brute force, midpoint counting)
+  quantize_codes    pinned (exact-rational IEEE quotient on every decision edge;
+                    a reciprocal multiply or the dequantized absmax fail it)
+  double_quant      pinned (exact halves round to even, exact multiply-then-
+                    divide chain; half-up and divide-first fail it)
   quantize_flat     pinned (special cases, round-trip bound, brute force)
+  dequant_absmax    pinned (exact product-then-quotient chain)
+  dequantize_codes  pinned (one exactly rounded product per weight)
   dequantize_flat   pinned (round-trip bound, special cases)
   matmul_fwd        pinned (one-hot rows, exact small integer case)
   matmul_bwd_dx     pinned (transpose identity against matmul_fwd, one-hot rows)
