@@ -545,6 +545,129 @@ METRIC = ("fused NF4 matmul TFLOP/s and HBM GB/s vs roofline; nf4_quantize GB/s 
           "(value: matmul FLOP of one layer step / device time of the step, quantization included)")
 
 
+# The single-GPU workloads beside the default one, each measured into a record
+# of its own in the same JSON line (the tiny 256x256 case is a parity case).
+CONFIG_WORKLOADS = ("decode_4096", "prefill_up_11008x4096", "bwd_down_4096x11008")
+
+
+def class_record(flop, nbytes, seconds, pk):
+    """Throughput of one kernel class over `seconds` of device time and its
+    place under the roofline: the HBM fraction, the tensor fractions against
+    the burst and the sustained bf16 peaks, and the fraction of the larger of
+    the two roofline times (bytes / copy bandwidth, FLOP / burst peak)."""
+    tf = flop / seconds / 1e12
+    gbs = nbytes / seconds / 1e9
+    t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tensor = flop / (pk["bf16_tflops"] * 1e12)
+    return {"TFLOP/s": tf, "GB/s": gbs, "hbm_frac": gbs / pk["hbm_gbs"],
+            "tensor_frac_burst": tf / pk["bf16_tflops"],
+            "tensor_frac_sustained": tf / pk["bf16_tflops_sustained"],
+            "bound": "tensor" if t_tensor > t_mem else "hbm",
+            "roofline_frac": max(t_mem, t_tensor) / seconds}
+
+
+def measure_workload(name, dev, steps, warmup, world, clocks=False):
+    """Build a workload's step, capture it, warm up, and time `steps` steps
+    with CUDA events around every kernel-class graph. Inputs larger than L2
+    are read once per step; smaller weight sets rotate over enough quantized
+    copies to exceed 3x L2."""
+    import dequant_gemm_gb300 as nf4
+    work = wl.WORKLOADS[name]
+    ws_bytes = sum(4 * p.rows * p.cols for p in work.projections)
+    rotate = 1 if ws_bytes > L2_BYTES else max(2, int(np.ceil(3 * L2_BYTES / sum(
+        packed_bytes(p.rows, p.cols) for p in work.projections))))
+    step = Step(name, dev, rotate=rotate)
+    stream = torch.cuda.current_stream(dev)
+    step.capture()
+    for _ in range(warmup):
+        step.run()
+    status, site = nf4.nf4_poll_device_status_site(dev)
+    if status != 0:
+        raise SystemExit(f"{name}: device status {status} after warm-up ({nf4.describe_site(site)})")
+
+    ngraphs = len(step.graphs)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ngraphs * steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = clock_sampler(dev.index) if clocks else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
+    t_start.record(stream)
+    for s in range(steps):
+        step.run(events[s * ngraphs:(s + 1) * ngraphs])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark(h0, time.perf_counter())
+    barrier(world)
+    clk = sampler.stop() if sampler else None
+    status, site = nf4.nf4_poll_device_status_site(dev)
+    if status != 0:
+        raise SystemExit(f"{name}: device status {status} after the timed steps ({nf4.describe_site(site)})")
+
+    cat_ms, cat_flop, cat_bytes, cat_n = {}, {}, {}, {}
+    for s in range(steps):
+        for j, (cat, idx, _) in enumerate(step.graphs):
+            e0, e1 = events[s * ngraphs + j]
+            cat_ms[cat] = cat_ms.get(cat, 0.0) + e0.elapsed_time(e1)
+            for k in idx:
+                _, f, b, n, _, _, _ = step.calls[k]
+                cat_flop[cat] = cat_flop.get(cat, 0) + f
+                cat_bytes[cat] = cat_bytes.get(cat, 0) + b
+                cat_n[cat] = cat_n.get(cat, 0) + n
+    pk, _ = peaks()
+    parts = {}
+    for cat in cat_ms:
+        rec = {"ms_per_step": cat_ms[cat] / steps, "launches_per_step": cat_n[cat] // steps}
+        rec.update(class_record(cat_flop[cat], cat_bytes[cat], cat_ms[cat] * 1e-3, pk))
+        parts[cat] = rec
+
+    # the same calls launched one by one from Python, without graphs
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step.run_eager()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_ms = e0.elapsed_time(e1) / steps
+    l2 = (("inputs larger than L2: %.2f GB of fp32 weights read per step" % (ws_bytes / 1e9))
+          if rotate == 1 else f"one step walks {rotate} quantized copies (> 3x L2)")
+    return {"work": work, "step": step, "elapsed_ms": t_start.elapsed_time(t_end), "parts": parts,
+            "clocks": clk, "l2": l2, "rotate": rotate, "eager_ms_per_step": eager_ms,
+            "steps": steps}
+
+
+def config_record(r):
+    """The record of one workload measured beside the default one."""
+    work, step = r["work"], r["step"]
+    steps_ms = r["elapsed_ms"]
+    rec = {"workload": work.name,
+           "projections": [f"{p.name} {p.rows}x{p.cols}" for p in work.projections],
+           "fwd_m": list(work.fwd_m), "dx_m": list(work.dx_m), "l2": r["l2"],
+           "timing": "CUDA graph per kernel class, CUDA events between graphs",
+           "graph_ms_per_step": steps_ms / r["steps"],
+           "eager_ms_per_step": r["eager_ms_per_step"],
+           "launches_per_step": step.launches(), "classes": {}}
+    for cat, p in r["parts"].items():
+        c = dict(p)
+        n = max(1, p["launches_per_step"])
+        c["us_per_launch"] = 1e3 * p["ms_per_step"] / n
+        bound = p["bound"]
+        c["roofline"] = ({"bound": "hbm", "achieved": p["GB/s"], "unit": "GB/s",
+                          "frac": p["hbm_frac"]} if bound == "hbm" else
+                         {"bound": "tensor", "achieved": p["TFLOP/s"], "unit": "TFLOP/s",
+                          "frac": p["tensor_frac_burst"],
+                          "frac_sustained": p["tensor_frac_sustained"]})
+        rec["classes"][cat] = c
+    if r["clocks"]:
+        rec["clocks"] = r["clocks"]
+    return rec
+
+
 def run_naive(args, dev):
     """The fused NF4 forward against the naive path that the pages' speed claim
     compares with: dequantize the whole weight to fp32 in HBM, cast it to bf16,
@@ -597,6 +720,8 @@ def main():
     ap.add_argument("--workload", default="qwen2.5_7b_layer", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload records (decode, prefill + quantize, dX)")
     ap.add_argument("--naive", action="store_true",
                     help="time the fused forward against dequantize + cuBLAS instead")
     args = ap.parse_args()
@@ -614,82 +739,33 @@ def main():
     if args.naive:
         return run_naive(args, dev)
 
-    work = wl.WORKLOADS[args.workload]
-    ws_bytes = sum(4 * p.rows * p.cols for p in work.projections)
-    rotate = 1 if ws_bytes > L2_BYTES else max(2, int(np.ceil(3 * L2_BYTES / sum(
-        packed_bytes(p.rows, p.cols) for p in work.projections))))
-    step = Step(args.workload, dev, rotate=rotate)
     stream = torch.cuda.current_stream(dev)
-
-    step.capture()
-    for i in range(args.warmup):
-        step.run()
-    status, site = nf4.nf4_poll_device_status_site(dev)
-    if status != 0:
-        raise SystemExit(f"device status {status} after warm-up ({nf4.describe_site(site)})")
-
-    ngraphs = len(step.graphs)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ngraphs * args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    clocks = clock_sampler(dev.index)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    h0 = time.perf_counter()
-    t_start.record(stream)
-    for s in range(args.steps):
-        step.run(events[s * ngraphs:(s + 1) * ngraphs])
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark(h0, time.perf_counter())
-    barrier(world)
-    clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    status, site = nf4.nf4_poll_device_status_site(dev)
-    if status != 0:
-        raise SystemExit(f"device status {status} after the timed steps ({nf4.describe_site(site)})")
-
-    # per-category device time from the per-call events
-    cat_ms, cat_flop, cat_bytes, cat_n = {}, {}, {}, {}
-    for s in range(args.steps):
-        for j, (cat, idx, _) in enumerate(step.graphs):
-            e0, e1 = events[s * ngraphs + j]
-            cat_ms[cat] = cat_ms.get(cat, 0.0) + e0.elapsed_time(e1)
-            for k in idx:
-                _, f, b, n, _, _, _ = step.calls[k]
-                cat_flop[cat] = cat_flop.get(cat, 0) + f
-                cat_bytes[cat] = cat_bytes.get(cat, 0) + b
-                cat_n[cat] = cat_n.get(cat, 0) + n
-
-    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    main_run = measure_workload(args.workload, dev, args.steps, args.warmup, world, clocks=True)
+    work, step = main_run["work"], main_run["step"]
+    elapsed_ms = max_over_ranks(main_run["elapsed_ms"], world, dev)
     ms_per_step = elapsed_ms / args.steps
     flop_step = step.flop()
     value = world * flop_step * args.steps / (elapsed_ms * 1e-3) / 1e12
 
     pk, pk_kind = peaks()
-    parts = {}
-    for cat in cat_ms:
-        t = cat_ms[cat] * 1e-3
-        gbs = cat_bytes[cat] / t / 1e9
-        tf = cat_flop[cat] / t / 1e12
-        parts[cat] = {"ms_per_step": cat_ms[cat] / args.steps, "launches_per_step": cat_n[cat] // args.steps,
-                      "TFLOP/s": tf, "GB/s": gbs,
-                      "hbm_frac": gbs / pk["hbm_gbs"],
-                      "tensor_frac": tf / pk["bf16_tflops_sustained"]}
-    dom = max(cat_ms, key=cat_ms.get)
+    parts = main_run["parts"]
+    dom = max(parts, key=lambda c: parts[c]["ms_per_step"])
     d = parts[dom]
-    tensor_bound = cat_flop[dom] / max(1, cat_bytes[dom]) > (1e3 * pk["bf16_tflops_sustained"] / pk["hbm_gbs"])
-    if cat_flop[dom] == 0 or not tensor_bound:
+    if d["bound"] == "hbm":
         roof = {"bound": "hbm", "achieved": d["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": d["GB/s"] / pk["hbm_gbs"]}
+                "frac": d["hbm_frac"]}
     else:
-        roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": d["TFLOP/s"] / pk["bf16_tflops_sustained"]}
+        roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": d["tensor_frac_burst"],
+                "frac_sustained": d["tensor_frac_sustained"],
+                "peak_sustained": pk["bf16_tflops_sustained"]}
     roof.update({"kernel": dom, "traffic": traffic_per_launch(work.name, dom),
                  "traffic_unit": "bytes per launch (ncu dram read+write)",
-                 "achieved_per": "launch-average over the class", "peak_kind": f"{pk_kind} ("
-                 + ("sustained bf16" if roof["bound"] == "tensor" else "copy") + ")"})
+                 "achieved_per": "launch-average over the class",
+                 "peak_kind": f"{pk_kind} " + (
+                     "burst bf16 (the class runs for well under a second at full clock); "
+                     "frac_sustained divides by the power-capped sustained figure"
+                     if roof["bound"] == "tensor" else "copy bandwidth")})
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -700,16 +776,18 @@ def main():
                    "projections": [f"{p.name} {p.rows}x{p.cols}" for p in work.projections],
                    "fwd_m": list(work.fwd_m), "dx_m": list(work.dx_m),
                    "quantize_in_step": step.quantize_in_step,
-                   "l2": ("inputs larger than L2: %.2f GB of fp32 weights read per step" % (ws_bytes / 1e9))
-                   if rotate == 1 else f"one step walks {rotate} quantized copies (> 3x L2)",
+                   "l2": main_run["l2"],
                    "timing": "CUDA graph per kernel class, CUDA events between graphs",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": step.launches() * args.steps,
         "roofline": roof,
         "parts": parts,
     }
-    if clk:
-        line["clocks"] = clk
+    if main_run["clocks"]:
+        line["clocks"] = main_run["clocks"]
+    line["peaks"] = {k: pk.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}
+    line["peaks"]["kind"] = pk_kind
+    line["peaks"]["sustained_sm_mhz_median"] = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
 
     if not args.no_e2e:
         h2d, d2h = step.host_buffers()
@@ -728,6 +806,19 @@ def main():
         line["e2e"] = {"value": world * flop_step * args.steps / (e2e_ms * 1e-3) / 1e12,
                        "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_ms / args.steps}
+
+    if not args.no_configs:
+        del step
+        main_run.clear()
+        torch.cuda.empty_cache()
+        line["configs"] = {}
+        for name in CONFIG_WORKLOADS:
+            if name == args.workload:
+                continue
+            r = measure_workload(name, dev, args.steps, args.warmup, world, clocks=True)
+            line["configs"][name] = config_record(r)
+            r.clear()
+            torch.cuda.empty_cache()
 
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores, secs = oracle_sample(args.workload, budget_s=20.0)

@@ -122,13 +122,46 @@ class NF4Weight:
         return self.codes.numel() + self.absmax_q.numel() + 4 * self.absmax_scale.numel()
 
 
-def _require_cuda(t: torch.Tensor, name: str, dtype: torch.dtype):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _require(t, name: str, dtype: torch.dtype, shape=None, numel=None):
+    """Dtype, contiguity and extent of one tensor argument (no device check)."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
+
+
+def _same_device(device: torch.device, **tensors):
+    for name, t in tensors.items():
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _require_cuda_device(device: torch.device):
+    """Checked last, after every shape and device-equality check, so that the
+    host-side checks can be exercised on CPU tensors."""
+    if device.type != "cuda":
+        raise ValueError(f"tensors must be on a CUDA device, got {device}")
+
+
+def _check_weight(w: "NF4Weight", device: torch.device):
+    """The three arrays of a quantized weight: dtypes, exact sizes for its
+    shape, contiguity, and the device of the call."""
+    if w.rows < 0 or w.cols < 0 or w.cols % BLOCKSIZE:
+        raise ValueError(f"weight shape {w.rows}x{w.cols}: cols must be a multiple of {BLOCKSIZE}")
+    n = w.rows * w.cols
+    nb = n // BLOCKSIZE
+    _require(w.codes, "weight.codes", torch.uint8, numel=n // 2)
+    _require(w.absmax_q, "weight.absmax_q", torch.uint8, numel=nb)
+    _require(w.absmax_scale, "weight.absmax_scale", torch.float32,
+             numel=(nb + DQ_GROUP - 1) // DQ_GROUP)
+    _same_device(device, **{"weight.codes": w.codes, "weight.absmax_q": w.absmax_q,
+                            "weight.absmax_scale": w.absmax_scale})
 
 
 def alloc_weight(rows: int, cols: int, device) -> NF4Weight:
@@ -142,10 +175,17 @@ def alloc_weight(rows: int, cols: int, device) -> NF4Weight:
 
 def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None) -> NF4Weight:
     """NF4-quantize an fp32 [rows, cols] CUDA tensor (blocksize 64, double quant)."""
-    _require_cuda(W, "W", torch.float32)
+    _require(W, "W", torch.float32)
     if W.dim() != 2:
         raise ValueError("W must be 2-D [rows, cols]")
     rows, cols = W.shape
+    if cols % BLOCKSIZE:
+        raise ValueError(f"cols = {cols} is not a multiple of {BLOCKSIZE}")
+    if out is not None:
+        if (out.rows, out.cols) != (rows, cols):
+            raise ValueError(f"out is a {out.rows}x{out.cols} weight, W is {rows}x{cols}")
+        _check_weight(out, W.device)
+    _require_cuda_device(W.device)
     q = out if out is not None else alloc_weight(rows, cols, W.device)
     with torch.cuda.device(W.device):
         _check("nf4_quantize", lib().nf4_quantize(
@@ -156,6 +196,11 @@ def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None) -> NF4Weight:
 
 def nf4_dequantize(w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tensor:
     """fp32 [rows, cols] dequantized weight (for checks and export only)."""
+    _check_weight(w, w.device)
+    if out is not None:
+        _require(out, "out", torch.float32, shape=(w.rows, w.cols))
+        _same_device(w.device, out=out)
+    _require_cuda_device(w.device)
     y = out if out is not None else torch.empty(w.rows, w.cols, dtype=torch.float32,
                                                 device=w.device)
     s = w.c_struct()
@@ -166,10 +211,15 @@ def nf4_dequantize(w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tenso
 
 def nf4_matmul_fwd(X: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tensor:
     """Y = X * dequant(W)^T; X bf16 [M, cols] -> Y fp32 [M, rows]."""
-    _require_cuda(X, "X", torch.bfloat16)
+    _require(X, "X", torch.bfloat16)
     if X.dim() != 2 or X.shape[1] != w.cols:
         raise ValueError(f"X must be [M, {w.cols}]")
     M = X.shape[0]
+    _check_weight(w, X.device)
+    if out is not None:
+        _require(out, "out", torch.float32, shape=(M, w.rows))
+        _same_device(X.device, out=out)
+    _require_cuda_device(X.device)
     y = out if out is not None else torch.empty(M, w.rows, dtype=torch.float32, device=X.device)
     s = w.c_struct()
     with torch.cuda.device(X.device):
@@ -181,10 +231,15 @@ def nf4_matmul_fwd(X: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = Non
 def nf4_matmul_bwd_dx(dY: torch.Tensor, w: NF4Weight,
                       out: torch.Tensor | None = None) -> torch.Tensor:
     """dX = dY * dequant(W); dY bf16 [M, rows] -> dX fp32 [M, cols]. No dW."""
-    _require_cuda(dY, "dY", torch.bfloat16)
+    _require(dY, "dY", torch.bfloat16)
     if dY.dim() != 2 or dY.shape[1] != w.rows:
         raise ValueError(f"dY must be [M, {w.rows}]")
     M = dY.shape[0]
+    _check_weight(w, dY.device)
+    if out is not None:
+        _require(out, "out", torch.float32, shape=(M, w.cols))
+        _same_device(dY.device, out=out)
+    _require_cuda_device(dY.device)
     y = out if out is not None else torch.empty(M, w.cols, dtype=torch.float32, device=dY.device)
     s = w.c_struct()
     with torch.cuda.device(dY.device):

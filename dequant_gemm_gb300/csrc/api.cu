@@ -125,7 +125,7 @@ nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, flo
   DeviceInfo* d = nullptr;
   if (nf4_status s = current_device(&d)) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (M <= kSmallMFwd)
+  if (M <= kSmallMFwd && w->cols <= nf4::kGemvMaxCols)
     return launched(nf4::launch_gemv_fwd(X, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,
                                          w->cols, Y, d->num_sms, d->status, st));
   return launched(nf4::launch_tc_fwd(X, M, w->codes, w->absmax_q, w->absmax_scale, w->rows,

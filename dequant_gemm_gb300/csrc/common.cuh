@@ -14,6 +14,10 @@ namespace nf4 {
 constexpr int kBlock = 64;                    // weights per absmax block
 constexpr int kGroup = 256;                   // blocks per second-level scale
 constexpr int kGroupElems = kBlock * kGroup;  // 16384 weights per group
+// Longest reduction the small-M forward takes: at most 8 K-slices (the
+// portable cluster size) of at most 96 blocks each. Longer rows go to the
+// tensor-core kernel.
+constexpr int64_t kGemvMaxCols = 8 * 96 * kBlock;
 
 // The 16 NF4 levels: standard-normal quantiles at evenly spaced probabilities
 // (8 on the positive side from delta = (1 - 1/30 + 1 - 1/32) / 2 to 1/2,

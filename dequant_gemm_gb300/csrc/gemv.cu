@@ -25,8 +25,11 @@
 //    sum is scaled by its dequantized absmax in fp32 afterwards. The levels
 //    enter the tensor core as fp16 (relative error <= 2^-12), which needs the
 //    activations in fp16 too: each token's slice of X is scaled by a power of
-//    two that puts its max |x| in [2^14, 2^15) before conversion (exact for
-//    bf16 values), and the scale is removed from the fp32 result.
+//    two that puts its max |x| in [2^14, 2^15) before conversion, and the
+//    scale is removed from the fp32 result. The conversion keeps every bit of
+//    a bf16 value that lands in fp16's normal range; values below about
+//    2^-28 of the slice's max |x| become fp16 subnormals and lose low bits
+//    (their share of the sum is below 2^-28 of the largest term).
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
 //    that every lookup of a warp hits 32 distinct banks. Each CTA lays the
@@ -58,6 +61,7 @@ constexpr int kTabBytes = kHalfPairTableBytes;
 constexpr int kMaxSliceBlocks = 96;
 constexpr int kMaxCluster = 8;
 constexpr int kOutStride = kGemvRows + 4;       // floats, keeps rows 16-byte aligned
+static_assert(kMaxCluster * kMaxSliceBlocks * kBlock == kGemvMaxCols, "K limit");
 
 // fp16 bits of level i (0 <= i < 16) as a select tree over immediates: no
 // memory access, so the table set-up does not wait on a constant-cache miss.
@@ -202,6 +206,11 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     tc::prefetch_tensormap(&tm_codes);
   }
   __syncwarp();
+  // First half of a split cluster barrier: the CTAs of a cluster store into
+  // one another's shared memory at the end, which is only allowed once every
+  // CTA of the cluster has started; the matching wait sits just before those
+  // stores, so the barrier costs nothing on the way.
+  if (p.slices > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Activations first, ahead of the code stream: warp w copies token w of
@@ -260,7 +269,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   if (nmine > 1) issue_box(1);
 
   // max |x| over the slice -> power-of-two scale into [2^14, 2^15) -> fp16
-  // (exact for bf16 inputs)
+  // (bit-preserving down to fp16's normal range, see the file comment)
   if (warp < mt) {
     float mx = xmax;
 #pragma unroll
@@ -434,6 +443,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     // visible, and each owner sums its slots and writes Y once.
     const int rpc = kGemvRows / p.slices;          // rows owned per CTA (a power of two)
     const int rpc_shift = 31 - __clz(rpc);
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer has started
     if (kh == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {

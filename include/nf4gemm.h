@@ -104,9 +104,17 @@ nf4_status nf4_dequantize(const nf4_weight* w, float* W_out, void* stream);
  * only in registers, shared memory and tensor memory.
  *   X  device bf16 (raw uint16 bits) [M, cols]
  *   Y  device fp32 [M, rows] (output, overwritten)
- * Requires rows % 8 == 0. Accuracy against an fp64 dequantize-then-multiply:
- * relative Frobenius error <= 2e-3 and max error <= 5e-3 * max|Y_ref|
- * (weights enter the tensor cores as bf16). */
+ * Requires rows % 8 == 0; any cols that is a multiple of 64 is accepted.
+ * M <= 16 with cols <= 49152 runs the streaming small-M kernel, every other
+ * shape the tensor-core kernel. Accuracy against an fp64
+ * dequantize-then-multiply: relative Frobenius error <= 2e-3 and max error
+ * <= 5e-3 * max|Y_ref| (weights enter the tensor cores as bf16, or as fp16
+ * levels with the block scale applied in fp32 on the small-M kernel).
+ * Determinism: when the output tiles alone cannot fill the GPU the reduction
+ * is split across CTAs and the partial sums are added into Y with fp32
+ * atomics, in an order that varies between runs, so the low bits of Y can
+ * differ between identical calls. The small-M kernel reduces its splits in
+ * a fixed order and is bitwise repeatable. */
 nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, float* Y,
                           void* stream);
 
@@ -115,7 +123,9 @@ nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, flo
  * computed).
  *   dY device bf16 (raw uint16 bits) [M, rows]
  *   dX device fp32 [M, cols] (output, overwritten)
- * Requires rows % 8 == 0. Same accuracy statement as nf4_matmul_fwd. */
+ * Requires rows % 8 == 0. Same accuracy statement as nf4_matmul_fwd, and
+ * the same determinism note: split reductions (small grids, and M <= 16)
+ * add partial sums with atomics. */
 nf4_status nf4_matmul_bwd_dx(const uint16_t* dY, int64_t M, const nf4_weight* w, float* dX,
                              void* stream);
 
