@@ -29,7 +29,11 @@ Sources (page title, section):
 * same page, double-quantization paragraph: absmax per 64-weight block, the
   absmax vector itself quantized to 8 bits with its own scale; at dequant time
   the scales are dequantized first, then the weights.
-* same page, quantized-GEMM paragraph: dequantize on the fly, fp32 output.
+* same page, quantized-GEMM paragraph: dequantize on the fly, fp32 output;
+  weights int8 or 4-bit, activations float16/float32.
+* same page, 4-bit paragraph: NF4 or FP4 (standard floating-point 4-bit) data
+  types with double quantization of the scales.
+* "Zenbit", ``zenbit.int8`` bullet: uniform int8 weight quantization.
 
 Where the pages leave a step open, the reading taken is stated in the
 docstring of the function that takes it.
@@ -47,6 +51,14 @@ Parity status per function:
   dequantize_flat   pinned (round-trip bound, special cases)
   matmul_fwd        pinned (one-hot rows, exact small integer case)
   matmul_bwd_dx     pinned (transpose identity against matmul_fwd, one-hot rows)
+  fp4_levels        pinned (E2M1 decode from the format definition, exact)
+  quantize_flat / dequantize_flat with the FP4 table
+                    pinned (exact brute-force nearest incl. the signed-zero tie,
+                    special cases, round-trip bound)
+  int8_quantize_flat, int8_dequantize_flat
+                    pinned (exact multiply-then-divide chain, halves to even,
+                    range, round-trip bound, memory invariant)
+  bf16_to_fp32      pinned (all 65536 bit patterns against torch's conversion)
 """
 from __future__ import annotations
 
@@ -90,6 +102,43 @@ def nf4_levels() -> np.ndarray:
     return nf4_levels_fp64().astype(np.float32)
 
 
+def fp4_levels() -> np.ndarray:
+    """The 16 FP4 levels, indexed by the 4-bit code (fp32).
+
+    The "bitsandbytes" page names FP4 "standard floating-point 4-bit" beside
+    NF4, with the same blockwise scaling and double quantization. Reading
+    taken: the E2M1 layout, code = sign (bit 3) | exponent (bits 2-1) |
+    mantissa (bit 0), exponent bias 1, exponent 0 subnormal:
+      magnitude = m / 2                     if e == 0
+                = 2^(e-1) * (1 + m / 2)     otherwise,
+    i.e. 0, 0.5, 1, 1.5, 2, 3, 4, 6; normalised to [-1, 1] by the largest
+    magnitude 6 like the NF4 levels. Computed in fp64 and rounded once to
+    fp32 (the thirds have non-terminating binary expansions, so no fp32 tie
+    arises for the double rounding to break). Code 8 is -0.0.
+    """
+    out = np.empty(16, dtype=np.float64)
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        mag = m / 2.0 if e == 0 else 2.0 ** (e - 1) * (1.0 + m / 2.0)
+        out[code] = (-mag if s else mag) / 6.0
+    return out.astype(np.float32)
+
+
+def levels_of(dtype: str) -> np.ndarray:
+    """The fp32 table of a 4-bit data type ("nf4" or "fp4")."""
+    if dtype == "nf4":
+        return nf4_levels()
+    if dtype == "fp4":
+        return fp4_levels()
+    raise ValueError(f"no 4-bit table for {dtype!r}")
+
+
+def zero_code(levels: np.ndarray) -> int:
+    """The code an all-zero block gets: the first index holding level 0
+    (NF4: 7; FP4: 0, ahead of -0.0 at 8)."""
+    return int(np.flatnonzero(levels == 0)[0])
+
+
 # --------------------------------------------------------------------------
 # Quantization
 # --------------------------------------------------------------------------
@@ -116,23 +165,26 @@ def block_absmax(w_flat: np.ndarray) -> np.ndarray:
     return np.max(np.abs(w_flat.reshape(-1, BLOCKSIZE)), axis=1).astype(np.float32)
 
 
-def quantize_codes(w_flat: np.ndarray, absmax: np.ndarray) -> np.ndarray:
-    """4-bit codes of every weight: nearest NF4 level of w / absmax.
+def quantize_codes(w_flat: np.ndarray, absmax: np.ndarray,
+                   levels: np.ndarray | None = None) -> np.ndarray:
+    """4-bit codes of every weight: nearest level of w / absmax (NF4 table
+    unless another 4-bit table is given).
 
     Readings taken: the normalisation is the IEEE fp32 quotient
     fl32(w / absmax) with the block's true fp32 absmax (the scale is computed
     first and only then double-quantized); a block whose absmax is 0 has all
-    codes 7, the index of the exact zero level.
+    codes equal to the index of the exact zero level (7 for NF4).
     """
+    lv = nf4_levels() if levels is None else levels
     blocks = w_flat.reshape(-1, BLOCKSIZE).astype(np.float32)
-    codes = np.full(blocks.shape, 7, dtype=np.uint8)
+    codes = np.full(blocks.shape, zero_code(lv), dtype=np.uint8)
     nz = absmax > 0
     rows = np.flatnonzero(nz)
     step = 1 << 12                                # bounded temporaries
     for i0 in range(0, rows.size, step):
         r = rows[i0:i0 + step]
         x = blocks[r] / absmax[r, None]           # float32 / float32: IEEE RN
-        codes[r] = nearest_code(x)
+        codes[r] = nearest_code(x, lv)
     return codes.reshape(-1)
 
 
@@ -175,8 +227,9 @@ def double_quant(absmax: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return a8, s2
 
 
-def quantize_flat(w_flat: np.ndarray):
-    """NF4 + double-quant of a row-major flattened fp32 weight.
+def quantize_flat(w_flat: np.ndarray, levels: np.ndarray | None = None):
+    """NF4 (or, given its table, FP4) + double-quant of a row-major flattened
+    fp32 weight.
 
     Blocks of 64 and groups of 256 blocks run over the flattened weight.
     Returns (packed codes uint8 [n/2], a8 uint8 [n/64], s2 fp32 [ceil(n/16384)]).
@@ -186,14 +239,14 @@ def quantize_flat(w_flat: np.ndarray):
     w = np.ascontiguousarray(w_flat, dtype=np.float32).reshape(-1)
     assert w.size % BLOCKSIZE == 0
     absmax = block_absmax(w)
-    codes = quantize_codes(w, absmax)
+    codes = quantize_codes(w, absmax, levels)
     a8, s2 = double_quant(absmax)
     return pack_nibbles(codes), a8, s2
 
 
-def quantize(W: np.ndarray):
+def quantize(W: np.ndarray, levels: np.ndarray | None = None):
     """quantize_flat over W [rows, cols] in row-major order."""
-    return quantize_flat(np.asarray(W, dtype=np.float32).reshape(-1))
+    return quantize_flat(np.asarray(W, dtype=np.float32).reshape(-1), levels)
 
 
 # --------------------------------------------------------------------------
@@ -210,22 +263,70 @@ def dequant_absmax(a8: np.ndarray, s2: np.ndarray) -> np.ndarray:
     return (prod / np.float32(255.0)).astype(np.float32)
 
 
-def dequantize_codes(codes: np.ndarray, ahat: np.ndarray) -> np.ndarray:
+def dequantize_codes(codes: np.ndarray, ahat: np.ndarray,
+                     levels: np.ndarray | None = None) -> np.ndarray:
     """Weights second: what = fl32(c[q] * ahat) for codes [nblocks, 64] and the
     blocks' dequantized absmax [nblocks] (fp32 [nblocks, 64])."""
-    lv = nf4_levels()
+    lv = nf4_levels() if levels is None else levels
     q = np.asarray(codes, dtype=np.uint8).reshape(-1, BLOCKSIZE)
     return (lv[q] * np.asarray(ahat, dtype=np.float32)[:, None]).astype(np.float32)
 
 
-def dequantize_flat(packed: np.ndarray, a8: np.ndarray, s2: np.ndarray) -> np.ndarray:
+def dequantize_flat(packed: np.ndarray, a8: np.ndarray, s2: np.ndarray,
+                    levels: np.ndarray | None = None) -> np.ndarray:
     """Dequantize a whole flat weight (fp32 [n])."""
     ahat = dequant_absmax(a8, s2)
-    return dequantize_codes(unpack_nibbles(packed), ahat).reshape(-1)
+    return dequantize_codes(unpack_nibbles(packed), ahat, levels).reshape(-1)
 
 
-def dequantize(packed, a8, s2, rows: int, cols: int) -> np.ndarray:
-    return dequantize_flat(packed, a8, s2).reshape(rows, cols)
+def dequantize(packed, a8, s2, rows: int, cols: int,
+               levels: np.ndarray | None = None) -> np.ndarray:
+    return dequantize_flat(packed, a8, s2, levels).reshape(rows, cols)
+
+
+# --------------------------------------------------------------------------
+# Uniform int8 weight quantization
+# --------------------------------------------------------------------------
+def int8_quantize_flat(w_flat: np.ndarray):
+    """Uniform symmetric int8 quantization per 64-weight block ("Zenbit",
+    zenbit.int8 bullet: uniform int8 weight quantization; "bitsandbytes",
+    CPU paragraph: int8 dequantization with per-block scaling factors).
+
+    Readings taken: the block is the NF4 path's 64-weight block over the
+    row-major flattened weight; a = max |w| of the block, kept in fp32 (no
+    double quantization); q = rint(fl32(fl32(127 w) / a)), the multiply
+    first and round-half-to-even as in the double quantization; q = 0 when
+    a = 0. Returns (q int8 [n], a fp32 [n/64]).
+    """
+    w = np.ascontiguousarray(w_flat, dtype=np.float32).reshape(-1, BLOCKSIZE)
+    a = block_absmax(w)
+    q = np.zeros(w.shape, dtype=np.int8)
+    nz = np.flatnonzero(a > 0)
+    step = 1 << 14
+    for i0 in range(0, nz.size, step):
+        r = nz[i0:i0 + step]
+        t = (np.float32(127.0) * w[r]) / a[r, None]      # fp32 RN, multiply first
+        q[r] = np.rint(t).astype(np.int8)
+    return q.reshape(-1), a
+
+
+def int8_dequantize_flat(q: np.ndarray, absmax: np.ndarray) -> np.ndarray:
+    """what = fl32(fl32(q * a) / 127): the inverse of int8_quantize_flat,
+    each operation rounded to fp32 (fp32 [n])."""
+    qb = np.asarray(q, dtype=np.int8).reshape(-1, BLOCKSIZE).astype(np.float32)
+    prod = qb * np.asarray(absmax, dtype=np.float32)[:, None]
+    return (prod / np.float32(127.0)).astype(np.float32).reshape(-1)
+
+
+# --------------------------------------------------------------------------
+# bf16 inputs
+# --------------------------------------------------------------------------
+def bf16_to_fp32(bits: np.ndarray) -> np.ndarray:
+    """The fp32 value of each bf16 bit pattern: bf16 is the upper half of an
+    fp32 (sign, 8 exponent bits, 7 fraction bits), so the value is exact.
+    A bf16 weight is quantized as this fp32 weight."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)
 
 
 # --------------------------------------------------------------------------
