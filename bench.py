@@ -82,23 +82,36 @@ def peaks():
 
 
 # ----------------------------------------------------------- work accounting --
-def packed_bytes(rows, cols):
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+ELEM_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+def packed_bytes(rows, cols, wdtype="nf4"):
+    """Stored bytes of a quantized weight: 4-bit codes + uint8 absmax codes +
+    fp32 group scales, or int8 values + fp32 block absmax."""
     n = rows * cols
     nb = n // 64
+    if wdtype == "int8":
+        return n + 4 * nb
     return n // 2 + nb + 4 * ((nb + 255) // 256)
 
 
-def fwd_work(p, M):
+def fwd_work(p, M, w=None):
     """(flop, algorithmic bytes) of Y = X W^T: packed W + X in + Y out."""
-    return 2 * M * p.rows * p.cols, packed_bytes(p.rows, p.cols) + 2 * M * p.cols + 4 * M * p.rows
+    wd, a, o = (w.wdtype, w.act, w.out) if w else ("nf4", "bf16", "f32")
+    return 2 * M * p.rows * p.cols, (packed_bytes(p.rows, p.cols, wd) + ELEM_BYTES[a] * M * p.cols
+                                     + ELEM_BYTES[o] * M * p.rows)
 
 
-def dx_work(p, M):
-    return 2 * M * p.rows * p.cols, packed_bytes(p.rows, p.cols) + 2 * M * p.rows + 4 * M * p.cols
+def dx_work(p, M, w=None):
+    wd, a, o = (w.wdtype, w.act, w.out) if w else ("nf4", "bf16", "f32")
+    return 2 * M * p.rows * p.cols, (packed_bytes(p.rows, p.cols, wd) + ELEM_BYTES[a] * M * p.rows
+                                     + ELEM_BYTES[o] * M * p.cols)
 
 
-def quant_bytes(p):
-    return 4 * p.rows * p.cols + packed_bytes(p.rows, p.cols)
+def quant_bytes(p, w=None):
+    wd, wi = (w.wdtype, w.w_in) if w else ("nf4", "f32")
+    return ELEM_BYTES[wi] * p.rows * p.cols + packed_bytes(p.rows, p.cols, wd)
 
 
 # --------------------------------------------------------------------- clocks --
@@ -243,23 +256,29 @@ class Step:
         self.dy = {}            # (N, M) -> bf16 output gradients
         self.y = {}             # (proj index, M) -> fp32 outputs
         self.dx = {}
+        w = self.w
+        act_dt, out_dt = TORCH_DT[w.act], TORCH_DT[w.out]
         for i, p in enumerate(self.w.projections):
-            W = p.make_weight().to(device)
+            W = p.make_weight().to(TORCH_DT[w.w_in]).to(device)
             self.weights.append(W)
+        # with rotation, every copy of the quantized weight has its own copy of
+        # the input weight, so that quantize also reads from HBM
+        self.wcopies = [self.weights] + [[W.clone() for W in self.weights] for _ in range(rotate - 1)]
         for r in range(rotate):
-            self.q.append([nf4.nf4_quantize(W) for W in self.weights])
+            self.q.append([nf4.nf4_quantize(W, dtype=w.wdtype) for W in self.wcopies[r]])
         for i, p in enumerate(self.w.projections):
             for M in self.w.fwd_m:
                 if (p.cols, M) not in self.x:
                     self.x[(p.cols, M)] = wl.activations(M, p.cols, std=self.w.x_std,
-                                                         seed=wl.SEED_X + M).to(device)
-                self.y[(i, M)] = torch.empty(M, p.rows, dtype=torch.float32, device=device)
+                                                         seed=wl.SEED_X + M, dtype=act_dt).to(device)
+                self.y[(i, M)] = torch.empty(M, p.rows, dtype=out_dt, device=device)
             for M in self.w.dx_m:
                 if (p.rows, M) not in self.dy:
                     self.dy[(p.rows, M)] = wl.activations(M, p.rows, std=self.w.dy_std,
-                                                          seed=wl.SEED_X + 7 + M).to(device)
-                self.dx[(i, M)] = torch.empty(M, p.cols, dtype=torch.float32, device=device)
-        self.quantize_in_step = rotate == 1
+                                                          seed=wl.SEED_X + 7 + M,
+                                                          dtype=act_dt).to(device)
+                self.dx[(i, M)] = torch.empty(M, p.cols, dtype=out_dt, device=device)
+        self.quantize_in_step = True
         self.calls = self._calls()
         self.side = []
         self.graphs = None
@@ -274,17 +293,18 @@ class Step:
         calls = []
         P = self.w.projections
         groups = self.w.issue_groups()
-        if self.quantize_in_step:
+        for r in range(self.rotate):
             for i, p in enumerate(P):
-                calls.append(("quantize", 0, quant_bytes(p), 1,
-                              lambda i=i: nf4.nf4_quantize(self.weights[i], out=self.q[0][i]),
-                              ("quantize", 0), i))
+                calls.append(("quantize", 0, quant_bytes(p, self.w), 1,
+                              lambda r=r, i=i: nf4.nf4_quantize(self.wcopies[r][i], out=self.q[r][i],
+                                                                dtype=self.w.wdtype),
+                              ("quantize", r), i))
         for M in sorted(self.w.fwd_m, reverse=True):
             for r in range(self.rotate):
                 for gi, g in enumerate(groups):
                     for i in g:
                         p = P[i]
-                        f, b = fwd_work(p, M)
+                        f, b = fwd_work(p, M, self.w)
                         calls.append((f"fwd_M{M}", f, b, 1,
                                       lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_fwd(
                                           self.x[(p.cols, M)], self.q[r][i], out=self.y[(i, M)]),
@@ -294,7 +314,7 @@ class Step:
                 for gi, g in enumerate(groups):
                     for i in g:
                         p = P[i]
-                        f, b = dx_work(p, M)
+                        f, b = dx_work(p, M, self.w)
                         calls.append((f"dx_M{M}", f, b, 1,
                                       lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_bwd_dx(
                                           self.dy[(p.rows, M)], self.q[r][i], out=self.dx[(i, M)]),
@@ -547,7 +567,10 @@ METRIC = ("fused NF4 matmul TFLOP/s and HBM GB/s vs roofline; nf4_quantize GB/s 
 
 # The single-GPU workloads beside the default one, each measured into a record
 # of its own in the same JSON line (the tiny 256x256 case is a parity case).
-CONFIG_WORKLOADS = ("decode_4096", "prefill_up_11008x4096", "bwd_down_4096x11008")
+CONFIG_WORKLOADS = ("decode_4096", "prefill_up_11008x4096", "bwd_down_4096x11008",
+                    "prefill_up_11008x4096_bf16", "bwd_down_4096x11008_f16",
+                    "decode_4096_fp4", "decode_4096_int8", "prefill_up_11008x4096_fp4",
+                    "prefill_up_11008x4096_int8")
 
 
 def class_record(flop, nbytes, seconds, pk):
@@ -573,9 +596,9 @@ def measure_workload(name, dev, steps, warmup, world, clocks=False):
     copies to exceed 3x L2."""
     import dequant_gemm_gb300 as nf4
     work = wl.WORKLOADS[name]
-    ws_bytes = sum(4 * p.rows * p.cols for p in work.projections)
+    ws_bytes = sum(ELEM_BYTES[work.w_in] * p.rows * p.cols for p in work.projections)
     rotate = 1 if ws_bytes > L2_BYTES else max(2, int(np.ceil(3 * L2_BYTES / sum(
-        packed_bytes(p.rows, p.cols) for p in work.projections))))
+        packed_bytes(p.rows, p.cols, work.wdtype) for p in work.projections))))
     step = Step(name, dev, rotate=rotate)
     stream = torch.cuda.current_stream(dev)
     step.capture()
@@ -634,7 +657,7 @@ def measure_workload(name, dev, steps, warmup, world, clocks=False):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     eager_ms = e0.elapsed_time(e1) / steps
-    l2 = (("inputs larger than L2: %.2f GB of fp32 weights read per step" % (ws_bytes / 1e9))
+    l2 = (("inputs larger than L2: %.2f GB of weights read per step" % (ws_bytes / 1e9))
           if rotate == 1 else f"one step walks {rotate} quantized copies (> 3x L2)")
     return {"work": work, "step": step, "elapsed_ms": t_start.elapsed_time(t_end), "parts": parts,
             "clocks": clk, "l2": l2, "rotate": rotate, "eager_ms_per_step": eager_ms,
@@ -647,6 +670,8 @@ def config_record(r):
     steps_ms = r["elapsed_ms"]
     rec = {"workload": work.name,
            "projections": [f"{p.name} {p.rows}x{p.cols}" for p in work.projections],
+           "weight_format": work.wdtype, "weight_in": work.w_in, "activations": work.act,
+           "outputs": work.out,
            "fwd_m": list(work.fwd_m), "dx_m": list(work.dx_m), "l2": r["l2"],
            "timing": "CUDA graph per kernel class, CUDA events between graphs",
            "graph_ms_per_step": steps_ms / r["steps"],

@@ -29,22 +29,32 @@ STATUS = {
 }
 
 # Every symbol the header declares, for load checks.
-EXPORTS = ("nf4_quantize", "nf4_dequantize", "nf4_matmul_fwd", "nf4_matmul_bwd_dx",
+EXPORTS = ("nf4_quantize", "nf4_quantize_ex", "nf4_dequantize", "nf4_matmul_fwd",
+           "nf4_matmul_bwd_dx", "nf4_matmul_fwd_ex", "nf4_matmul_bwd_dx_ex",
            "nf4_poll_device_status", "nf4_poll_device_status_site", "nf4_codebook",
+           "nf4_codebook_of", "nf4_set_mma_wait_limit", "nf4_last_cuda_error",
            "nf4_status_string")
+
+# Weight data types (nf4_dtype) and element types (nf4_elem) of the C ABI.
+DTYPES = {"nf4": 0, "fp4": 1, "int8": 2}
+ELEM = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+ACCUMULATE = 1
 
 
 class NF4Error(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: {STATUS.get(status, status)} ({status_string(status)})")
+        msg = f"{fn}: {STATUS.get(status, status)} ({status_string(status)})"
+        if status == 6:
+            msg += f": {lib().nf4_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 class nf4_weight(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("absmax_q", ctypes.c_void_p),
                 ("absmax_scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
                 ("cols", ctypes.c_int64), ("blocksize", ctypes.c_int32),
-                ("dq_group", ctypes.c_int32)]
+                ("dq_group", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 _lib = None
@@ -65,12 +75,17 @@ def lib() -> ctypes.CDLL:
             W = ctypes.POINTER(nf4_weight)
             sig = {
                 "nf4_quantize": [vp, i64, i64, i32, vp, vp, vp, vp],
+                "nf4_quantize_ex": [vp, i32, i64, i64, i32, i32, vp, vp, vp, vp],
                 "nf4_dequantize": [W, vp, vp],
                 "nf4_matmul_fwd": [vp, i64, W, vp, vp],
                 "nf4_matmul_bwd_dx": [vp, i64, W, vp, vp],
+                "nf4_matmul_fwd_ex": [vp, i32, i64, W, vp, i32, i32, vp],
+                "nf4_matmul_bwd_dx_ex": [vp, i32, i64, W, vp, i32, i32, vp],
                 "nf4_poll_device_status": [vp],
                 "nf4_poll_device_status_site": [vp, vp],
                 "nf4_codebook": [vp],
+                "nf4_codebook_of": [i32, vp],
+                "nf4_set_mma_wait_limit": [i64],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -78,6 +93,8 @@ def lib() -> ctypes.CDLL:
                 f.restype = ctypes.c_int32
             L.nf4_status_string.argtypes = [ctypes.c_int32]
             L.nf4_status_string.restype = ctypes.c_char_p
+            L.nf4_last_cuda_error.argtypes = []
+            L.nf4_last_cuda_error.restype = ctypes.c_char_p
             _lib = L
         return _lib
 
@@ -101,25 +118,34 @@ def _stream(device: torch.device):
 
 @dataclass
 class NF4Weight:
-    """A quantized weight: codes, absmax codes, second-level scales, shape
-    (the QuantState of the bitsandbytes page). Plain tensors; save them with
-    torch.save."""
-    codes: torch.Tensor          # uint8 [rows*cols/2]
-    absmax_q: torch.Tensor       # uint8 [rows*cols/64]
-    absmax_scale: torch.Tensor   # float32 [ceil(rows*cols/16384)]
+    """A quantized weight: codes, scales, shape and data type (the QuantState
+    of the bitsandbytes page). Plain tensors; save them with torch.save.
+
+    dtype "nf4" / "fp4": codes uint8 [rows*cols/2] (two 4-bit codes a byte),
+    absmax_q uint8 [rows*cols/64], absmax_scale float32 [ceil(rows*cols/16384)].
+    dtype "int8": codes int8 [rows*cols], absmax_q None, absmax_scale float32
+    [rows*cols/64] (the fp32 absmax of each 64-weight block)."""
+    codes: torch.Tensor
+    absmax_q: torch.Tensor | None
+    absmax_scale: torch.Tensor
     rows: int
     cols: int
+    dtype: str = "nf4"
 
     def c_struct(self) -> nf4_weight:
-        return nf4_weight(self.codes.data_ptr(), self.absmax_q.data_ptr(),
-                          self.absmax_scale.data_ptr(), self.rows, self.cols, BLOCKSIZE, DQ_GROUP)
+        four = self.dtype != "int8"
+        return nf4_weight(self.codes.data_ptr(),
+                          self.absmax_q.data_ptr() if four else None,
+                          self.absmax_scale.data_ptr(), self.rows, self.cols, BLOCKSIZE,
+                          DQ_GROUP if four else 0, DTYPES[self.dtype])
 
     @property
     def device(self) -> torch.device:
         return self.codes.device
 
     def nbytes(self) -> int:
-        return self.codes.numel() + self.absmax_q.numel() + 4 * self.absmax_scale.numel()
+        n = self.codes.numel() * self.codes.element_size() + 4 * self.absmax_scale.numel()
+        return n + (self.absmax_q.numel() if self.absmax_q is not None else 0)
 
 
 def _require(t, name: str, dtype: torch.dtype, shape=None, numel=None):
@@ -150,12 +176,21 @@ def _require_cuda_device(device: torch.device):
 
 
 def _check_weight(w: "NF4Weight", device: torch.device):
-    """The three arrays of a quantized weight: dtypes, exact sizes for its
-    shape, contiguity, and the device of the call."""
+    """The arrays of a quantized weight: dtypes, exact sizes for its shape and
+    data type, contiguity, and the device of the call."""
+    if w.dtype not in DTYPES:
+        raise ValueError(f"unknown weight dtype {w.dtype!r}; expected one of {sorted(DTYPES)}")
     if w.rows < 0 or w.cols < 0 or w.cols % BLOCKSIZE:
         raise ValueError(f"weight shape {w.rows}x{w.cols}: cols must be a multiple of {BLOCKSIZE}")
     n = w.rows * w.cols
     nb = n // BLOCKSIZE
+    if w.dtype == "int8":
+        _require(w.codes, "weight.codes", torch.int8, numel=n)
+        if w.absmax_q is not None:
+            raise ValueError("an int8 weight has no absmax_q")
+        _require(w.absmax_scale, "weight.absmax_scale", torch.float32, numel=nb)
+        _same_device(device, **{"weight.codes": w.codes, "weight.absmax_scale": w.absmax_scale})
+        return
     _require(w.codes, "weight.codes", torch.uint8, numel=n // 2)
     _require(w.absmax_q, "weight.absmax_q", torch.uint8, numel=nb)
     _require(w.absmax_scale, "weight.absmax_scale", torch.float32,
@@ -164,33 +199,46 @@ def _check_weight(w: "NF4Weight", device: torch.device):
                             "weight.absmax_scale": w.absmax_scale})
 
 
-def alloc_weight(rows: int, cols: int, device) -> NF4Weight:
+def alloc_weight(rows: int, cols: int, device, dtype: str = "nf4") -> NF4Weight:
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown weight dtype {dtype!r}")
     n = rows * cols
     nb = n // BLOCKSIZE
+    if dtype == "int8":
+        return NF4Weight(torch.empty(n, dtype=torch.int8, device=device), None,
+                         torch.empty(nb, dtype=torch.float32, device=device), rows, cols, dtype)
     ng = (nb + DQ_GROUP - 1) // DQ_GROUP
     return NF4Weight(torch.empty(n // 2, dtype=torch.uint8, device=device),
                      torch.empty(nb, dtype=torch.uint8, device=device),
-                     torch.empty(ng, dtype=torch.float32, device=device), rows, cols)
+                     torch.empty(ng, dtype=torch.float32, device=device), rows, cols, dtype)
 
 
-def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None) -> NF4Weight:
-    """NF4-quantize an fp32 [rows, cols] CUDA tensor (blocksize 64, double quant)."""
-    _require(W, "W", torch.float32)
+def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None,
+                 dtype: str = "nf4") -> NF4Weight:
+    """Quantize an fp32 or bf16 [rows, cols] CUDA tensor (blocksize 64):
+    dtype "nf4" or "fp4" (double-quantized absmax) or "int8"."""
+    if not isinstance(W, torch.Tensor) or W.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"W must be float32 or bfloat16, got {getattr(W, 'dtype', type(W))}")
+    _require(W, "W", W.dtype)
     if W.dim() != 2:
         raise ValueError("W must be 2-D [rows, cols]")
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown weight dtype {dtype!r}")
     rows, cols = W.shape
     if cols % BLOCKSIZE:
         raise ValueError(f"cols = {cols} is not a multiple of {BLOCKSIZE}")
     if out is not None:
         if (out.rows, out.cols) != (rows, cols):
             raise ValueError(f"out is a {out.rows}x{out.cols} weight, W is {rows}x{cols}")
+        if out.dtype != dtype:
+            raise ValueError(f"out holds a {out.dtype} weight, asked for {dtype}")
         _check_weight(out, W.device)
     _require_cuda_device(W.device)
-    q = out if out is not None else alloc_weight(rows, cols, W.device)
+    q = out if out is not None else alloc_weight(rows, cols, W.device, dtype)
     with torch.cuda.device(W.device):
-        _check("nf4_quantize", lib().nf4_quantize(
-            _ptr(W), rows, cols, BLOCKSIZE, _ptr(q.codes), _ptr(q.absmax_q),
-            _ptr(q.absmax_scale), _stream(W.device)))
+        _check("nf4_quantize_ex", lib().nf4_quantize_ex(
+            _ptr(W), ELEM[W.dtype], rows, cols, BLOCKSIZE, DTYPES[dtype], _ptr(q.codes),
+            _ptr(q.absmax_q), _ptr(q.absmax_scale), _stream(W.device)))
     return q
 
 
@@ -209,43 +257,55 @@ def nf4_dequantize(w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tenso
     return y
 
 
-def nf4_matmul_fwd(X: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tensor:
-    """Y = X * dequant(W)^T; X bf16 [M, cols] -> Y fp32 [M, rows]."""
-    _require(X, "X", torch.bfloat16)
-    if X.dim() != 2 or X.shape[1] != w.cols:
-        raise ValueError(f"X must be [M, {w.cols}]")
-    M = X.shape[0]
-    _check_weight(w, X.device)
+def _matmul(name: str, fn: str, A: torch.Tensor, w: NF4Weight, width: int, out_cols: int,
+            out, out_dtype, accumulate: bool) -> torch.Tensor:
+    if not isinstance(A, torch.Tensor) or A.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"{name} must be bfloat16 or float16, got {getattr(A, 'dtype', type(A))}")
+    _require(A, name, A.dtype)
+    if A.dim() != 2 or A.shape[1] != width:
+        raise ValueError(f"{name} must be [M, {width}]")
+    M = A.shape[0]
+    _check_weight(w, A.device)
     if out is not None:
-        _require(out, "out", torch.float32, shape=(M, w.rows))
-        _same_device(X.device, out=out)
-    _require_cuda_device(X.device)
-    y = out if out is not None else torch.empty(M, w.rows, dtype=torch.float32, device=X.device)
+        out_dtype = out.dtype
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"the output must be float32 or bfloat16, got {out_dtype}")
+    if out is not None:
+        _require(out, "out", out_dtype, shape=(M, out_cols))
+        _same_device(A.device, out=out)
+    elif accumulate:
+        raise ValueError("accumulate=True needs the output tensor to add to (out=)")
+    _require_cuda_device(A.device)
+    y = out if out is not None else torch.empty(M, out_cols, dtype=out_dtype, device=A.device)
     s = w.c_struct()
-    with torch.cuda.device(X.device):
-        _check("nf4_matmul_fwd", lib().nf4_matmul_fwd(_ptr(X), M, ctypes.byref(s), _ptr(y),
-                                                      _stream(X.device)))
+    with torch.cuda.device(A.device):
+        _check(fn, getattr(lib(), fn)(_ptr(A), ELEM[A.dtype], M, ctypes.byref(s), _ptr(y),
+                                      ELEM[out_dtype], ACCUMULATE if accumulate else 0,
+                                      _stream(A.device)))
     return y
 
 
-def nf4_matmul_bwd_dx(dY: torch.Tensor, w: NF4Weight,
-                      out: torch.Tensor | None = None) -> torch.Tensor:
-    """dX = dY * dequant(W); dY bf16 [M, rows] -> dX fp32 [M, cols]. No dW."""
-    _require(dY, "dY", torch.bfloat16)
-    if dY.dim() != 2 or dY.shape[1] != w.rows:
-        raise ValueError(f"dY must be [M, {w.rows}]")
-    M = dY.shape[0]
-    _check_weight(w, dY.device)
-    if out is not None:
-        _require(out, "out", torch.float32, shape=(M, w.cols))
-        _same_device(dY.device, out=out)
-    _require_cuda_device(dY.device)
-    y = out if out is not None else torch.empty(M, w.cols, dtype=torch.float32, device=dY.device)
-    s = w.c_struct()
-    with torch.cuda.device(dY.device):
-        _check("nf4_matmul_bwd_dx", lib().nf4_matmul_bwd_dx(_ptr(dY), M, ctypes.byref(s), _ptr(y),
-                                                            _stream(dY.device)))
-    return y
+def nf4_matmul_fwd(X: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None,
+                   out_dtype: torch.dtype = torch.float32, accumulate: bool = False) -> torch.Tensor:
+    """Y = X * dequant(W)^T (+ out when accumulate): X bf16 or fp16 [M, cols]
+    -> Y fp32 or bf16 [M, rows]."""
+    return _matmul("X", "nf4_matmul_fwd_ex", X, w, w.cols, w.rows, out, out_dtype, accumulate)
+
+
+def nf4_matmul_bwd_dx(dY: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None,
+                      out_dtype: torch.dtype = torch.float32,
+                      accumulate: bool = False) -> torch.Tensor:
+    """dX = dY * dequant(W) (+ out when accumulate): dY bf16 or fp16 [M, rows]
+    -> dX fp32 or bf16 [M, cols]. No dW."""
+    return _matmul("dY", "nf4_matmul_bwd_dx_ex", dY, w, w.rows, w.cols, out, out_dtype,
+                   accumulate)
+
+
+def nf4_set_mma_wait_limit(cycles: int = 0) -> None:
+    """Diagnostic: the tensor-core kernels' MMA issuer gives up waiting for a
+    stage after `cycles` clock cycles (0 restores the default of about a
+    second). For testing the timeout path only."""
+    _check("nf4_set_mma_wait_limit", lib().nf4_set_mma_wait_limit(int(cycles)))
 
 
 def nf4_poll_device_status(device=None) -> int:
@@ -276,8 +336,9 @@ def describe_site(site: int) -> str:
             f"CTA {u & 0xffffff}")
 
 
-def nf4_codebook() -> torch.Tensor:
-    """The 16 fp32 NF4 levels compiled into the library (host only)."""
+def nf4_codebook(dtype: str = "nf4") -> torch.Tensor:
+    """The 16 fp32 levels of a 4-bit dtype compiled into the library, by code
+    (host only)."""
     buf = (ctypes.c_float * 16)()
-    _check("nf4_codebook", lib().nf4_codebook(ctypes.cast(buf, ctypes.c_void_p)))
+    _check("nf4_codebook_of", lib().nf4_codebook_of(DTYPES[dtype], ctypes.cast(buf, ctypes.c_void_p)))
     return torch.tensor(list(buf), dtype=torch.float32)

@@ -35,6 +35,36 @@ static __constant__ uint32_t kLevelBitsDev[16] = {
     0xbdba7869u, 0x00000000u, 0x3da2fb01u, 0x3e24cadfu, 0x3e7c04dau, 0x3ead0336u,
     0x3ee1a4b5u, 0x3f1007a9u, 0x3f3913b0u, 0x3f800000u};
 
+// The 16 FP4 levels by code: E2M1 (sign bit 3, exponent bits 2-1 with bias 1,
+// mantissa bit 0; exponent 0 subnormal), magnitudes 0, 0.5, 1, 1.5, 2, 3, 4,
+// 6 divided by 6 and rounded once to fp32 ("bitsandbytes", 4-bit paragraph:
+// NF4 or standard floating-point 4-bit). Code 8 is -0.
+constexpr uint32_t kFp4LevelBits[16] = {
+    0x00000000u, 0x3daaaaabu, 0x3e2aaaabu, 0x3e800000u, 0x3eaaaaabu, 0x3f000000u,
+    0x3f2aaaabu, 0x3f800000u, 0x80000000u, 0xbdaaaaabu, 0xbe2aaaabu, 0xbe800000u,
+    0xbeaaaaabu, 0xbf000000u, 0xbf2aaaabu, 0xbf800000u};
+
+static __constant__ uint32_t kFp4LevelBitsDev[16] = {
+    0x00000000u, 0x3daaaaabu, 0x3e2aaaabu, 0x3e800000u, 0x3eaaaaabu, 0x3f000000u,
+    0x3f2aaaabu, 0x3f800000u, 0x80000000u, 0xbdaaaaabu, 0xbe2aaaabu, 0xbe800000u,
+    0xbeaaaaabu, 0xbf000000u, 0xbf2aaaabu, 0xbf800000u};
+
+// Weight formats (the nf4_dtype values of the C ABI).
+constexpr int kFmtNf4 = NF4_DTYPE_NF4, kFmtFp4 = NF4_DTYPE_FP4, kFmtInt8 = NF4_DTYPE_INT8;
+
+__host__ __device__ constexpr const uint32_t (&level_bits(int fmt))[16] {
+  return fmt == kFmtFp4 ? kFp4LevelBits : kLevelBits;
+}
+
+// FP4 magnitude thresholds: t[i] is the largest fp32 value not above the
+// exact midpoint of magnitudes i and i + 1 (of the fp32 levels). With ties to
+// the lower code, a value of magnitude |x| gets magnitude #{i : |x| > t[i]};
+// a magnitude of 0 is code 0 (+0) whatever the sign, since +0 comes first.
+__host__ __device__ constexpr uint32_t fp4_threshold_bits(int i) {
+  return i == 0 ? 0x3d2aaaabu : i == 1 ? 0x3e000000u : i == 2 ? 0x3e555555u
+       : i == 3 ? 0x3e955555u : i == 4 ? 0x3ed55555u : i == 5 ? 0x3f155555u : 0x3f555555u;
+}
+
 // Decision thresholds between neighbouring levels: t[i] is the largest fp32
 // value not above the exact midpoint (c[i] + c[i+1]) / 2. For an fp32 x the
 // nearest level, ties to the lower index, is #{i : x > t[i]}. A constexpr
@@ -81,11 +111,12 @@ struct HalfPairTable {
   uint32_t w[256 * 32];
 };
 
-constexpr HalfPairTable make_half_pair_table() {
+constexpr HalfPairTable make_half_pair_table(int fmt = kFmtNf4) {
   HalfPairTable t{};
+  const uint32_t (&lv)[16] = level_bits(fmt);
   for (int i = 0; i < 256 * 32; ++i) {
     const int b = i >> 5;
-    t.w[i] = level_to_f16(kLevelBits[b >> 4]) | (level_to_f16(kLevelBits[b & 15]) << 16);
+    t.w[i] = level_to_f16(lv[b >> 4]) | (level_to_f16(lv[b & 15]) << 16);
   }
   return t;
 }
@@ -113,6 +144,29 @@ __device__ __forceinline__ float dequant_absmax(uint32_t a8, float s2) {
   return __fdiv_rn(__fmul_rn(static_cast<float>(a8), s2), 255.0f);
 }
 
+// Element types of activations and outputs (the nf4_elem values of the C ABI).
+constexpr int kElemF32 = NF4_F32, kElemBf16 = NF4_BF16, kElemF16 = NF4_F16;
+
+// One fused matmul call, as the launchers take it. The activation operand is
+// X [M, K] (forward) or dY [M, N] (input gradient), bf16 or fp16; the output
+// Y [M, N] or dX [M, K], fp32 or bf16, overwritten or (accumulate) added to.
+struct MatmulCall {
+  const void* act;
+  bool act_f16;
+  int64_t M, N, K;
+  int fmt;                 // kFmtNf4, kFmtFp4 or kFmtInt8
+  const uint8_t* codes;    // packed 4-bit codes, or int8 values
+  const uint8_t* a8;       // 4-bit formats: absmax codes [N*K/64]
+  const float* scale;      // 4-bit formats: s2 [groups]; int8: absmax [N*K/64]
+  void* out;
+  bool out_bf16;
+  bool accumulate;
+  int num_sms;
+  int* status;
+  long long wait_limit;    // cycles before the MMA issuer's stage wait gives up
+  cudaStream_t st;
+};
+
 }  // namespace nf4
 
 // Kernel launchers (each returns cudaGetLastError() of its launch).
@@ -123,20 +177,14 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
                uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swizzle);
 
-cudaError_t launch_quantize(const float* W, int64_t n_elems, uint8_t* codes, uint8_t* a8,
-                            float* s2, cudaStream_t st);
-cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const float* s2,
+// W is fp32 or (w_bf16) bf16; fmt selects NF4 / FP4 (codes, a8, s2) or
+// int8 (codes = int8 values, s2 = fp32 absmax per block, a8 unused).
+cudaError_t launch_quantize(const void* W, bool w_bf16, int fmt, int64_t n_elems, uint8_t* codes,
+                            uint8_t* a8, float* s2, cudaStream_t st);
+cudaError_t launch_dequantize(int fmt, const uint8_t* codes, const uint8_t* a8, const float* s2,
                               int64_t n_elems, float* out, cudaStream_t st);
-cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
-                            const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
-                            int num_sms, int* status, cudaStream_t st);
-cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
-                          const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
-                          int* status, cudaStream_t st);
-cudaError_t launch_tc_dx(const uint16_t* dY, int64_t M, const uint8_t* codes, const uint8_t* a8,
-                         const float* s2, int64_t N, int64_t K, float* dX, int num_sms,
-                         int* status, cudaStream_t st);
-cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,
-                           const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* dX,
-                           int num_sms, cudaStream_t st);
+cudaError_t launch_gemv_fwd(const MatmulCall& c);
+cudaError_t launch_tc_fwd(const MatmulCall& c);
+cudaError_t launch_tc_dx(const MatmulCall& c);
+cudaError_t launch_simt_dx(const MatmulCall& c);
 }  // namespace nf4

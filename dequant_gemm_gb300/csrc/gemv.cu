@@ -1,7 +1,9 @@
-// Small-M fused NF4-dequant matmul: Y = X * dequant(W)^T for M <= 16 tokens
-// (decode shapes), and a plain fp32 input-gradient kernel for small M
-// ("Zenbit", zenbit.pallas_nf4 bullet: the compressed weight is streamed and
+// Small-M fused dequant matmul: Y = X * dequant(W)^T for M <= 16 tokens
+// (decode shapes) ("Zenbit", zenbit.pallas_nf4 bullet: the compressed weight is streamed and
 // dequantized on chip; the full-precision weight never reaches HBM).
+// Weights are NF4 or FP4 (packed 4-bit codes, double-quantized absmax) or
+// int8 ("bitsandbytes", 4-bit paragraph; "Zenbit", zenbit.int8 bullet);
+// activations bf16 or fp16; outputs fp32 or bf16, overwritten or added to.
 //
 // Forward design (HBM-bound: 0.516 B of weight per 2*M flops):
 //  * CTA = 16 warps = 8 row groups of 16 weight rows (128 rows) x 2 halves of
@@ -33,7 +35,11 @@
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
 //    that every lookup of a warp hits 32 distinct banks. Each CTA lays the
-//    copies out itself, by shuffles from levels held in registers.
+//    copies out itself, by shuffles from levels held in registers. Int8
+//    weights need no table: two bytes become an f16x2 of 1024 + (q + 128)
+//    by one byte permute with the fp16 exponent of 1024, less 1152, which is
+//    q exactly; the block scale absmax / 127 is applied after the MMA like
+//    the 4-bit one.
 //  * Within a block the 4 threads of an MMA quad each own 16 contiguous k
 //    (8 code bytes); the reduction order over k is permuted consistently in A
 //    and B, which leaves the sum unchanged.
@@ -54,7 +60,6 @@ constexpr int kGemvRows = 128;                  // weight rows per CTA
 constexpr int kRowGroups = 8;                   // 16 rows each
 constexpr int kGemvWarps = 2 * kRowGroups;      // two K-halves per row group
 constexpr int kGemvThreads = 32 * kGemvWarps;
-constexpr int kBoxBlocks = 4;                   // 64-weight blocks per code box
 constexpr int kBoxBytes = 16 * 128;             // 16 rows x 128 bytes
 constexpr int kWarpSlots = 2;                   // code boxes in flight per warp
 constexpr int kTabBytes = kHalfPairTableBytes;
@@ -63,16 +68,29 @@ constexpr int kMaxCluster = 8;
 constexpr int kOutStride = kGemvRows + 4;       // floats, keeps rows 16-byte aligned
 static_assert(kMaxCluster * kMaxSliceBlocks * kBlock == kGemvMaxCols, "K limit");
 
-// fp16 bits of level i (0 <= i < 16) as a select tree over immediates: no
-// memory access, so the table set-up does not wait on a constant-cache miss.
-template <int kLo, int kN>
+// fp16 bits of level i (0 <= i < 16) of a 4-bit format as a select tree
+// over immediates: no memory access, so the table set-up does not wait on a
+// constant-cache miss.
+template <int kFmt, int kLo, int kN>
 __device__ __forceinline__ uint32_t level_f16(int i) {
   if constexpr (kN == 1) {
-    return level_to_f16(kLevelBits[kLo]);
+    return level_to_f16(kFmt == kFmtFp4 ? kFp4LevelBits[kLo] : kLevelBits[kLo]);
   } else {
-    const uint32_t lo = level_f16<kLo, kN / 2>(i), hi = level_f16<kLo + kN / 2, kN / 2>(i);
+    const uint32_t lo = level_f16<kFmt, kLo, kN / 2>(i);
+    const uint32_t hi = level_f16<kFmt, kLo + kN / 2, kN / 2>(i);
     return (i & (kN / 2)) ? hi : lo;
   }
+}
+
+// Two int8 weights (bytes `sel` of w, sel = 0x4140 for bytes 0-1, 0x4342 for
+// bytes 2-3) as an exact f16x2: the biased bytes q + 128 become the low
+// mantissa bits of fp16 1024 (0x6400), giving 1024 + q + 128, and
+// subtracting 1152 leaves q.
+__device__ __forceinline__ uint32_t int8_pair_f16(uint32_t w_biased, uint32_t sel) {
+  const uint32_t h = __byte_perm(w_biased, 0x64646464u, sel);
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                            __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Not volatile: independent MMA chains of different blocks may interleave.
@@ -105,16 +123,55 @@ __device__ __forceinline__ void st_dsmem(float* local, uint32_t rank, float v) {
 }
 
 struct GemvArgs {
-  const uint16_t* X;     // bf16 [M, K]
-  const uint8_t* a8;     // [N*K/64]
-  const float* s2;       // [groups]
-  float* Y;              // fp32 [M, N]
+  const uint16_t* X;     // bf16 or fp16 [M, K]
+  const uint8_t* a8;     // 4-bit formats: [N*K/64]
+  const float* scale;    // 4-bit formats: s2 [groups]; int8: absmax [N*K/64]
+  void* Y;               // fp32 or bf16 [M, N]
   int64_t M, N, K;
   int nblk;              // K / 64
   int slices;            // K-slices = cluster size along y
   int max_nb;            // largest slice, in blocks
+  int out_bf16;
+  int accumulate;
   int* status;
 };
+
+// One output element: Y[i] = v (+ Y[i] with accumulate), fp32 or bf16 (RN).
+__device__ __forceinline__ void store_out(void* Y, int64_t i, float v, int out_bf16,
+                                          int accumulate) {
+  if (out_bf16) {
+    __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(Y) + i;
+    if (accumulate) v += __bfloat162float(*y);
+    *y = __float2bfloat16_rn(v);
+  } else {
+    float* y = reinterpret_cast<float*>(Y) + i;
+    if (accumulate) v += *y;
+    *y = v;
+  }
+}
+
+// Four consecutive outputs starting at i (a multiple of 4).
+__device__ __forceinline__ void store_out4(void* Y, int64_t i, float4 v, int out_bf16,
+                                           int accumulate) {
+  if (out_bf16) {
+    uint2* y = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(Y) + i);
+    if (accumulate) {
+      const uint2 o = *y;
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
+      v.x += a.x; v.y += a.y; v.z += b.x; v.w += b.y;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    *y = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  } else {
+    float4* y = reinterpret_cast<float4*>(reinterpret_cast<float*>(Y) + i);
+    if (accumulate) {
+      const float4 o = *y;
+      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+    }
+    *y = v;
+  }
+}
 
 // First absmax block of K-slice s (nblk * slices stays far below 2^31).
 __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
@@ -135,9 +192,21 @@ __host__ __device__ constexpr int gemv_off_inbox(int) { return kOffInbox; }
 __host__ __device__ constexpr int gemv_off_xs(int nt) { return gemv_off_inbox(nt) + 8 * nt * kGemvRows * 4; }
 __host__ __device__ constexpr int gemv_xstride(int max_nb) { return max_nb * 128 + 8; }
 
-template <int NT>
+// Per-format constants of the small-M forward: 64-weight blocks per 128-byte
+// code box row (four of 32 bytes, or two of 64 for int8).
+template <int kFmt>
+struct GemvFmt {
+  static constexpr bool kInt8 = kFmt == kFmtInt8;
+  static constexpr int kBoxBlocks = kInt8 ? 2 : 4;
+  static constexpr int kBlockBytes = kInt8 ? 64 : 32;   // code bytes of one block row
+};
+
+template <int NT, int kFmt, bool kF16>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) {
+  constexpr bool kInt8 = GemvFmt<kFmt>::kInt8;
+  constexpr int kBoxBlocks = GemvFmt<kFmt>::kBoxBlocks;
+  constexpr int kBlockBytes = GemvFmt<kFmt>::kBlockBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -180,20 +249,25 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     const int nmine_pf = (nboxes - kh + 1) / 2;
     if (lane == 0 && nmine_pf <= kWarpSlots && row0 + rgp * 16 < p.N)   // boxes inside the weight
       for (int i = 0; i < nmine_pf; ++i)
-        tma_prefetch_2d(&tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * 32,
+        tma_prefetch_2d(&tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * kBlockBytes,
                             static_cast<int32_t>(row0 + rgp * 16));
     const int64_t pr = row0 + rgp * 16 + lane;
     if (kh == 0 && lane < 16 && pr < p.N && nb > 0 && nmine_pf <= kWarpSlots) {
       const int64_t ia = pr * p.nblk + kb0;
-      prefetch_l2(p.a8 + ia);
-      prefetch_l2(p.a8 + ia + nb - 1);
-      prefetch_l2(p.s2 + (ia >> 8));
+      if constexpr (kInt8) {
+        prefetch_l2(p.scale + ia);
+        prefetch_l2(p.scale + ia + nb - 1);
+      } else {
+        prefetch_l2(p.a8 + ia);
+        prefetch_l2(p.a8 + ia + nb - 1);
+        prefetch_l2(p.scale + (ia >> 8));
+      }
     }
   }
   // level table: entry e, copy l at word 32 e + l (one conflict-free store per
   // entry and warp); lane l holds level l & 15, entries come by shuffles
-  {
-    const uint32_t lev = level_f16<0, 16>(lane & 15);
+  if constexpr (!kInt8) {
+    const uint32_t lev = level_f16<kFmt, 0, 16>(lane & 15);
     for (int e = warp; e < 256; e += kGemvWarps) {
       const uint32_t hi = __shfl_sync(0xffffffffu, lev, e >> 4);
       const uint32_t lo = __shfl_sync(0xffffffffu, lev, e & 15);
@@ -217,7 +291,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   // the tile, as bf16, into its staging row and takes its max |x| on the way
   // (one global round trip); the conversion to fp16 happens in place below.
   auto to_f2 = [](uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+    if constexpr (kF16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
   };
   auto amax4 = [&](uint2 v) {
     const float2 f0 = to_f2(v.x), f1 = to_f2(v.y);
@@ -249,17 +324,26 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       const uint32_t bar = bars + 8u * (i % kWarpSlots);
       tc::mbar_arrive_expect_tx(bar, kBoxBytes);
       tc::tma_load_2d(slots + (i % kWarpSlots) * kBoxBytes, &tm_codes,
-                      (kb0 + kBoxBlocks * b) * 32, static_cast<int32_t>(row0 + rgp * 16), bar);
+                      (kb0 + kBoxBlocks * b) * kBlockBytes, static_cast<int32_t>(row0 + rgp * 16),
+                      bar);
     }
   };
+  // 4-bit: absmax codes qa, qb and scales sa, sb; int8: the block absmax in
+  // sa, sb (qa, qb unused)
   auto load_scales = [&](int i, uint32_t& qa, uint32_t& qb, float& sa, float& sb) {
     const int j = (kh + 2 * i) * kBoxBlocks + (lane >> 3);
-    const bool in = i < nmine && j < nb;
+    const bool in = i < nmine && j < nb && (lane >> 3) < kBoxBlocks;
     const int64_t ia = ar * p.nblk + kb0 + j, ib = ia + 8 * p.nblk;
-    qa = (in && ar_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ia)) : 0u;
-    qb = (in && br_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ib)) : 0u;
-    sa = (in && ar_ok) ? __ldg(p.s2 + (ia >> 8)) : 0.0f;
-    sb = (in && br_ok) ? __ldg(p.s2 + (ib >> 8)) : 0.0f;
+    if constexpr (kInt8) {
+      qa = qb = 0u;
+      sa = (in && ar_ok) ? __ldg(p.scale + ia) : 0.0f;
+      sb = (in && br_ok) ? __ldg(p.scale + ib) : 0.0f;
+    } else {
+      qa = (in && ar_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ia)) : 0u;
+      qb = (in && br_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ib)) : 0u;
+      sa = (in && ar_ok) ? __ldg(p.scale + (ia >> 8)) : 0.0f;
+      sb = (in && br_ok) ? __ldg(p.scale + (ib >> 8)) : 0.0f;
+    }
   };
   uint32_t qa0, qb0, qa1, qb1;
   float sa0, sb0, sa1, sb1;
@@ -308,14 +392,22 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     return *reinterpret_cast<const uint32_t*>(tabl + (__byte_perm(w, 0u, 0x4440u + b) << 7));
   };
   // rows g and g + 8 of the box; 16-byte chunk c of row r sits at c ^ (r & 7)
-  const uint8_t* slot_g = smem + kOffSlots + warp * kWarpSlots * kBoxBytes + g * 128 + (t & 1) * 8;
+  const uint8_t* slot_g = smem + kOffSlots + warp * kWarpSlots * kBoxBytes + g * 128 +
+                          (kInt8 ? 0 : (t & 1) * 8);
   bool ok = true;
   int waited = 0;
   // one box: lane e's row-pair scales (block e >> 3, rows (e & 7, + 8)),
   // then its four blocks, each taking its scales from lane 8 jj + g
   auto do_box = [&](int i, uint32_t qa, uint32_t qb, float sa, float sb) {
     const int sl = i % kWarpSlots;
-    const float aha = dequant_absmax(qa, sa), ahb = dequant_absmax(qb, sb);
+    float aha, ahb;
+    if constexpr (kInt8) {   // scale of the raw integer sums
+      aha = __fdiv_rn(sa, 127.0f);
+      ahb = __fdiv_rn(sb, 127.0f);
+    } else {
+      aha = dequant_absmax(qa, sa);
+      ahb = dequant_absmax(qb, sb);
+    }
     // warp-uniform outcome: the lanes leave together or go on together
     const bool got = tc::mbar_wait(bars + 8u * sl, (i / kWarpSlots) & 1);
     if (!__all_sync(0xffffffffu, got)) return false;
@@ -325,9 +417,23 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     for (int jj = 0; jj < kBoxBlocks; ++jj) {
       const int j = b * kBoxBlocks + jj;
       if (j < nb) {
-        const int chunk = ((2 * jj + (t >> 1)) ^ g) << 4;
-        const uint2 wa = *reinterpret_cast<const uint2*>(sg + chunk);
-        const uint2 wb = *reinterpret_cast<const uint2*>(sg + 8 * 128 + chunk);
+        // this thread's 16 weights of the block in rows g and g + 8
+        uint32_t ra[4], rb[4];
+        if constexpr (kInt8) {
+          const int chunk = ((4 * jj + t) ^ g) << 4;
+          const uint4 wa = *reinterpret_cast<const uint4*>(sg + chunk);
+          const uint4 wb = *reinterpret_cast<const uint4*>(sg + 8 * 128 + chunk);
+          ra[0] = wa.x ^ 0x80808080u; ra[1] = wa.y ^ 0x80808080u;
+          ra[2] = wa.z ^ 0x80808080u; ra[3] = wa.w ^ 0x80808080u;
+          rb[0] = wb.x ^ 0x80808080u; rb[1] = wb.y ^ 0x80808080u;
+          rb[2] = wb.z ^ 0x80808080u; rb[3] = wb.w ^ 0x80808080u;
+        } else {
+          const int chunk = ((2 * jj + (t >> 1)) ^ g) << 4;
+          const uint2 wa = *reinterpret_cast<const uint2*>(sg + chunk);
+          const uint2 wb = *reinterpret_cast<const uint2*>(sg + 8 * 128 + chunk);
+          ra[0] = wa.x; ra[1] = wa.y; rb[0] = wb.x; rb[1] = wb.y;
+          ra[2] = ra[3] = rb[2] = rb[3] = 0u;
+        }
         float part[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -335,11 +441,22 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
           for (int q = 0; q < 4; ++q) part[nt][q] = 0.0f;
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          const uint32_t xa = s < 2 ? wa.x : wa.y, xb = s < 2 ? wb.x : wb.y;
-          const int bs = 2 * (s & 1);
-          // byte 2s -> logical k (2t, 2t+1); byte 2s+1 -> logical k (2t+8, 2t+9)
-          const uint32_t a0 = lut(xa, bs), a2 = lut(xa, bs + 1);
-          const uint32_t a1 = lut(xb, bs), a3 = lut(xb, bs + 1);
+          // step s covers weights 4s .. 4s + 3 of the thread's 16: logical k
+          // (2t, 2t+1) then (2t+8, 2t+9) of the MMA fragment
+          uint32_t a0, a1, a2, a3;
+          if constexpr (kInt8) {
+            a0 = int8_pair_f16(ra[s], 0x4140u);
+            a2 = int8_pair_f16(ra[s], 0x4342u);
+            a1 = int8_pair_f16(rb[s], 0x4140u);
+            a3 = int8_pair_f16(rb[s], 0x4342u);
+          } else {
+            const uint32_t xa = s < 2 ? ra[0] : ra[1], xb = s < 2 ? rb[0] : rb[1];
+            const int bs = 2 * (s & 1);
+            a0 = lut(xa, bs);
+            a2 = lut(xa, bs + 1);
+            a1 = lut(xb, bs);
+            a3 = lut(xb, bs + 1);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             uint2 bx = make_uint2(0u, 0u);
@@ -433,8 +550,9 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
       const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
       if (tk < mt && row0 + r4 < p.N)
-        *reinterpret_cast<float4*>(p.Y + (m0 + tk) * p.N + row0 + r4) =
-            *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4);
+        store_out4(p.Y, (m0 + tk) * p.N + row0 + r4,
+                   *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4), p.out_bf16,
+                   p.accumulate);
     }
   } else {
     // Cluster reduction, push form: CTA `rank` owns rows [rank*rpc, (rank+1)*rpc)
@@ -465,81 +583,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       if (tk < mt && row0 + r < p.N) {
         float v = 0.0f;
         for (int c = 0; c < p.slices; ++c) v += inbox[((c * 8 * NT + tk) << rpc_shift) + rl];
-        p.Y[(m0 + tk) * p.N + row0 + r] = v;
-      }
-    }
-  }
-}
-
-// Input gradient for small M in plain fp32: dX[m, k] = sum_n dY[m, n] w[n, k].
-// CTA = 256 consecutive k (4 absmax blocks) x a slice of rows n; one thread
-// per k column; dY and the dequantized absmax of 64 rows at a time are staged
-// in shared memory. Slices of n are summed with atomics into a zeroed dX.
-constexpr int kDxThreads = 256;
-constexpr int kDxRows = 64;
-constexpr int kDxMaxM = 16;
-
-__global__ void __launch_bounds__(kDxThreads)
-simt_dx_kernel(const uint16_t* __restrict__ dY, int64_t M, const uint8_t* __restrict__ codes,
-               const uint8_t* __restrict__ a8, const float* __restrict__ s2, int64_t N,
-               int64_t K, float* __restrict__ dX, int64_t rows_per_slice, int atomic_out) {
-  __shared__ float s_levels[16];
-  __shared__ float s_ahat[kDxRows][4];
-  __shared__ float s_dy[kDxMaxM][kDxRows];
-  const int tid = threadIdx.x;
-  if (tid < 16) s_levels[tid] = __uint_as_float(kLevelBitsDev[tid]);
-  const int64_t k = static_cast<int64_t>(blockIdx.x) * kDxThreads + tid;
-  const int64_t kb_base = (static_cast<int64_t>(blockIdx.x) * kDxThreads) / kBlock;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.z) * kDxMaxM;
-  const int mt = static_cast<int>(min(static_cast<int64_t>(kDxMaxM), M - m0));
-  const int64_t n_begin = blockIdx.y * rows_per_slice;
-  const int64_t n_end = min(N, n_begin + rows_per_slice);
-  const int64_t nblk = K / kBlock;
-  float acc[kDxMaxM];
-#pragma unroll
-  for (int m = 0; m < kDxMaxM; ++m) acc[m] = 0.0f;
-
-  for (int64_t n0 = n_begin; n0 < n_end; n0 += kDxRows) {
-    __syncthreads();
-    {
-      const int r = tid >> 2, j = tid & 3;
-      const int64_t n = n0 + r;
-      float v = 0.0f;
-      if (n < n_end && kb_base + j < nblk) {
-        const int64_t bi = n * nblk + kb_base + j;
-        v = dequant_absmax(a8[bi], s2[bi / kGroup]);
-      }
-      s_ahat[r][j] = v;
-    }
-    for (int i = tid; i < kDxMaxM * kDxRows; i += kDxThreads) {
-      const int m = i / kDxRows, r = i % kDxRows;
-      const int64_t n = n0 + r;
-      float v = 0.0f;
-      if (m < mt && n < n_end) {
-        const uint16_t bits = dY[(m0 + m) * N + n];
-        v = __bfloat162float(__ushort_as_bfloat16(bits));
-      }
-      s_dy[m][r] = v;
-    }
-    __syncthreads();
-    if (k < K) {
-      const int rows = static_cast<int>(min(static_cast<int64_t>(kDxRows), n_end - n0));
-      for (int r = 0; r < rows; ++r) {
-        const uint8_t byte = codes[((n0 + r) * K + k) >> 1];
-        const uint32_t q = (k & 1) ? (byte & 15u) : (byte >> 4);
-        const float w = __fmul_rn(s_levels[q], s_ahat[r][tid >> 6]);
-#pragma unroll
-        for (int m = 0; m < kDxMaxM; ++m) acc[m] = fmaf(s_dy[m][r], w, acc[m]);
-      }
-    }
-  }
-  if (k < K) {
-#pragma unroll
-    for (int m = 0; m < kDxMaxM; ++m) {
-      if (m < mt) {
-        float* dst = dX + (m0 + m) * K + k;
-        if (atomic_out) atomicAdd(dst, acc[m]);
-        else *dst = acc[m];
+        store_out(p.Y, (m0 + tk) * p.N + row0 + r, v, p.out_bf16, p.accumulate);
       }
     }
   }
@@ -555,24 +599,39 @@ constexpr size_t gemv_smem_bytes(int nt, int max_nb, int xrows) {
 constexpr size_t kGemvSmemTwoPerSm = 112 * 1024;   // two CTAs per SM
 constexpr size_t kGemvSmemLimit = 220 * 1024;
 
-template <int NT>
-cudaError_t launch_gemv_nt(const cudaLaunchConfig_t& cfg, const CUtensorMap& tm, const GemvArgs& a) {
-  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<NT>, tm, a);
+template <int NT, int kFmt, bool kF16>
+void set_smem_limit() {
+  cudaFuncSetAttribute(gemv_fwd_kernel<NT, kFmt, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(kGemvSmemLimit));
 }
 
-cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
-                            const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* Y,
-                            int num_sms, int* status, cudaStream_t st) {
+template <int kFmt, bool kF16>
+cudaError_t launch_gemv_as(int nt, const cudaLaunchConfig_t& cfg, const CUtensorMap& tm,
+                           const GemvArgs& a) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    set_smem_limit<1, kFmt, kF16>();
+    set_smem_limit<2, kFmt, kF16>();
+  });
+  return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1, kFmt, kF16>, tm, a)
+                 : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16>, tm, a);
+}
+
+cudaError_t launch_gemv_fwd(const MatmulCall& c) {
+  const int64_t M = c.M, N = c.N, K = c.K;
+  const int num_sms = c.num_sms;
   GemvArgs a;
-  a.X = X;
-  a.a8 = a8;
-  a.s2 = s2;
-  a.Y = Y;
+  a.X = static_cast<const uint16_t*>(c.act);
+  a.a8 = c.a8;
+  a.scale = c.scale;
+  a.Y = c.out;
   a.M = M;
   a.N = N;
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
-  a.status = status;
+  a.out_bf16 = c.out_bf16 ? 1 : 0;
+  a.accumulate = c.accumulate ? 1 : 0;
+  a.status = c.status;
   // Launch shape: K-slices (cluster size, a power of two <= 8) and n-tiles
   // per CTA. Fewest waves (two CTAs per SM when they fit in shared memory,
   // else one); among those, the fewest CTAs that still keep 70% of the SMs
@@ -622,24 +681,19 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   // stream (programmatic dependent launch) cannot pile up two on one SM while
   // others stay idle.
   const size_t smem = best.ctas <= num_sms ? std::max(best_smem, kGemvSmemTwoPerSm + 4096) : best_smem;
-  // packed codes [N, K/2] bytes, box 128 B (4 absmax blocks) x 16 rows, 128-byte swizzle
+  // codes [N, row bytes] (K/2 packed 4-bit, K int8), box 128 B x 16 rows,
+  // 128-byte swizzle
+  const uint64_t row_bytes = static_cast<uint64_t>(c.fmt == kFmtInt8 ? K : K / 2);
   CUtensorMap tm;
-  if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
-                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), 128, 16,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.codes, row_bytes, static_cast<uint64_t>(N),
+                 row_bytes, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    const int lim = static_cast<int>(kGemvSmemLimit);
-    cudaFuncSetAttribute(gemv_fwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    cudaFuncSetAttribute(gemv_fwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(a.slices),
                      static_cast<unsigned>(mtiles));
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
+  cfg.stream = c.st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -649,28 +703,15 @@ cudaError_t launch_gemv_fwd(const uint16_t* X, int64_t M, const uint8_t* codes,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return nt == 1 ? launch_gemv_nt<1>(cfg, tm, a) : launch_gemv_nt<2>(cfg, tm, a);
-}
-
-cudaError_t launch_simt_dx(const uint16_t* dY, int64_t M, const uint8_t* codes,
-                           const uint8_t* a8, const float* s2, int64_t N, int64_t K, float* dX,
-                           int num_sms, cudaStream_t st) {
-  const int64_t kctas = (K + kDxThreads - 1) / kDxThreads;
-  const int64_t mtiles = (M + kDxMaxM - 1) / kDxMaxM;
-  int64_t slices = (2 * static_cast<int64_t>(num_sms) + kctas * mtiles - 1) / (kctas * mtiles);
-  slices = std::max<int64_t>(1, std::min<int64_t>(slices, (N + kDxRows - 1) / kDxRows));
-  int64_t rows_per_slice = (N + slices - 1) / slices;
-  rows_per_slice = ((rows_per_slice + kDxRows - 1) / kDxRows) * kDxRows;
-  slices = (N + rows_per_slice - 1) / rows_per_slice;
-  if (slices > 1) {
-    cudaError_t e = cudaMemsetAsync(dX, 0, static_cast<size_t>(M) * K * sizeof(float), st);
-    if (e != cudaSuccess) return e;
+  switch (c.fmt * 2 + (c.act_f16 ? 1 : 0)) {
+    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, cfg, tm, a);
+    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, cfg, tm, a);
+    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, cfg, tm, a);
+    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, cfg, tm, a);
+    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, cfg, tm, a);
+    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, cfg, tm, a);
   }
-  dim3 grid(static_cast<unsigned>(kctas), static_cast<unsigned>(slices),
-            static_cast<unsigned>(mtiles));
-  simt_dx_kernel<<<grid, kDxThreads, 0, st>>>(dY, M, codes, a8, s2, N, K, dX, rows_per_slice,
-                                              slices > 1 ? 1 : 0);
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace nf4

@@ -1,9 +1,14 @@
-// NF4 blockwise quantization with 8-bit double-quantized absmax, and the
-// stand-alone dequantization ("Zenbit", zenbit.nf4 bullet; "bitsandbytes",
-// NF4 and double-quantization paragraphs).
+// Blockwise weight quantization and the stand-alone dequantization:
+//  * NF4 and FP4 with 8-bit double-quantized absmax ("Zenbit", zenbit.nf4
+//    bullet; "bitsandbytes", NF4, 4-bit and double-quantization paragraphs);
+//  * uniform symmetric int8 with an fp32 absmax per 64-weight block
+//    ("Zenbit", zenbit.int8 bullet).
+// Weights come in as fp32 or bf16 (a bf16 value is exact in fp32, so both
+// give the codes of the same fp32 weight).
 //
-// Both kernels are HBM-bound streaming passes: quantize reads 4 B and writes
-// 0.516 B per weight, dequantize reads 0.516 B and writes 4 B per weight.
+// All kernels are HBM-bound streaming passes: the 4-bit quantize reads 4 (or
+// 2) B and writes 0.516 B per weight, int8 writes 1.0625 B; dequantize reads
+// the packed weight and writes 4 B per weight.
 #include "common.cuh"
 
 namespace nf4 {
@@ -24,29 +29,48 @@ __device__ __forceinline__ float markstein_div(float w, float a, float r) {
   return __fmaf_rn(rem, r, q0);
 }
 
-// Nearest level of x in [-1, 1], ties to the lower index, through 33 buckets
-// of width 1/16 centred on the multiples of 1/16: b = round(16 x + 16), read
-// from the low bits of fl32(16 x + 16 + 1.5 * 2^23). No decision threshold lies
-// within 0.004 of a bucket edge (an odd multiple of 1/32) and neighbouring
-// thresholds are more than 1/16 apart, so a bucket holds at most one
-// threshold and an x rounded into the neighbouring bucket at an edge gets the
-// same code; the code is lo[b] + (x > thr[b]) with lo[b] the number of
-// thresholds below the bucket and thr[b] the threshold inside it (2 if none).
+constexpr float kMinFastAbsmax = 5.421010862427522e-20f;   // 2^-64
+
+// Nearest level through buckets of width 1/16 centred on the multiples of
+// 1/16: b = round(16 v + off), read from the low bits of
+// fl32(16 v + off + 1.5 * 2^23). No decision threshold lies within 0.004 of a
+// bucket edge (an odd multiple of 1/32) and neighbouring thresholds are more
+// than 1/16 apart, so a bucket holds at most one threshold and a value
+// rounded into the neighbouring bucket at an edge gets the same answer; the
+// answer is lo[b] + (v > thr[b]) with lo[b] the number of thresholds below
+// the bucket and thr[b] the threshold inside it (2 if none).
+//  NF4: v = x in [-1, 1], 33 buckets (off = 16), 15 thresholds, the answer
+//       is the code (ties to the lower code: x > t).
+//  FP4: v = |x| in [0, 1], 17 buckets (off = 0), 7 magnitude thresholds, the
+//       answer is the magnitude; the code adds the sign bit unless the
+//       magnitude is 0 (+0 precedes -0, so ties at zero go to code 0).
 struct Bucket {
   float thr;
   uint32_t lo;
 };
 
+template <int kFmt>
+struct Buckets {
+  static constexpr int kCount = kFmt == kFmtFp4 ? 17 : 33;
+  static constexpr int kThresholds = kFmt == kFmtFp4 ? 7 : 15;
+  static constexpr float kOff = kFmt == kFmtFp4 ? 0.0f : 16.0f;
+  __device__ static float threshold(int i) {
+    return __uint_as_float(kFmt == kFmtFp4 ? fp4_threshold_bits(i) : threshold_bits(i));
+  }
+};
+
+template <int kFmt>
 __device__ __forceinline__ void build_buckets(Bucket* tab) {
+  using B = Buckets<kFmt>;
   const int b = threadIdx.x;
-  if (b <= 32) {
-    const float lo_edge = static_cast<float>(2 * b - 33) * 0.03125f;
+  if (b < B::kCount) {
+    const float lo_edge = static_cast<float>(2 * b - 1) * 0.03125f - B::kOff * 0.0625f;
     const float hi_edge = lo_edge + 0.0625f;
     uint32_t lo = 0;
     float thr = 2.0f;
 #pragma unroll
-    for (int i = 0; i < 15; ++i) {
-      const float t = __uint_as_float(threshold_bits(i));
+    for (int i = 0; i < B::kThresholds; ++i) {
+      const float t = B::threshold(i);
       lo += (t < lo_edge) ? 1u : 0u;
       if (t > lo_edge && t < hi_edge) thr = t;
     }
@@ -55,82 +79,124 @@ __device__ __forceinline__ void build_buckets(Bucket* tab) {
   }
 }
 
+template <int kFmt>
 __device__ __forceinline__ uint32_t nearest_code(float x, const Bucket* tab) {
-  const uint32_t b = __float_as_uint(__fmaf_rn(x, 16.0f, 12582928.0f)) & 63u;
-  const Bucket e = tab[b];
-  return e.lo + ((x > e.thr) ? 1u : 0u);
+  if constexpr (kFmt == kFmtFp4) {
+    const float ax = fabsf(x);
+    const uint32_t b = __float_as_uint(__fmaf_rn(ax, 16.0f, 12582912.0f)) & 31u;
+    const Bucket e = tab[b];
+    const uint32_t mag = e.lo + ((ax > e.thr) ? 1u : 0u);
+    return (mag != 0u && x < 0.0f) ? (mag | 8u) : mag;
+  } else {
+    const uint32_t b = __float_as_uint(__fmaf_rn(x, 16.0f, 12582928.0f)) & 63u;
+    const Bucket e = tab[b];
+    return e.lo + ((x > e.thr) ? 1u : 0u);
+  }
 }
 
 // Two bytes of codes for four consecutive weights (little-endian u16):
 // element 4j in the high nibble of the first byte.
-__device__ __forceinline__ uint32_t pack4(const float (&x)[4], const Bucket* tab) {
-  return (nearest_code(x[0], tab) << 4) | nearest_code(x[1], tab) |
-         (nearest_code(x[2], tab) << 12) | (nearest_code(x[3], tab) << 8);
-}
-
-__device__ __forceinline__ float abs_max4(float4 v) {
-  return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+template <int kFmt>
+__device__ __forceinline__ uint32_t pack4(const float* x, const Bucket* tab) {
+  return (nearest_code<kFmt>(x[0], tab) << 4) | nearest_code<kFmt>(x[1], tab) |
+         (nearest_code<kFmt>(x[2], tab) << 12) | (nearest_code<kFmt>(x[3], tab) << 8);
 }
 
 constexpr int kQThreads = 256;   // one thread per block of the group
 
+// Each lane of a block's 8 holds 8 of its weights in two runs of 4:
+// fp32 input: float4 `sub` and `sub + 8` (elements 4 sub.. and 32 + 4 sub..);
+// bf16 input: one 16-byte load of elements 8 sub .. 8 sub + 7.
+template <bool kBf16>
+struct LaneRuns {
+  static __device__ int offset(int sub, int h) { return kBf16 ? 8 * sub + 4 * h : 4 * sub + 32 * h; }
+};
+
+template <bool kBf16>
+__device__ __forceinline__ void load_lane(const void* W, int64_t blk, int sub, bool ok,
+                                          float (&w)[2][4]) {
+  if constexpr (kBf16) {
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) r = __ldcs(reinterpret_cast<const uint4*>(W) + blk * 8 + sub);
+    const uint32_t u[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[i >> 1][2 * (i & 1)] = __uint_as_float(u[i] << 16);
+      w[i >> 1][2 * (i & 1) + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(W) + blk * 16;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (ok) {
+      a = __ldcs(src + sub);
+      b = __ldcs(src + sub + 8);
+    }
+    w[0][0] = a.x; w[0][1] = a.y; w[0][2] = a.z; w[0][3] = a.w;
+    w[1][0] = b.x; w[1][1] = b.y; w[1][2] = b.z; w[1][3] = b.w;
+  }
+}
+
+__device__ __forceinline__ float lane_absmax(const float (&w)[2][4]) {
+  float a = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a = fmaxf(a, fabsf(w[h][e]));
+#pragma unroll
+  for (int off = 4; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  return a;
+}
+
 // One CTA per double-quant group of 256 blocks (16384 weights). Warp w owns
 // blocks [32w, 32w + 32) of the group, 4 blocks per step: 8 lanes per block,
-// each holding float4 number `sub` and `sub + 8` of it (128 contiguous bytes
-// per block per load), so a lane's 8 weights share one absmax (3 shuffle
-// steps) and one reciprocal. All 16 loads of a lane are issued before any is
-// used (64 KB in flight per CTA).
+// so a lane's 8 weights share one absmax (3 shuffle steps) and one
+// reciprocal. All loads of a lane are issued before any is used.
+template <int kFmt, bool kBf16>
 __global__ void __launch_bounds__(kQThreads, 3)
-quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restrict__ codes,
+quantize_kernel(const void* __restrict__ W, int64_t n_blocks, uint8_t* __restrict__ codes,
                 uint8_t* __restrict__ a8_out, float* __restrict__ s2_out) {
   __shared__ float s_absmax[kGroup];
   __shared__ float s_warp_max[kQThreads / 32];
   __shared__ Bucket s_buckets[33];
-  build_buckets(s_buckets);
+  build_buckets<kFmt>(s_buckets);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane & 7;
   const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kGroup;
   const int nblk = static_cast<int>(min(static_cast<int64_t>(kGroup), n_blocks - blk0));
 
-  const float4* src = reinterpret_cast<const float4*>(W) + blk0 * (kBlock / 4);
-  float4 v[8][2];
+  float v[8][2][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int b = warp * 32 + 4 * j + (lane >> 3);
-    const bool ok = b < nblk;
-    v[j][0] = ok ? __ldcs(src + b * 16 + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
-    v[j][1] = ok ? __ldcs(src + b * 16 + sub + 8) : make_float4(0.f, 0.f, 0.f, 0.f);
+    load_lane<kBf16>(W, blk0 + b, sub, b < nblk, v[j]);
   }
   __syncthreads();   // bucket table ready
 
   uint16_t* dst = reinterpret_cast<uint16_t*>(codes + blk0 * (kBlock / 2));
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    float a = fmaxf(abs_max4(v[j][0]), abs_max4(v[j][1]));
-#pragma unroll
-    for (int off = 4; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    const float a = lane_absmax(v[j]);
     const int b = warp * 32 + 4 * j + (lane >> 3);
     float x[2][4];
-    const float w[2][4] = {{v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w},
-                           {v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w}};
-    if (a >= 5.421010862427522e-20f) {   // 2^-64: fast exact quotient
+    if (a >= kMinFastAbsmax) {   // fast exact quotient
       const float r = __frcp_rn(a);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[h][e] = markstein_div(w[h][e], a, r);
+        for (int e = 0; e < 4; ++e) x[h][e] = markstein_div(v[j][h][e], a, r);
     } else {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[h][e] = (a > 0.0f) ? __fdiv_rn(w[h][e], a) : 0.0f;
+        for (int e = 0; e < 4; ++e) x[h][e] = (a > 0.0f) ? __fdiv_rn(v[j][h][e], a) : 0.0f;
     }
     if (b < nblk) {
-      // block b's 32 code bytes: float4 `sub` -> bytes 2 sub, 2 sub + 1;
-      // float4 `sub + 8` -> bytes 16 + 2 sub, 17 + 2 sub
-      dst[b * 16 + sub] = static_cast<uint16_t>(pack4(x[0], s_buckets));
-      dst[b * 16 + 8 + sub] = static_cast<uint16_t>(pack4(x[1], s_buckets));
+      // run h of 4 elements at element offset o -> the u16 at byte o / 2
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        dst[b * 16 + LaneRuns<kBf16>::offset(sub, h) / 4] =
+            static_cast<uint16_t>(pack4<kFmt>(x[h], s_buckets));
       if (sub == 0) s_absmax[b] = a;
     }
   }
@@ -155,12 +221,58 @@ quantize_kernel(const float* __restrict__ W, int64_t n_blocks, uint8_t* __restri
   if (t == 0) s2_out[blockIdx.x] = s2;
 }
 
-// Dequantize: one thread per 32 weights (16 code bytes, half a block).
+// Uniform int8: q = rint(fl32(fl32(127 w) / a)) with a the block's fp32
+// absmax, kept as the block's scale. Same lane layout as the 4-bit kernel;
+// the quotient is the exact IEEE one (Markstein correction of 127 w times
+// RN(1/a)), and |q| <= 127 since 127 |w| <= 127 a.
+template <bool kBf16>
+__global__ void __launch_bounds__(kQThreads, 3)
+quantize_int8_kernel(const void* __restrict__ W, int64_t n_blocks, int8_t* __restrict__ q_out,
+                     float* __restrict__ absmax_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kGroup;
+  const int nblk = static_cast<int>(min(static_cast<int64_t>(kGroup), n_blocks - blk0));
+  float v[8][2][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int b = warp * 32 + 4 * j + (lane >> 3);
+    load_lane<kBf16>(W, blk0 + b, sub, b < nblk, v[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float a = lane_absmax(v[j]);
+    const int b = warp * 32 + 4 * j + (lane >> 3);
+    const bool fast = a >= kMinFastAbsmax;
+    const float r = fast ? __frcp_rn(a) : 0.0f;
+    if (b < nblk) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float y = __fmul_rn(127.0f, v[j][h][e]);
+          const float t = fast ? markstein_div(y, a, r) : (a > 0.0f ? __fdiv_rn(y, a) : 0.0f);
+          const int q = __float2int_rn(t);
+          word |= (static_cast<uint32_t>(q) & 0xffu) << (8 * e);
+        }
+        *reinterpret_cast<uint32_t*>(q_out + (blk0 + b) * kBlock + LaneRuns<kBf16>::offset(sub, h)) =
+            word;
+      }
+      if (sub == 0) absmax_out[blk0 + b] = a;
+    }
+  }
+}
+
+// Dequantize (4-bit): one thread per 32 weights (16 code bytes, half a block).
+template <int kFmt>
 __global__ void __launch_bounds__(256)
 dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ a8,
                   const float* __restrict__ s2, int64_t n_chunks, float* __restrict__ out) {
   __shared__ float s_levels[16];
-  if (threadIdx.x < 16) s_levels[threadIdx.x] = __uint_as_float(kLevelBitsDev[threadIdx.x]);
+  if (threadIdx.x < 16)
+    s_levels[threadIdx.x] = __uint_as_float(kFmt == kFmtFp4 ? kFp4LevelBitsDev[threadIdx.x]
+                                                            : kLevelBitsDev[threadIdx.x]);
   __syncthreads();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n_chunks) return;
@@ -185,22 +297,74 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__
   }
 }
 
+// Dequantize (int8): w = fl32(fl32(q * a) / 127); one thread per 16 weights.
+__global__ void __launch_bounds__(256)
+dequantize_int8_kernel(const int8_t* __restrict__ q, const float* __restrict__ absmax,
+                       int64_t n_chunks, float* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_chunks) return;
+  const float a = absmax[i >> 2];
+  const uint4 c = __ldg(reinterpret_cast<const uint4*>(q) + i);
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+  float4* o = reinterpret_cast<float4*>(out) + i * 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int v = static_cast<int8_t>((words[j] >> (8 * e)) & 0xffu);
+      r[e] = __fdiv_rn(__fmul_rn(static_cast<float>(v), a), 127.0f);
+    }
+    __stcs(o + j, make_float4(r[0], r[1], r[2], r[3]));
+  }
+}
+
+template <int kFmt, bool kBf16>
+void launch_q4(const void* W, int64_t n_blocks, uint8_t* codes, uint8_t* a8, float* s2,
+               cudaStream_t st) {
+  const int64_t n_groups = (n_blocks + kGroup - 1) / kGroup;
+  quantize_kernel<kFmt, kBf16><<<static_cast<unsigned>(n_groups), kQThreads, 0, st>>>(
+      W, n_blocks, codes, a8, s2);
+}
+
+template <bool kBf16>
+void launch_q8(const void* W, int64_t n_blocks, uint8_t* codes, float* absmax, cudaStream_t st) {
+  const int64_t n_groups = (n_blocks + kGroup - 1) / kGroup;
+  quantize_int8_kernel<kBf16><<<static_cast<unsigned>(n_groups), kQThreads, 0, st>>>(
+      W, n_blocks, reinterpret_cast<int8_t*>(codes), absmax);
+}
+
 }  // namespace
 
-cudaError_t launch_quantize(const float* W, int64_t n_elems, uint8_t* codes, uint8_t* a8,
-                            float* s2, cudaStream_t st) {
+cudaError_t launch_quantize(const void* W, bool w_bf16, int fmt, int64_t n_elems, uint8_t* codes,
+                            uint8_t* a8, float* s2, cudaStream_t st) {
   const int64_t n_blocks = n_elems / kBlock;
-  const int64_t n_groups = (n_blocks + kGroup - 1) / kGroup;
-  quantize_kernel<<<static_cast<unsigned>(n_groups), kQThreads, 0, st>>>(W, n_blocks, codes, a8,
-                                                                         s2);
+  if (fmt == kFmtInt8) {
+    if (w_bf16) launch_q8<true>(W, n_blocks, codes, s2, st);
+    else launch_q8<false>(W, n_blocks, codes, s2, st);
+  } else if (fmt == kFmtFp4) {
+    if (w_bf16) launch_q4<kFmtFp4, true>(W, n_blocks, codes, a8, s2, st);
+    else launch_q4<kFmtFp4, false>(W, n_blocks, codes, a8, s2, st);
+  } else {
+    if (w_bf16) launch_q4<kFmtNf4, true>(W, n_blocks, codes, a8, s2, st);
+    else launch_q4<kFmtNf4, false>(W, n_blocks, codes, a8, s2, st);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* a8, const float* s2,
+cudaError_t launch_dequantize(int fmt, const uint8_t* codes, const uint8_t* a8, const float* s2,
                               int64_t n_elems, float* out, cudaStream_t st) {
+  if (fmt == kFmtInt8) {
+    const int64_t n_chunks = n_elems / 16;
+    const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
+    dequantize_int8_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const int8_t*>(codes), s2,
+                                                 n_chunks, out);
+    return cudaGetLastError();
+  }
   const int64_t n_chunks = n_elems / 32;
   const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
-  dequantize_kernel<<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
+  if (fmt == kFmtFp4) dequantize_kernel<kFmtFp4><<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
+  else dequantize_kernel<kFmtNf4><<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
   return cudaGetLastError();
 }
 

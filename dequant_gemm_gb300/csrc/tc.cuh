@@ -83,6 +83,47 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t pa
   return done != 0;
 }
 
+// Outcome of a wait that also watches a CTA's abort flag.
+enum WaitResult { kWaitDone = 0, kWaitAborted = 1, kWaitTimeout = 2 };
+
+// A wait that has lasted this many cycles starts to look at the abort flag.
+// Stage waits normally end within a few hundred cycles, so the flag's
+// shared-memory load stays off their path.
+constexpr long long kAbortCheckAfter = 4096;
+
+// Bounded wait on a phase that gives up early once *abort becomes nonzero
+// (another role of the CTA, or the peer CTA of a pair, has failed).
+__device__ __forceinline__ int mbar_wait_abortable(uint32_t bar, uint32_t parity,
+                                                   const volatile int* abort,
+                                                   long long limit = (1ll << 31)) {
+  if (mbar_try_wait(bar, parity)) return kWaitDone;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return kWaitDone;
+    const long long dt = clock64() - t0;
+    if (dt > kAbortCheckAfter && *abort) return kWaitAborted;
+    if (dt > limit) return kWaitTimeout;
+  }
+}
+
+// The same on the non-blocking probe (kCluster: cluster-scope acquire), for
+// the tcgen05 issuing warp, which must not suspend.
+template <bool kCluster>
+__device__ __forceinline__ int mbar_spin_abortable(uint32_t bar, uint32_t parity,
+                                                   const volatile int* abort, long long limit) {
+  auto probe = [&] {
+    return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+  };
+  if (probe()) return kWaitDone;
+  const long long t0 = clock64();
+  while (true) {
+    if (probe()) return kWaitDone;
+    const long long dt = clock64() - t0;
+    if (dt > kAbortCheckAfter && *abort) return kWaitAborted;
+    if (dt > limit) return kWaitTimeout;
+  }
+}
+
 // Bounded spin on mbar_test_wait, for a thread with nothing else to do;
 // kCluster selects the cluster-scope acquire.
 template <bool kCluster = false>
@@ -331,15 +372,15 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_byte_addr, 
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B, fp32 D, both
-// operands K-major, shape M x N:
-//   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)
-//   bits 10-12 B format (1 = bf16) bit 15/16 A/B major (0 = K)
+// Instruction descriptor for kind::f16 with A and B both bf16 (or both fp16),
+// fp32 D, B K-major, shape M x N:
+//   bits 4-5 D format (1 = f32)   bits 7-9 A format (0 = f16, 1 = bf16)
+//   bits 10-12 B format (as A)     bit 15/16 A/B major (0 = K)
 //   bits 17-22 N >> 3              bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n,
-                                                      bool a_mn_major = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) |
-         ((n >> 3) << 17) | ((m >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(uint32_t m, uint32_t n, bool a_mn_major,
+                                                         bool f16) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7)) | (f16 ? 0u : (1u << 10)) |
+         (a_mn_major ? (1u << 15) : 0u) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 }  // namespace tc

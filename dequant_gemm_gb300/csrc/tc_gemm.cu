@@ -1,30 +1,34 @@
-// Large-M fused NF4-dequant matmuls on the sm_103a tensor cores (tcgen05):
+// Large-M fused dequant matmuls on the sm_103a tensor cores (tcgen05):
 //   forward   Y[m, n]  = sum_k X[m, k]  * w[n, k]
 //   input grad dX[m, k] = sum_n dY[m, n] * w[n, k]      (no dW)
 // ("Zenbit", zenbit.pallas_nf4 bullet: compressed weight tiles streamed in and
 // dequantized on chip, full-precision weight never in HBM; dL/dX only.)
+// Weights are NF4 or FP4 (4-bit codes, double-quantized absmax) or int8 with
+// an fp32 absmax per block; activations bf16 or fp16 (the dequantized weight
+// then enters the MMA in the same type); outputs fp32 or bf16, overwritten or
+// added to ("bitsandbytes", quantized-GEMM and 4-bit paragraphs).
 //
 // One CTA computes a 128 x BN tile of D = A * B^T with the weight as the
 // 128-row A operand and the tokens as the BN-column B operand (BN = 64, 128 or
 // 256; 256 on CTA pairs that share one 256 x 256 MMA), looping over the
 // reduction in stages of 64:
-//   * warp 0 TMA-loads the stage's activation tile (bf16, 128-byte swizzle,
-//     the K-major B operand) and its packed-code tile from one elected lane;
+//   * warp 0 TMA-loads the stage's activation tile (16-bit, 128-byte swizzle,
+//     the K-major B operand) and its code tile from one elected lane;
 //   * the dequant warps, in four groups of four that take the stages in
-//     turn, dequantize the codes (level * dequantized absmax, rounded to
-//     bf16) into the stage's A operand;
+//     turn, dequantize the codes (level * dequantized absmax, rounded to the
+//     activation type) into the stage's A operand;
 //   * warp 1 issues tcgen05.mma (128 x BN x 16) from one elected lane into
 //     an fp32 accumulator in tensor memory and commits each stage back to the
 //     producer;
 //   * the dequant warps then read the accumulator with tcgen05.ld and store
-//     fp32 outputs (32 consecutive outputs of one token per warp store).
+//     the outputs (32 consecutive outputs of one token per warp store).
 //
 // Both directions walk the weight along its rows, one thread per (row, 64
-// columns) run, which is one absmax block: both levels of a code byte come
-// from one lookup in a 256-entry fp16 level pair table kept in 32
-// lane-private copies (every lookup of a warp hits 32 distinct banks), are
-// widened to fp32 and multiplied by the block's dequantized absmax, a
-// register.
+// columns) run, which is one absmax block. A 4-bit code byte gives both
+// levels from one lookup in a 256-entry fp16 level pair table kept in 32
+// lane-private copies (every lookup of a warp hits 32 distinct banks); an
+// int8 byte is converted directly. Either is widened to fp32 and multiplied
+// by the block's dequantized absmax (for int8, absmax / 127), a register.
 //
 // Forward: the tile is 128 weight rows, the reduction runs along a row, so a
 // thread's run is K-contiguous and goes straight into tensor memory (one
@@ -38,12 +42,14 @@
 // an MN-major descriptor: no transposition and no per-row scale exchange
 // between lanes.
 //
-// When the output tiles alone cannot fill the GPU the reduction is split
-// across CTAs and summed with atomics into a zeroed output.
+// When the output tiles alone cannot fill the GPU and the output is fp32,
+// the reduction is split across CTAs and summed with atomics into a zeroed
+// (or, accumulating, the caller's) output. A bf16 output is never split.
 //
 // Every mbarrier wait is bounded; a CTA that gives up records a timeout in the
-// device status word, skips the remaining work and still releases its tensor
-// memory.
+// device status word and raises an abort flag (its own and, on a pair, the
+// peer's); every role then stops at its next wait, the copies and MMAs in
+// flight are waited for, and the tensor memory is freed before the CTA exits.
 #include <algorithm>
 #include <mutex>
 
@@ -54,26 +60,25 @@ namespace nf4 {
 namespace {
 
 constexpr int kTileRows = 128;               // MMA M
-constexpr int kCodesStageBytes = 4096;       // 128 x 64 nibbles
 constexpr uint32_t kTmemCols = 512;
 
-// Per-direction and per-token-tile configuration and shared-memory layout.
-// The token tile BN (MMA N) sets the stage size; smaller tiles get deeper
-// rings, so that enough code bytes are in flight per SM to cover the memory
-// latency. Tensor memory holds the BN fp32 accumulator columns, then one
-// 32-column A-operand slot per stage.
+// Per-direction, per-token-tile and per-format configuration and shared-memory
+// layout. The token tile BN (MMA N) sets the stage size; smaller tiles get
+// deeper rings, so that enough code bytes are in flight per SM to cover the
+// memory latency. Tensor memory holds the BN fp32 accumulator columns, then
+// (forward) one 32-column A-operand slot per stage.
 //
-// The forward with BN = 256 runs on CTA pairs (cta_group::2): the two CTAs of
-// a cluster hold 128 weight rows each, and half of the token tile each; the
-// MMA warp of the even CTA issues 256 x 256 x 16 MMAs over both SMs. Each SM
-// then stages and reads only half of the activation tile, which is most of
-// the shared-memory traffic of a stage. The dequant warps of
-// both CTAs arrive on the issuing CTA's stage barrier. The arrival takes the
+// The BN = 256 tiles run on CTA pairs (cta_group::2): the two CTAs of a
+// cluster hold 128 weight rows (columns) each, and half of the token tile
+// each; the MMA warp of the even CTA issues 256 x 256 x 16 MMAs over both
+// SMs. Each SM then stages and reads only half of the activation tile, which
+// is most of the shared-memory traffic of a stage. The dequant warps of both
+// CTAs arrive on the issuing CTA's stage barrier. The arrival takes the
 // instruction's default (CTA-scope) release: by then the warp's tensor-memory
-// stores have retired (tcgen05.wait::st) and the stage's copies have been seen
-// complete, and a cluster-scope release was measured to stall the arriving
-// thread for 1-2.5K cycles on a busy SM, enough to halve the MMA rate.
-template <bool kDx, int kBN>
+// stores have retired (tcgen05.wait::st) and the stage's copies have been
+// seen complete, and a cluster-scope release was measured to stall the
+// arriving thread for 1-2.5K cycles on a busy SM, enough to halve the MMA rate.
+template <bool kDx, int kBN, bool kInt8>
 struct Cfg {
   static constexpr bool kPair = kBN == 256;
   static constexpr int kCg = kPair ? 2 : 1;          // tcgen05 cta_group
@@ -81,6 +86,9 @@ struct Cfg {
   static constexpr int kGroups = 4;
   static constexpr int kDqWarps = 4 * kGroups;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
+  // code bytes of a stage: 128 weight rows (forward) or 64 weight rows of 128
+  // columns (input gradient) x 64 weights, at 4 or 8 bits
+  static constexpr int kCodesStageBytes = kInt8 ? 8192 : 4096;
   // The input gradient stages its A tile in shared memory as well, in a ring
   // of its own: one slot per dequant group, freed by the stage's MMAs, while
   // the copies run further ahead (a shared 5-deep ring left the MMA waiting
@@ -89,12 +97,12 @@ struct Cfg {
   static constexpr int kStages = kDx ? (kBN == 64 ? 8 : 6) : (kBN == 64 ? 12 : 8);
   static constexpr int kASlots = kDx ? 4 : kStages;   // forward: the TMEM slot of the stage
   static constexpr int kBRows = kPair ? kBN / 2 : kBN;   // tokens staged per CTA
-  static constexpr int kActStageBytes = kBRows * 128;    // 64 bf16 per token row
+  static constexpr int kActStageBytes = kBRows * 128;    // 64 16-bit values per token row
   static constexpr uint32_t kTmemA0 = kBN;
   // the forward's A slots follow the accumulator; the input gradient holds
   // only the accumulator (BN columns, a power of two >= 32)
   static constexpr uint32_t kTmemAlloc = kDx ? static_cast<uint32_t>(kBN) : kTmemCols;
-  static constexpr int kLutBytes = kHalfPairTableBytes;
+  static constexpr int kLutBytes = kInt8 ? 0 : kHalfPairTableBytes;
   static constexpr int kOffAct = 0;
   static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
   static constexpr int kOffCodes = kOffA + kASlots * kAStageBytes;
@@ -110,20 +118,25 @@ struct Cfg {
 };
 
 struct TcArgs {
-  const uint8_t* a8;
-  const float* s2;
-  float* out;        // Y [M, N] or dX [M, K]
+  const uint8_t* a8;       // 4-bit formats: absmax codes
+  const float* scale;      // 4-bit formats: s2 per group; int8: absmax per block
+  void* out;               // Y [M, N] or dX [M, K], fp32 or bf16
   int64_t M, N, K;
-  int nblk;          // K / 64
-  int bn;            // token tile
+  int nblk;                // K / 64
+  int bn;                  // token tile
+  int fmt;                 // 4-bit table: kFmtNf4 or kFmtFp4
   int stages_total;
   int stages_per_split;
   int atomic_out;
+  int out_bf16;
+  int accumulate;
+  long long mma_wait_limit;
   int* status;
 };
 
-// Level pair table of both directions (fp16 levels, layout in common.cuh).
-__device__ __align__(128) const HalfPairTable kHalfPairs = make_half_pair_table();
+// Level pair tables of the 4-bit formats (fp16 levels, layout in common.cuh).
+__device__ __align__(128) const HalfPairTable kHalfPairsNf4 = make_half_pair_table(kFmtNf4);
+__device__ __align__(128) const HalfPairTable kHalfPairsFp4 = make_half_pair_table(kFmtFp4);
 
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
@@ -134,22 +147,90 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+// Two fp32 values rounded to the MMA operand type (bf16 or fp16), packed.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_operand(float lo, float hi) {
+  if constexpr (kF16) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
 }
 
+// 16 code bytes of a 4-bit format (32 weights) -> 16 packed operand words.
+template <bool kF16>
+__device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab, float2 ahat2,
+                                               uint32_t (&v)[16]) {
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
+      const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
+      const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
+      v[4 * j + b] = pack_operand<kF16>(lv.x, lv.y);
+    }
+  }
+}
 
-template <bool kDx, int kBN>
-__global__ void __launch_bounds__(Cfg<kDx, kBN>::kThreads, 1)
+// 16 int8 weights -> 8 packed operand words.
+template <bool kF16>
+__device__ __forceinline__ void dequant16_int8(const uint4 c, float2 ahat2, uint32_t* v) {
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = words[j];
+    const float2 p0 = make_float2(static_cast<float>(static_cast<int8_t>(w & 0xffu)),
+                                  static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)));
+    const float2 p1 = make_float2(static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)),
+                                  static_cast<float>(static_cast<int8_t>(w >> 24)));
+    const float2 l0 = __fmul2_rn(p0, ahat2), l1 = __fmul2_rn(p1, ahat2);
+    v[2 * j] = pack_operand<kF16>(l0.x, l0.y);
+    v[2 * j + 1] = pack_operand<kF16>(l1.x, l1.y);
+  }
+}
+
+// One output element: out[i] = v (+ out[i] with accumulate), fp32 or bf16.
+__device__ __forceinline__ void store_out(void* out, int64_t i, float v, int out_bf16,
+                                          int accumulate) {
+  if (out_bf16) {
+    __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(out) + i;
+    if (accumulate) v += __bfloat162float(*y);
+    *y = __float2bfloat16_rn(v);
+  } else {
+    float* y = reinterpret_cast<float*>(out) + i;
+    if (accumulate) v += *y;
+    *y = v;
+  }
+}
+
+// The first nm of 16 consecutive tokens' outputs of one tile row (stride nd),
+// bf16 or accumulating. Kept out of line: its registers would otherwise
+// count against the whole kernel's budget of 96 a thread.
+__device__ __noinline__ void store_out16(void* out, int64_t i0, int64_t nd, int nm, uint4 a,
+                                         uint4 b, uint4 c, uint4 d, int out_bf16,
+                                         int accumulate) {
+  const uint32_t v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
+                          c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < nm) store_out(out, i0 + j * nd, __uint_as_float(v[j]), out_bf16, accumulate);
+}
+
+template <bool kDx, int kBN, bool kF16, bool kInt8>
+__global__ void __launch_bounds__(Cfg<kDx, kBN, kInt8>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                const TcArgs p) {
-  using C = Cfg<kDx, kBN>;
+  using C = Cfg<kDx, kBN, kInt8>;
   constexpr bool kPair = C::kPair;
   constexpr int kCg = C::kCg;
   constexpr int kStages = C::kStages;
   constexpr int kGroups = C::kGroups;
   constexpr int kActStageBytes = C::kActStageBytes;
+  constexpr int kCodesStageBytes = C::kCodesStageBytes;
   constexpr uint32_t kTmemA0 = C::kTmemA0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -190,8 +271,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     tc::mbar_init(lut_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
-    tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
-    bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), &kHalfPairs, C::kLutBytes, lut_bar);
+    if constexpr (!kInt8) {
+      const HalfPairTable* lut = p.fmt == kFmtFp4 ? &kHalfPairsFp4 : &kHalfPairsNf4;
+      tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
+      bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), lut, C::kLutBytes, lut_bar);
+    }
   }
   if (warp == 0 && lane == 0) {
     tc::prefetch_tensormap(&tm_act);
@@ -204,9 +288,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // A failure stops this CTA and, on a pair, the peer (whose barriers wait on
+  // this CTA's MMAs or arrivals).
   auto fail = [&](uint32_t role) {
     report_status(p.status, kStatusTimeout, kDx ? kSiteTcDx : kSiteTcFwd, role);
     *abort_flag = 1;
+    if constexpr (kPair) {
+      const uint32_t peer = tc::mapa(tc::smem_addr(const_cast<int*>(abort_flag)), rank ^ 1u);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1u) : "memory");
+    }
+  };
+  // a wait that gave up because of a failure elsewhere is not a failure of its own
+  auto waited = [&](int r, uint32_t role) {
+    if (r == tc::kWaitTimeout) fail(role);
+    return r == tc::kWaitDone;
   };
 
   if (warp == 0) {
@@ -219,13 +314,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     const int32_t m_load = static_cast<int32_t>(m0) + static_cast<int32_t>(rank) * C::kBRows;
     int issued = 0;
     for (int i = 0; i < nst; ++i) {
-      // one vote, so that the lanes leave together (a lane-wise read of the
-      // flag could split the warp ahead of the vote below)
+      // one vote, so that the lanes leave together
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(empty_bar(slot), ph ^ 1))) {
-        if (lane == 0) fail(kRoleProducer);
+      // every lane waits (a wait in lane 0 alone, the others parked at the
+      // shuffle, was measured 4% slower on the prefill forward: the warp
+      // reconverged late after each stage), then lane 0's outcome decides
+      int r = tc::mbar_wait_abortable(empty_bar(slot), ph ^ 1, abort_flag);
+      r = __shfl_sync(0xffffffffu, r, 0);
+      if (r != tc::kWaitDone) {
+        if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleProducer);
         break;
       }
       const int s = s_begin + i;
@@ -235,12 +334,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         tc::mbar_arrive_expect_tx(full_bar(slot), tx);
         tc::tma_load_2d(act, &tm_act, s * 64, m_load, full_bar(slot));
         if (!kDx) {
-          // 128 rows x 32 bytes
-          tc::tma_load_2d(cod, &tm_codes, s * 32, static_cast<int32_t>(r0), full_bar(slot));
+          // 128 rows x 32 (4-bit) or 64 (int8) bytes
+          tc::tma_load_2d(cod, &tm_codes, s * (kInt8 ? 64 : 32), static_cast<int32_t>(r0),
+                          full_bar(slot));
         } else {
-          // one 64-byte (128 columns) x 64-row box with the 64-byte swizzle:
-          // row r's 16-byte chunk c lands at r * 64 + 16 * (c ^ ((r >> 1) & 3))
-          tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(r0 / 2), s * 64, full_bar(slot));
+          // 128 columns x 64 rows: 64 bytes with the 64-byte swizzle (4-bit,
+          // row r's 16-byte chunk c at r * 64 + 16 * (c ^ ((r >> 1) & 3))) or
+          // 128 bytes with the 128-byte swizzle (int8, chunk c at
+          // r * 128 + 16 * (c ^ (r & 7)))
+          tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(kInt8 ? r0 : r0 / 2), s * 64,
+                          full_bar(slot));
         }
       }
       __syncwarp();
@@ -258,14 +361,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     // dq_bar only after they have seen the stage's copies land on full_bar,
     // so its completion orders both the tensor-memory A operand and the
     // shared-memory B tile before the MMAs; a failure elsewhere surfaces here
-    // as a timeout. The wait is a spin on the non-blocking test: a suspending
-    // try_wait on the issuing warp lets the MMAs already queued drain (about
-    // 380 idle tensor cycles per wait, as measured). On a pair the peer's
-    // dequant warps arrive here too, once they have stored the stage and
-    // seen their own copies land.
+    // through the abort flag. The wait is a spin on the non-blocking test: a
+    // suspending try_wait on the issuing warp lets the MMAs already queued
+    // drain (about 380 idle tensor cycles per wait, as measured). On a pair
+    // the peer's dequant warps arrive here too, once they have stored the
+    // stage and seen their own copies land.
     if (rank == 0) {
       const uint32_t idesc =
-          tc::idesc_bf16_f32(kTileRows * kCg, static_cast<uint32_t>(p.bn), kDx);
+          tc::idesc_f16kind_f32(kTileRows * kCg, static_cast<uint32_t>(p.bn), kDx, kF16);
       const uint64_t bdesc0 = tc::sw128_kmajor_desc(tc::smem_addr(smem + C::kOffAct));
       // input gradient: A tile atoms (column half h, row group g) at
       // (2 g + h) KB, i.e. 1 KB apart along M and 2 KB along K
@@ -273,9 +376,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       for (int i = 0; i < nst; ++i) {
         const int sl = i % kStages;
         const int as = i % kASlots;
-        const bool ok = tc::mbar_wait_spin<kPair>(dq_bar(as), (i / kASlots) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0) fail(kRoleMma);
+        int r = tc::mbar_spin_abortable<kPair>(dq_bar(as), (i / kASlots) & 1, abort_flag,
+                                               p.mma_wait_limit);
+        r = __shfl_sync(0xffffffffu, r, 0);
+        if (r != tc::kWaitDone) {
+          if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleMma);
           break;
         }
         tc::fence_after_sync();
@@ -300,7 +405,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       }
       if (tc::elect_one()) tc::mma_commit<kCg>(accum_bar);
       __syncwarp();
-      // all MMAs done before teardown
+      // all MMAs done before teardown (a drain: full limit, no abort exit)
       if (lane == 0 && !tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);
     }
   } else {
@@ -313,55 +418,76 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int grp = (warp - 2) >> 2;        // takes the stages i % kGroups == grp
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const uint8_t* tab = smem + C::kOffLut + 4 * lane;
+    // block scale: 4-bit ahat = fl32(fl32(a8 s2) / 255); int8 absmax / 127
+    auto block_scale = [&](uint32_t a8v, float sv) {
+      return kInt8 ? __fdiv_rn(sv, 127.0f) : dequant_absmax(a8v, sv);
+    };
+    auto load_block = [&](int64_t bi, uint32_t& a8v, float& sv) {
+      if constexpr (kInt8) {
+        sv = p.scale[bi];
+      } else {
+        a8v = p.a8[bi];
+        sv = p.scale[bi >> 8];
+      }
+    };
+    // The level table's bulk copy is waited for in full even after an abort
+    // (no copy may still be landing in this CTA's shared memory when it
+    // exits), after the first scale loads have gone out so that their latency
+    // overlaps the copy's.
+    auto wait_lut = [&] {
+      if constexpr (!kInt8) {
+        if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
+      }
+    };
     // tile row (forward: weight row; input gradient: weight column) held by
     // this thread's accumulator lane
-    int tile_row = 32 * q + lane;
+    const int tile_row = 32 * q + lane;
     if (!kDx) {
       const int64_t n = r0 + tile_row;      // this thread's weight row
       const bool vrow = n < p.N;
-      const uint8_t* tab = smem + C::kOffLut + 4 * lane;
       uint32_t a8v = 0;
-      float s2v = 0.0f;
+      float sv = 0.0f;
       auto load_scale = [&](int i) {
-        if (vrow && i < nst) {
-          const int64_t bi = n * p.nblk + s_begin + i;
-          a8v = p.a8[bi];
-          s2v = p.s2[bi >> 8];
-        }
+        if (vrow && i < nst) load_block(n * p.nblk + s_begin + i, a8v, sv);
       };
       load_scale(grp);
-      if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
+      wait_lut();
       for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        const float ahat = vrow ? dequant_absmax(a8v, s2v) : 0.0f;
+        const float ahat = vrow ? block_scale(a8v, sv) : 0.0f;
         const float2 ahat2 = make_float2(ahat, ahat);
         load_scale(i + kGroups);
         // warp-uniform: the stage is done by all lanes or by none (the
         // arrival below follows a __syncwarp)
-        bool go = !*abort_flag;
-        if (go && !tc::mbar_wait(full_bar(slot), ph)) {
-          fail(kRoleCompute);
-          go = false;
-        }
+        bool go = !*abort_flag && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag),
+                                         kRoleCompute);
         if (!__all_sync(0xffffffffu, go)) continue;
-        const uint8_t* crow = smem + C::kOffCodes + slot * kCodesStageBytes + tile_row * 32;
+        const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
+        const uint32_t dst = tmem + lane_base + kTmemA0 + 32u * slot;
+        if constexpr (kInt8) {
+          // row tile_row's 64 bytes, 64-byte swizzle
+          const int sw = (tile_row >> 1) & 3;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint4 c = *reinterpret_cast<const uint4*>(crow + 16 * hf);
-          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-          uint32_t v[16];
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[16];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
-              const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
-              const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
-              v[4 * j + b] = pack_bf16x2(lv.x, lv.y);
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = 2 * hf + cc;
+              const uint4 w = *reinterpret_cast<const uint4*>(cst + tile_row * 64 + 16 * (c ^ sw));
+              dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
             }
+            tc::tmem_st16(dst + 16u * hf, v);
           }
-          tc::tmem_st16(tmem + lane_base + kTmemA0 + 32u * slot + 16u * hf, v);
+        } else {
+          const uint8_t* crow = cst + tile_row * 32;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[16];
+            dequant16_4bit<kF16>(*reinterpret_cast<const uint4*>(crow + 16 * hf), tab, ahat2, v);
+            tc::tmem_st16(dst + 16u * hf, v);
+          }
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
@@ -371,7 +497,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     } else {
       // Thread t of the group dequantizes weight row t % 64 of the stage over
       // the tile's columns 64 (t / 64) .. + 63, one absmax block, as the
-      // forward walks a row. The 64 bf16 results are one 128-byte row of a
+      // forward walks a row. The 64 results are one 128-byte row of a
       // 128-byte-swizzled MN-major atom of the A tile (64 weight columns along
       // M x 8 weight rows along K per 1 KB atom; atom (column half h, row
       // group g) at (2 g + h) KB).
@@ -379,68 +505,62 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       const int rr = t & 63, h = t >> 6;
       const int64_t kb = (r0 >> 6) + h;
       const bool kb_ok = kb < p.nblk;
-      const uint8_t* tab = smem + C::kOffLut + 4 * lane;
-      // 16-byte code chunks 2 h and 2 h + 1 of row rr (64-byte swizzle)
-      const int csw = (rr >> 1) & 3;
-      const int co0 = rr * 64 + 16 * ((2 * h) ^ csw), co1 = rr * 64 + 16 * ((2 * h + 1) ^ csw);
       const int ao = (2 * (rr >> 3) + h) * 1024 + (rr & 7) * 128;
       const int asw = rr & 7;
       uint32_t a8v = 0;
-      float s2v = 0.0f;
+      float sv = 0.0f;
       bool rok = false;
       auto load_scale = [&](int i) {
         if (i >= nst) return;
         const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + rr;
         rok = kb_ok && n < p.N;
-        if (rok) {
-          const int64_t bi = n * p.nblk + kb;
-          a8v = p.a8[bi];
-          s2v = p.s2[bi >> 8];
-        }
+        if (rok) load_block(n * p.nblk + kb, a8v, sv);
       };
       load_scale(grp);
-      if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
+      wait_lut();
       for (int i = grp; i < nst; i += kGroups) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        const float ahat = rok ? dequant_absmax(a8v, s2v) : 0.0f;
+        const float ahat = rok ? block_scale(a8v, sv) : 0.0f;
         const float2 ahat2 = make_float2(ahat, ahat);
         load_scale(i + kGroups);
-        bool go = !*abort_flag;
-        if (go && !tc::mbar_wait(full_bar(slot), ph)) {
-          fail(kRoleCompute);
-          go = false;
-        }
+        bool go = !*abort_flag && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag),
+                                         kRoleCompute);
         // the A slot's previous tile (stage i - kASlots) has been read by its MMAs
         const int as = i % kASlots;
-        if (go && i >= kASlots && !tc::mbar_wait(afree_bar(as), ((i / kASlots) - 1) & 1)) {
-          fail(kRoleCompute);
-          go = false;
-        }
+        if (go && i >= kASlots)
+          go = waited(tc::mbar_wait_abortable(afree_bar(as), ((i / kASlots) - 1) & 1, abort_flag),
+                      kRoleCompute);
         if (!__all_sync(0xffffffffu, go)) continue;
         const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
         uint8_t* arow = smem + C::kOffA + as * C::kAStageBytes + ao;
+        uint32_t v[32];
+        if constexpr (kInt8) {
+          // row rr's chunks 4 h .. 4 h + 3 of 128 bytes, 128-byte swizzle
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint4 c = *reinterpret_cast<const uint4*>(cst + (hf ? co1 : co0));
-          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-          uint32_t v[16];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
-              const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
-              const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
-              v[4 * j + b] = pack_bf16x2(lv.x, lv.y);
-            }
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint4 w =
+                *reinterpret_cast<const uint4*>(cst + rr * 128 + 16 * ((4 * h + cc) ^ (rr & 7)));
+            dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
           }
-          // columns 32 hf + 8 j .. + 7 form chunk 4 hf + j of the atom row
+        } else {
+          // row rr's chunks 2 h, 2 h + 1 of 64 bytes, 64-byte swizzle
+          const int csw = (rr >> 1) & 3;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(arow + 16 * ((4 * hf + j) ^ asw)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint4 w =
+                *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw));
+            uint32_t part[16];
+            dequant16_4bit<kF16>(w, tab, ahat2, part);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[16 * hf + e] = part[e];
+          }
         }
+        // columns 8 j .. 8 j + 7 form chunk j of the atom row
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(arow + 16 * (j ^ asw)) =
+              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         tc::fence_proxy_async();   // the MMA reads the tile through the async proxy
         __syncwarp();
         if (lane == 0) arrive_dq(as);
@@ -449,7 +569,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 
     // epilogue: accumulator lanes are tile rows, columns are tokens; the
     // groups share out the 16-column chunks
-    if (!*abort_flag && !tc::mbar_wait(accum_bar, 0)) fail(kRoleEpilogue);
+    if (!*abort_flag) waited(tc::mbar_wait_abortable(accum_bar, 0, abort_flag), kRoleEpilogue);
     tc::fence_after_sync();
     if (!*abort_flag) {
       const int64_t rg = r0 + tile_row;
@@ -459,14 +579,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
         tc::tmem_wait_ld();
+        // one output mode per launch: the branch stays outside the stores
+        const int nm = vrow ? static_cast<int>(min(static_cast<int64_t>(16), p.M - (m0 + c))) : 0;
+        float* of = reinterpret_cast<float*>(p.out) + (m0 + c) * nd + rg;
+        if (p.atomic_out) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int64_t m = m0 + c + j;
-          if (vrow && m < p.M) {
-            float* dst = p.out + m * nd + rg;
-            if (p.atomic_out) atomicAdd(dst, __uint_as_float(v[j]));
-            else *dst = __uint_as_float(v[j]);
-          }
+          for (int j = 0; j < 16; ++j)
+            if (j < nm) atomicAdd(of + j * nd, __uint_as_float(v[j]));
+        } else if (!p.out_bf16 && !p.accumulate) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nm) of[j * nd] = __uint_as_float(v[j]);
+        } else {
+          store_out16(p.out, (m0 + c) * nd + rg, nd, nm, make_uint4(v[0], v[1], v[2], v[3]),
+                      make_uint4(v[4], v[5], v[6], v[7]), make_uint4(v[8], v[9], v[10], v[11]),
+                      make_uint4(v[12], v[13], v[14], v[15]), p.out_bf16, p.accumulate);
         }
       }
     }
@@ -483,21 +610,24 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   }
 }
 
-template <bool kDx, int kBN>
-cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, const uint8_t* a8,
-                      const float* s2, int64_t N, int64_t K, float* out, int num_sms, int* status,
-                      cudaStream_t st) {
-  using C = Cfg<kDx, kBN>;
+template <bool kDx, int kBN, bool kF16, bool kInt8>
+cudaError_t launch_tc(const MatmulCall& c) {
+  using C = Cfg<kDx, kBN, kInt8>;
+  const int64_t M = c.M, N = c.N, K = c.K;
   TcArgs a;
-  a.a8 = a8;
-  a.s2 = s2;
-  a.out = out;
+  a.a8 = c.a8;
+  a.scale = c.scale;
+  a.out = c.out;
   a.M = M;
   a.N = N;
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
-  a.status = status;
+  a.fmt = c.fmt;
+  a.status = c.status;
   a.bn = kBN;
+  a.out_bf16 = c.out_bf16 ? 1 : 0;
+  a.accumulate = c.accumulate ? 1 : 0;
+  a.mma_wait_limit = c.wait_limit;
   const int64_t nd = kDx ? K : N;            // tile-row dimension
   const int64_t red = kDx ? N : K;           // reduction dimension
   // a pair's two CTAs take consecutive 128-row tiles
@@ -507,35 +637,42 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
   a.stages_total = static_cast<int>((red + 63) / 64);
   int splits = 1;
   const int64_t ctas = row_tiles * m_tiles;
-  if (ctas < num_sms) {   // each split fills the ring at least once
+  if (ctas < c.num_sms && !c.out_bf16) {   // each split fills the ring at least once
     splits = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>(num_sms / ctas, a.stages_total / C::kStages)));
+        1, std::min<int64_t>(c.num_sms / ctas, a.stages_total / C::kStages)));
   }
   a.stages_per_split = (a.stages_total + splits - 1) / splits;
   splits = (a.stages_total + a.stages_per_split - 1) / a.stages_per_split;
   a.atomic_out = splits > 1 ? 1 : 0;
 
   CUtensorMap tm_act, tm_codes;
-  // activations: [M, red] bf16, box 64 (reduction) x the tokens one CTA
+  // activations: [M, red] 16-bit, box 64 (reduction) x the tokens one CTA
   // stages, 128-byte swizzle
-  if (!encode_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, static_cast<uint64_t>(red),
-                 static_cast<uint64_t>(M), static_cast<uint64_t>(red) * 2, 64,
-                 static_cast<uint32_t>(C::kBRows), CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(&tm_act, kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 c.act, static_cast<uint64_t>(red), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(red) * 2, 64, static_cast<uint32_t>(C::kBRows),
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // packed codes: [N, K/2] bytes; the forward takes 32 B x 128 rows, the input
-  // gradient 64 B (128 columns) x 64 rows, 64-byte swizzled
-  if (!encode_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(K / 2),
-                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), kDx ? 64 : 32,
-                 kDx ? 64 : 128, kDx ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE))
+  // codes: [N, row bytes] (K/2 packed 4-bit, K int8). The forward takes 128
+  // rows x one stage's bytes (32, or 64 with the 64-byte swizzle); the input
+  // gradient 128 columns x 64 rows (64 bytes with the 64-byte swizzle, or 128
+  // with the 128-byte swizzle).
+  const uint64_t row_bytes = static_cast<uint64_t>(kInt8 ? K : K / 2);
+  const uint32_t box_x = kDx ? (kInt8 ? 128u : 64u) : (kInt8 ? 64u : 32u);
+  const uint32_t box_y = kDx ? 64u : 128u;
+  const CUtensorMapSwizzle sw = kDx ? (kInt8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)
+                                    : (kInt8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!encode_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.codes, row_bytes,
+                 static_cast<uint64_t>(N), row_bytes, box_x, box_y, sw))
     return cudaErrorInvalidValue;
 
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(tc_gemm_kernel<kDx, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         C::kSmemBytes);
+    cudaFuncSetAttribute(tc_gemm_kernel<kDx, kBN, kF16, kInt8>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
-  if (a.atomic_out) {
-    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(M) * nd * sizeof(float), st);
+  if (a.atomic_out && !c.accumulate) {
+    cudaError_t e = cudaMemsetAsync(c.out, 0, static_cast<size_t>(M) * nd * sizeof(float), c.st);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
@@ -545,7 +682,7 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
     cfg.gridDim = grid;
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.stream = st;
+    cfg.stream = c.st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -553,29 +690,31 @@ cudaError_t launch_tc(const uint16_t* act, int64_t M, const uint8_t* codes, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kDx, kBN>, tm_act, tm_codes, a);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kDx, kBN, kF16, kInt8>, tm_act, tm_codes, a);
   } else {
-    tc_gemm_kernel<kDx, kBN><<<grid, C::kThreads, C::kSmemBytes, st>>>(tm_act, tm_codes, a);
+    tc_gemm_kernel<kDx, kBN, kF16, kInt8><<<grid, C::kThreads, C::kSmemBytes, c.st>>>(tm_act,
+                                                                                   tm_codes, a);
     return cudaGetLastError();
   }
 }
 
+template <bool kDx, bool kF16, bool kInt8>
+cudaError_t launch_tc_by_m(const MatmulCall& c) {
+  if (c.M <= 64) return launch_tc<kDx, 64, kF16, kInt8>(c);
+  if (c.M <= 128) return launch_tc<kDx, 128, kF16, kInt8>(c);
+  return launch_tc<kDx, 256, kF16, kInt8>(c);
+}
+
+template <bool kDx>
+cudaError_t launch_tc_any(const MatmulCall& c) {
+  const bool i8 = c.fmt == kFmtInt8;
+  if (c.act_f16) return i8 ? launch_tc_by_m<kDx, true, true>(c) : launch_tc_by_m<kDx, true, false>(c);
+  return i8 ? launch_tc_by_m<kDx, false, true>(c) : launch_tc_by_m<kDx, false, false>(c);
+}
+
 }  // namespace
 
-cudaError_t launch_tc_fwd(const uint16_t* X, int64_t M, const uint8_t* codes, const uint8_t* a8,
-                          const float* s2, int64_t N, int64_t K, float* Y, int num_sms,
-                          int* status, cudaStream_t st) {
-  if (M <= 64) return launch_tc<false, 64>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
-  if (M <= 128) return launch_tc<false, 128>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
-  return launch_tc<false, 256>(X, M, codes, a8, s2, N, K, Y, num_sms, status, st);
-}
-
-cudaError_t launch_tc_dx(const uint16_t* dY, int64_t M, const uint8_t* codes, const uint8_t* a8,
-                         const float* s2, int64_t N, int64_t K, float* dX, int num_sms,
-                         int* status, cudaStream_t st) {
-  if (M <= 64) return launch_tc<true, 64>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
-  if (M <= 128) return launch_tc<true, 128>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
-  return launch_tc<true, 256>(dY, M, codes, a8, s2, N, K, dX, num_sms, status, st);
-}
+cudaError_t launch_tc_fwd(const MatmulCall& c) { return launch_tc_any<false>(c); }
+cudaError_t launch_tc_dx(const MatmulCall& c) { return launch_tc_any<true>(c); }
 
 }  // namespace nf4

@@ -40,9 +40,10 @@ def weight(rows: int, cols: int, std: float = 0.02, seed: int = SEED_W,
     return w.contiguous()
 
 
-def activations(m: int, k: int, std: float = 1.0, seed: int = SEED_X) -> torch.Tensor:
-    """bf16 [m, k] ~ N(0, std^2), rounded to nearest-even from fp32."""
-    return normal((m, k), std, seed).to(torch.bfloat16).contiguous()
+def activations(m: int, k: int, std: float = 1.0, seed: int = SEED_X,
+                dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """bf16 (or fp16) [m, k] ~ N(0, std^2), rounded to nearest-even from fp32."""
+    return normal((m, k), std, seed).to(dtype).contiguous()
 
 
 @dataclass(frozen=True)
@@ -72,6 +73,13 @@ class Workload:
     # Projections that read the same input and can be issued together, in
     # layer order; projections not named run alone.
     concurrent: tuple = ()
+    # Weight format ("nf4", "fp4", "int8"), element type of the weights fed to
+    # quantize ("f32", "bf16"), of the activations ("bf16", "f16") and of the
+    # matmul outputs ("f32", "bf16").
+    wdtype: str = "nf4"
+    w_in: str = "f32"
+    act: str = "bf16"
+    out: str = "f32"
 
     def issue_groups(self):
         """Projection indices grouped for issue, in order: each group's
@@ -111,4 +119,25 @@ WORKLOADS = {
     # (q, k, v share the layer input; gate and up share the MLP input)
     "qwen2.5_7b_layer": Workload("qwen2.5_7b_layer", QWEN_LAYER, fwd_m=(1, 64, 2048), dx_m=(2048,),
                                  concurrent=((0, 1, 2), (4, 5))),
+    # the prefill weight from a bf16 checkpoint, bf16 outputs
+    "prefill_up_11008x4096_bf16": Workload("prefill_up_11008x4096_bf16",
+                                           (Projection("up", 11008, 4096, SEED_W),), fwd_m=(4096,),
+                                           w_in="bf16", out="bf16"),
+    # the other weight formats on the decode and prefill shapes
+    "decode_4096_fp4": Workload("decode_4096_fp4",
+                                (Projection("w", 4096, 4096, SEED_W, outlier_frac=0.001),),
+                                fwd_m=(1, 4, 16), wdtype="fp4"),
+    "decode_4096_int8": Workload("decode_4096_int8",
+                                 (Projection("w", 4096, 4096, SEED_W, outlier_frac=0.001),),
+                                 fwd_m=(1, 4, 16), wdtype="int8"),
+    "prefill_up_11008x4096_fp4": Workload("prefill_up_11008x4096_fp4",
+                                          (Projection("up", 11008, 4096, SEED_W),), fwd_m=(4096,),
+                                          wdtype="fp4"),
+    "prefill_up_11008x4096_int8": Workload("prefill_up_11008x4096_int8",
+                                           (Projection("up", 11008, 4096, SEED_W),),
+                                           fwd_m=(4096,), wdtype="int8"),
+    # fp16 activations and output gradients on the backward weight
+    "bwd_down_4096x11008_f16": Workload("bwd_down_4096x11008_f16",
+                                        (Projection("down", 4096, 11008, SEED_W),), dx_m=(2048,),
+                                        dy_std=0.01, act="f16"),
 }

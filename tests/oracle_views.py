@@ -11,18 +11,28 @@ from oracle import nf4_oracle as o
 
 
 class OracleWeight:
-    def __init__(self, W: np.ndarray):
+    """dtype "nf4" / "fp4": codes per block, double quant over all blocks;
+    "int8": every block on its own (its absmax is its scale)."""
+
+    def __init__(self, W: np.ndarray, dtype: str = "nf4"):
         self.W = np.ascontiguousarray(W, dtype=np.float32)
+        self.dtype = dtype
         self.N, self.K = self.W.shape
         self.nblk = self.K // o.BLOCKSIZE
-        self.absmax = o.block_absmax(self.W.reshape(-1))
-        self.a8, self.s2 = o.double_quant(self.absmax)
-        self.ahat = o.dequant_absmax(self.a8, self.s2)
+        if dtype != "int8":
+            self.levels = o.levels_of(dtype)
+            self.absmax = o.block_absmax(self.W.reshape(-1))
+            self.a8, self.s2 = o.double_quant(self.absmax)
+            self.ahat = o.dequant_absmax(self.a8, self.s2)
 
     def _blocks(self, block_ids: np.ndarray) -> np.ndarray:
         wb = self.W.reshape(-1, o.BLOCKSIZE)[block_ids]
-        codes = o.quantize_codes(wb.reshape(-1), self.absmax[block_ids])
-        return o.dequantize_codes(codes.reshape(-1, o.BLOCKSIZE), self.ahat[block_ids])
+        if self.dtype == "int8":
+            q, a = o.int8_quantize_flat(wb.reshape(-1))
+            return o.int8_dequantize_flat(q, a).reshape(-1, o.BLOCKSIZE)
+        codes = o.quantize_codes(wb.reshape(-1), self.absmax[block_ids], self.levels)
+        return o.dequantize_codes(codes.reshape(-1, o.BLOCKSIZE), self.ahat[block_ids],
+                                  self.levels)
 
     def rows(self, rows) -> np.ndarray:
         rows = np.asarray(rows, dtype=np.int64)

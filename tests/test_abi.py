@@ -117,3 +117,56 @@ def test_autograd_wrapper_imports_and_validates_without_a_device():
         nf4_linear(torch.zeros(2, 64, dtype=torch.float32), q)      # not bf16
     with pytest.raises(ValueError):
         nf4_linear(torch.zeros(2, 32, dtype=torch.bfloat16), q)     # wrong width
+
+
+def test_fp4_codebook_matches_oracle_bits():
+    got = nf4.nf4_codebook("fp4").numpy().astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), o.fp4_levels().view(np.uint32))
+    buf = (ctypes.c_float * 16)()
+    assert nf4.lib().nf4_codebook_of(2, ctypes.cast(buf, ctypes.c_void_p)) == 2   # int8: no table
+    assert nf4.lib().nf4_codebook_of(0, None) == 1
+
+
+def test_quantize_ex_validation():
+    L = nf4.lib()
+    # dtype / element type
+    assert L.nf4_quantize_ex(P, 0, 8, 64, 64, 3, P, P, P, None) == 2
+    assert L.nf4_quantize_ex(P, 2, 8, 64, 64, 0, P, P, P, None) == 2       # fp16 weights
+    assert L.nf4_quantize_ex(P, 1, 8, 64, 32, 0, P, P, P, None) == 4
+    # int8 takes no absmax codes; 4-bit needs them
+    assert L.nf4_quantize_ex(P, 0, 8, 64, 64, 2, P, P, P, None) == 1
+    assert L.nf4_quantize_ex(P, 0, 8, 64, 64, 1, P, None, P, None) == 1
+    assert L.nf4_quantize_ex(P + 8, 1, 8, 64, 64, 2, P, None, P, None) == 3
+    assert L.nf4_quantize_ex(None, 1, 0, 64, 64, 2, None, None, None, None) == 0
+
+
+def test_matmul_ex_validation():
+    L = nf4.lib()
+    w = _weight(codes=P, a8=P, s2=P)
+    f, d = L.nf4_matmul_fwd_ex, L.nf4_matmul_bwd_dx_ex
+    assert f(P, 0, 4, ctypes.byref(w), P, 0, 0, None) == 2       # fp32 activations
+    assert f(P, 1, 4, ctypes.byref(w), P, 2, 0, None) == 2       # fp16 output
+    assert d(P, 2, 4, ctypes.byref(w), P, 0, 4, None) == 2       # unknown flag
+    assert f(P, 2, 0, ctypes.byref(w), None, 1, 1, None) == 0    # M = 0
+    i8 = nf4.nf4_weight(P, None, P, 8, 64, 64, 0, 2)
+    bad_group = nf4.nf4_weight(P, None, P, 8, 64, 64, 256, 2)
+    assert f(P, 1, 4, ctypes.byref(bad_group), P, 0, 0, None) == 4
+    four_no_group = nf4.nf4_weight(P, P, P, 8, 64, 64, 0, 1)
+    assert f(P, 1, 4, ctypes.byref(four_no_group), P, 0, 0, None) == 4
+    bad_dtype = nf4.nf4_weight(P, P, P, 8, 64, 64, 256, 7)
+    assert d(P, 1, 4, ctypes.byref(bad_dtype), P, 0, 0, None) == 2
+    assert f(P, 1, 4, ctypes.byref(i8), P + 4, 1, 0, None) == 3
+    mis = nf4.nf4_weight(P, None, P + 4, 8, 64, 64, 0, 2)
+    assert L.nf4_dequantize(ctypes.byref(mis), P, None) == 3
+    # an empty reduction with accumulate leaves the output alone: no launch
+    empty = nf4.nf4_weight(P, P, P, 8, 0, 64, 256, 0)
+    assert f(P, 1, 4, ctypes.byref(empty), P, 0, 1, None) == 0
+    assert L.nf4_set_mma_wait_limit(0) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_ex_calls_without_device_report_device_error():
+    L = nf4.lib()
+    i8 = nf4.nf4_weight(P, None, P, 8, 64, 64, 0, 2)
+    assert L.nf4_matmul_fwd_ex(P, 2, 4, ctypes.byref(i8), P, 1, 1, None) == 5
+    assert L.nf4_quantize_ex(P, 1, 8, 64, 64, 2, P, None, P, None) == 5

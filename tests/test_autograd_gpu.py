@@ -62,5 +62,36 @@ def test_module_is_frozen_and_matches():
     q = nf4.nf4_quantize(W)
     assert torch.equal(Y.detach(), nf4.nf4_matmul_fwd(X.detach(), q))
     ones = torch.ones(5, rows, dtype=torch.bfloat16, device=DEV)
-    assert torch.equal(X.grad, nf4.nf4_matmul_bwd_dx(ones, q).to(torch.bfloat16))
+    assert torch.equal(X.grad, nf4.nf4_matmul_bwd_dx(ones, q, out_dtype=torch.bfloat16))
+    assert nf4.nf4_poll_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["fp4", "int8"])
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float16])
+def test_module_formats_and_input_types(dtype, xdt):
+    """Linear layers over FP4 and int8 weights, with bf16 and fp16 inputs and
+    a bf16 output: forward and input gradient meet the oracle."""
+    rows, cols = 256, 384
+    W = wl.weight(rows, cols, seed=41)
+    layer = NF4Linear(W.to(DEV), dtype=dtype, out_dtype=torch.bfloat16)
+    assert list(layer.parameters()) == []
+    X = wl.normal((6, cols), 1.0, seed=42).to(xdt).to(DEV).requires_grad_(True)
+    Y = layer(X)
+    assert Y.dtype == torch.bfloat16
+    G = wl.normal((6, rows), 0.01, seed=43).to(DEV)
+    (Y.float() * G).sum().backward()
+    assert X.grad.dtype == xdt
+    if dtype == "int8":
+        What = o.int8_dequantize_flat(*o.int8_quantize_flat(W.numpy().reshape(-1))).reshape(rows, cols)
+    else:
+        lv = o.levels_of(dtype)
+        What = o.dequantize(*o.quantize(W.numpy(), lv), rows, cols, lv)
+    Xn = X.detach().float().cpu().numpy()
+    Gn = G.to(torch.bfloat16).to(xdt).float().cpu().numpy()
+    u = 2.0 ** -8     # one bf16 rounding of the output
+    rf = o.rel_frobenius(Y.float().detach().cpu().numpy(), o.matmul_fwd(Xn, What))
+    assert rf <= REL_FRO + u
+    ref = o.matmul_bwd_dx(Gn, What)
+    rfd = o.rel_frobenius(X.grad.float().cpu().numpy(), ref)
+    assert rfd <= REL_FRO + 2 * u
     assert nf4.nf4_poll_device_status() == 0

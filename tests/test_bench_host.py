@@ -70,3 +70,29 @@ def test_sampler_falls_back_to_nvidia_smi(monkeypatch):
     s = bench.clock_sampler(0)
     assert isinstance(s, bench.ClockSampler)
     s.mark(0.0, 1.0)   # accepted and ignored: nvidia-smi samples are not timestamped here
+
+
+def test_algorithmic_bytes_per_format():
+    # 4-bit: half a byte a weight + one absmax code a block + one fp32 a group
+    assert bench.packed_bytes(4096, 4096) == 4096 * 4096 // 2 + 4096 * 64 + 4 * 1024
+    # int8: a byte a weight + one fp32 absmax a block
+    assert bench.packed_bytes(4096, 4096, "int8") == 4096 * 4096 + 4 * 4096 * 64
+    from dequant_gemm_gb300 import workloads as wl
+    p = wl.WORKLOADS["prefill_up_11008x4096_bf16"].projections[0]
+    w = wl.WORKLOADS["prefill_up_11008x4096_bf16"]
+    f, b = bench.fwd_work(p, 4096, w)
+    assert f == 2 * 4096 * 11008 * 4096
+    assert b == bench.packed_bytes(11008, 4096) + 2 * 4096 * 4096 + 2 * 4096 * 11008
+    assert bench.quant_bytes(p, w) == 2 * 11008 * 4096 + bench.packed_bytes(11008, 4096)
+
+
+def test_class_record_roofline():
+    pk = {"hbm_gbs": 8000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    # 1 TFLOP and 1 GB in 1 ms: 1000 TFLOP/s (0.5 of burst), 1000 GB/s
+    r = bench.class_record(1e12, 1e9, 1e-3, pk)
+    assert r["bound"] == "tensor" and abs(r["tensor_frac_burst"] - 0.5) < 1e-12
+    assert abs(r["tensor_frac_sustained"] - 0.625) < 1e-12
+    assert abs(r["roofline_frac"] - 0.5) < 1e-12
+    # memory-bound: 8 GB in 2 ms at 8000 GB/s peak is half the copy bandwidth
+    r = bench.class_record(1e9, 8e9, 2e-3, pk)
+    assert r["bound"] == "hbm" and abs(r["hbm_frac"] - 0.5) < 1e-12 and abs(r["roofline_frac"] - 0.5) < 1e-12

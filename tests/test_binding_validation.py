@@ -83,3 +83,43 @@ def test_well_formed_cpu_call_is_refused_for_the_device_alone():
         nf4.nf4_matmul_fwd(X, weight(), out=torch.empty(2, 16))
     with pytest.raises(ValueError, match="CUDA device"):
         nf4.nf4_quantize(torch.zeros(16, 128))
+
+
+def test_int8_and_fp4_weights_are_checked_by_their_own_layout():
+    X = torch.zeros(2, 128, dtype=torch.float16)
+    w8 = nf4.alloc_weight(16, 128, "cpu", "int8")
+    assert w8.codes.dtype == torch.int8 and w8.absmax_q is None and w8.absmax_scale.numel() == 32
+    with pytest.raises(ValueError, match="CUDA device"):
+        nf4.nf4_matmul_fwd(X, w8)
+    bad = nf4.NF4Weight(w8.codes, None, w8.absmax_scale[:-1], 16, 128, "int8")
+    with pytest.raises(ValueError, match="absmax_scale"):
+        nf4.nf4_matmul_fwd(X, bad)
+    mixed = nf4.NF4Weight(w8.codes, torch.empty(32, dtype=torch.uint8), w8.absmax_scale, 16, 128,
+                          "int8")
+    with pytest.raises(ValueError, match="no absmax_q"):
+        nf4.nf4_matmul_fwd(X, mixed)
+    w4 = nf4.alloc_weight(16, 128, "cpu", "fp4")
+    as_int8 = nf4.NF4Weight(w4.codes, None, w4.absmax_scale, 16, 128, "int8")
+    with pytest.raises(ValueError, match="int8"):
+        nf4.nf4_matmul_fwd(X, as_int8)
+    with pytest.raises(ValueError, match="dtype"):
+        nf4.alloc_weight(16, 128, "cpu", "int4")
+
+
+def test_element_types_and_accumulate_are_checked():
+    w = weight()
+    with pytest.raises(ValueError, match="bfloat16 or float16"):
+        nf4.nf4_matmul_fwd(torch.zeros(2, 128), w)
+    with pytest.raises(ValueError, match="float32 or bfloat16"):
+        nf4.nf4_matmul_fwd(torch.zeros(2, 128, dtype=torch.bfloat16), w, out_dtype=torch.float16)
+    with pytest.raises(ValueError, match="accumulate"):
+        nf4.nf4_matmul_bwd_dx(torch.zeros(2, 16, dtype=torch.float16), w, accumulate=True)
+    with pytest.raises(ValueError, match="shape"):
+        nf4.nf4_matmul_fwd(torch.zeros(2, 128, dtype=torch.bfloat16), w,
+                           out=torch.empty(2, 8, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="float32 or bfloat16"):
+        nf4.nf4_quantize(torch.zeros(16, 128, dtype=torch.float16))
+    with pytest.raises(ValueError, match="nf4"):
+        nf4.nf4_quantize(torch.zeros(16, 128), out=nf4.alloc_weight(16, 128, "cpu", "fp4"))
+    with pytest.raises(ValueError, match="CUDA device"):
+        nf4.nf4_quantize(torch.zeros(16, 128, dtype=torch.bfloat16), dtype="int8")

@@ -134,11 +134,16 @@ def test_memory_size_invariant_matches_quoted_savings():
     assert 0.05 <= dq_extra <= 0.10               # "further 5-10%"
 
 
-def test_oracle_views_match_full_dequant():
+@pytest.mark.parametrize("dtype", ["nf4", "fp4", "int8"])
+def test_oracle_views_match_full_dequant(dtype):
     from tests.oracle_views import OracleWeight
     W = (np.random.default_rng(21).standard_normal((24, 704)) * 0.02).astype(np.float32)
-    full = o.dequantize(*o.quantize(W), 24, 704)
-    ow = OracleWeight(W)
+    if dtype == "int8":
+        full = o.int8_dequantize_flat(*o.int8_quantize_flat(W.reshape(-1))).reshape(24, 704)
+    else:
+        lv = o.levels_of(dtype)
+        full = o.dequantize(*o.quantize(W, lv), 24, 704, lv)
+    ow = OracleWeight(W, dtype)
     assert np.array_equal(ow.rows([0, 5, 23]), full[[0, 5, 23]])
     cols = OracleWeight.columns_of([0, 3, 10])
     assert np.array_equal(ow.col_blocks([0, 3, 10]), full[:, cols])
