@@ -59,6 +59,22 @@
 namespace nf4 {
 namespace {
 
+#ifndef NF4_TC_FWD_GROUPS
+#define NF4_TC_FWD_GROUPS 4
+#endif
+#ifndef NF4_TC_DX_GROUPS
+#define NF4_TC_DX_GROUPS 4
+#endif
+#ifndef NF4_TC_DX_STAGES
+#define NF4_TC_DX_STAGES 6
+#endif
+#ifndef NF4_TC_DX_ASLOTS
+#define NF4_TC_DX_ASLOTS 4
+#endif
+#ifndef NF4_TC_DX_LUT_COPIES
+#define NF4_TC_DX_LUT_COPIES 32
+#endif
+
 constexpr int kTileRows = 128;               // MMA M
 constexpr uint32_t kTmemCols = 512;
 
@@ -82,9 +98,16 @@ template <bool kDx, int kBN, bool kInt8>
 struct Cfg {
   static constexpr bool kPair = kBN == 256;
   static constexpr int kCg = kPair ? 2 : 1;          // tcgen05 cta_group
-  // dequant warp groups: a group needs several MMA stage times per stage
-  static constexpr int kGroups = 4;
-  static constexpr int kDqWarps = 4 * kGroups;
+  // 16 dequant warps in kGroups groups that take the stages in turn; a
+  // group's kGroupWarps warps split a stage, each thread taking kPartCols of
+  // a 64-weight run. Fewer, larger groups finish a stage sooner (the latency
+  // the pipeline must cover) at the same throughput.
+  static constexpr int kDqWarps = 16;
+  static constexpr int kGroups = kDx ? NF4_TC_DX_GROUPS : NF4_TC_FWD_GROUPS;
+  static constexpr int kGroupWarps = kDqWarps / kGroups;
+  static constexpr int kParts = kGroupWarps / 4;          // threads per 64-weight run
+  static constexpr int kPartCols = 64 / kParts;           // weights a thread dequantizes
+  static_assert(kGroups == 2 || kGroups == 4, "dequant groups");
   static constexpr int kThreads = 64 + 32 * kDqWarps;
   // code bytes of a stage: 128 weight rows (forward) or 64 weight rows of 128
   // columns (input gradient) x 64 weights, at 4 or 8 bits
@@ -94,15 +117,20 @@ struct Cfg {
   // the copies run further ahead (a shared 5-deep ring left the MMA waiting
   // on copy latency plus dequant every stage).
   static constexpr int kAStageBytes = kDx ? kTileRows * 64 * 2 : 0;
-  static constexpr int kStages = kDx ? (kBN == 64 ? 8 : 6) : (kBN == 64 ? 12 : 8);
-  static constexpr int kASlots = kDx ? 4 : kStages;   // forward: the TMEM slot of the stage
+  static constexpr int kStages = kDx ? (kBN == 64 ? 8 : (kInt8 ? 6 : NF4_TC_DX_STAGES))
+                                     : (kBN == 64 ? 12 : 8);
+  static constexpr int kASlots = kDx ? NF4_TC_DX_ASLOTS : kStages;   // forward: the TMEM slot of the stage
+  // lane-private copies of the level pair table: 32 make every lookup of a
+  // warp conflict-free; 16 halve the table at a two-way conflict
+  static constexpr int kLutCopies = kDx ? NF4_TC_DX_LUT_COPIES : 32;
+  static constexpr int kLutShift = kLutCopies == 32 ? 7 : 6;   // log2 bytes per table entry
   static constexpr int kBRows = kPair ? kBN / 2 : kBN;   // tokens staged per CTA
   static constexpr int kActStageBytes = kBRows * 128;    // 64 16-bit values per token row
   static constexpr uint32_t kTmemA0 = kBN;
   // the forward's A slots follow the accumulator; the input gradient holds
   // only the accumulator (BN columns, a power of two >= 32)
   static constexpr uint32_t kTmemAlloc = kDx ? static_cast<uint32_t>(kBN) : kTmemCols;
-  static constexpr int kLutBytes = kInt8 ? 0 : kHalfPairTableBytes;
+  static constexpr int kLutBytes = kInt8 ? 0 : 256 * kLutCopies * 4;
   static constexpr int kOffAct = 0;
   static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
   static constexpr int kOffCodes = kOffA + kASlots * kAStageBytes;
@@ -115,6 +143,15 @@ struct Cfg {
   static_assert(kOffA % 1024 == 0 && kOffCodes % 1024 == 0, "swizzled tiles");
   static_assert(kBN == 64 || kBN == 128 || kBN == 256, "token tile");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  // Every mbarrier a dequant group waits on with a parity test must not be
+  // able to run a phase behind the one the group expects (the test cannot
+  // tell them apart; a variant with 3 A slots for 4 groups deadlocked on
+  // exactly that). Each A slot is therefore waited by one group only, in
+  // order; the forward's copy slots likewise; the input gradient's copy
+  // slots, shared between groups, are waited on only after the A slot,
+  // which orders them (kStages >= kASlots).
+  static_assert(kASlots % kGroups == 0, "A slots per dequant group");
+  static_assert(kDx ? kStages >= kASlots : kStages % kGroups == 0, "copy slots per dequant group");
 };
 
 struct TcArgs {
@@ -134,9 +171,24 @@ struct TcArgs {
   int* status;
 };
 
-// Level pair tables of the 4-bit formats (fp16 levels, layout in common.cuh).
+// Level pair tables of the 4-bit formats (fp16 levels, layout in common.cuh),
+// and the same with 16 lane copies: entry b of copy l at word 16 b + l.
 __device__ __align__(128) const HalfPairTable kHalfPairsNf4 = make_half_pair_table(kFmtNf4);
 __device__ __align__(128) const HalfPairTable kHalfPairsFp4 = make_half_pair_table(kFmtFp4);
+
+struct HalfPairTable16 {
+  uint32_t w[256 * 16];
+};
+
+constexpr HalfPairTable16 make_half_pair_table16(int fmt) {
+  HalfPairTable16 t{};
+  const HalfPairTable full = make_half_pair_table(fmt);
+  for (int b = 0; b < 256; ++b)
+    for (int l = 0; l < 16; ++l) t.w[16 * b + l] = full.w[32 * b + l];
+  return t;
+}
+__device__ __align__(128) const HalfPairTable16 kHalfPairs16Nf4 = make_half_pair_table16(kFmtNf4);
+__device__ __align__(128) const HalfPairTable16 kHalfPairs16Fp4 = make_half_pair_table16(kFmtFp4);
 
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
@@ -160,7 +212,8 @@ __device__ __forceinline__ uint32_t pack_operand(float lo, float hi) {
 }
 
 // 16 code bytes of a 4-bit format (32 weights) -> 16 packed operand words.
-template <bool kF16>
+// tab is this lane's copy of the level pair table, entries 2^kShift bytes apart.
+template <bool kF16, int kShift = 7>
 __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab, float2 ahat2,
                                                uint32_t (&v)[16]) {
   const uint32_t words[4] = {c.x, c.y, c.z, c.w};
@@ -169,7 +222,7 @@ __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
-      const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
+      const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << kShift));
       const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
       v[4 * j + b] = pack_operand<kF16>(lv.x, lv.y);
     }
@@ -264,7 +317,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
     for (int a = 0; a < kASlots; ++a) {
       // one arrival per warp of the stage's group, in both CTAs of a pair
-      tc::mbar_init(dq_bar(a), 4 * kCg);
+      tc::mbar_init(dq_bar(a), C::kGroupWarps * kCg);
       tc::mbar_init(afree_bar(a), 1);
     }
     tc::mbar_init(accum_bar, 1);
@@ -272,7 +325,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     *abort_flag = 0;
     tc::fence_barrier_init();
     if constexpr (!kInt8) {
-      const HalfPairTable* lut = p.fmt == kFmtFp4 ? &kHalfPairsFp4 : &kHalfPairsNf4;
+      const void* lut;
+      if constexpr (C::kLutCopies == 32) lut = p.fmt == kFmtFp4 ? &kHalfPairsFp4 : &kHalfPairsNf4;
+      else lut = p.fmt == kFmtFp4 ? &kHalfPairs16Fp4 : &kHalfPairs16Nf4;
       tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
       bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), lut, C::kLutBytes, lut_bar);
     }
@@ -416,9 +471,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       else tc::mbar_arrive(dq_bar(a));
     };
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int grp = (warp - 2) >> 2;        // takes the stages i % kGroups == grp
+    const int grp = (warp - 2) / C::kGroupWarps;   // takes the stages i % kGroups == grp
+    const int gw = (warp - 2) % C::kGroupWarps;    // warp within the group
+    constexpr int kHalves = 2 / C::kParts;          // 32-weight halves of a run per thread
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const uint8_t* tab = smem + C::kOffLut + 4 * lane;
+    const uint8_t* tab = smem + C::kOffLut + 4 * (lane % C::kLutCopies);
     // block scale: 4-bit ahat = fl32(fl32(a8 s2) / 255); int8 absmax / 127
     auto block_scale = [&](uint32_t a8v, float sv) {
       return kInt8 ? __fdiv_rn(sv, 127.0f) : dequant_absmax(a8v, sv);
@@ -466,28 +523,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         if (!__all_sync(0xffffffffu, go)) continue;
         const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
         const uint32_t dst = tmem + lane_base + kTmemA0 + 32u * slot;
-        if constexpr (kInt8) {
-          // row tile_row's 64 bytes, 64-byte swizzle
-          const int sw = (tile_row >> 1) & 3;
+        // this thread's 32-weight halves of the row's 64: hf = half0 ..
+        const int half0 = (gw >> 2) * kHalves;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
+        for (int k = 0; k < kHalves; ++k) {
+          const int hf = half0 + k;
+          uint32_t v[16];
+          if constexpr (kInt8) {
+            // row tile_row's 64 bytes, 64-byte swizzle
+            const int sw = (tile_row >> 1) & 3;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               const int c = 2 * hf + cc;
               const uint4 w = *reinterpret_cast<const uint4*>(cst + tile_row * 64 + 16 * (c ^ sw));
               dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
             }
-            tc::tmem_st16(dst + 16u * hf, v);
+          } else {
+            const uint8_t* crow = cst + tile_row * 32;
+            dequant16_4bit<kF16, C::kLutShift>(*reinterpret_cast<const uint4*>(crow + 16 * hf), tab, ahat2, v);
           }
-        } else {
-          const uint8_t* crow = cst + tile_row * 32;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            dequant16_4bit<kF16>(*reinterpret_cast<const uint4*>(crow + 16 * hf), tab, ahat2, v);
-            tc::tmem_st16(dst + 16u * hf, v);
-          }
+          tc::tmem_st16(dst + 16u * hf, v);
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
@@ -496,13 +551,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       }
     } else {
       // Thread t of the group dequantizes weight row t % 64 of the stage over
-      // the tile's columns 64 (t / 64) .. + 63, one absmax block, as the
-      // forward walks a row. The 64 results are one 128-byte row of a
-      // 128-byte-swizzled MN-major atom of the A tile (64 weight columns along
-      // M x 8 weight rows along K per 1 KB atom; atom (column half h, row
-      // group g) at (2 g + h) KB).
-      const int t = ((warp - 2) & 3) * 32 + lane;
-      const int rr = t & 63, h = t >> 6;
+      // kPartCols of the tile's columns 64 h .. 64 h + 63, one absmax block,
+      // as the forward walks a row. A run of 64 results is one 128-byte row of
+      // a 128-byte-swizzled MN-major atom of the A tile (64 weight columns
+      // along M x 8 weight rows along K per 1 KB atom; atom (column half h,
+      // row group g) at (2 g + h) KB).
+      const int t = gw * 32 + lane;
+      const int rr = t & 63, part = t >> 6;
+      const int h = part / C::kParts;                 // 64-column block of the tile
+      const int half0 = (part % C::kParts) * kHalves; // first 32-column half of the run
       const int64_t kb = (r0 >> 6) + h;
       const bool kb_ok = kb < p.nblk;
       const int ao = (2 * (rr >> 3) + h) * 1024 + (rr & 7) * 128;
@@ -524,58 +581,62 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const float ahat = rok ? block_scale(a8v, sv) : 0.0f;
         const float2 ahat2 = make_float2(ahat, ahat);
         load_scale(i + kGroups);
-        bool go = !*abort_flag && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag),
-                                         kRoleCompute);
-        // the A slot's previous tile (stage i - kASlots) has been read by its MMAs
+        // First the A slot: its previous tile (stage i - kASlots) has been read
+        // by its MMAs. Only then the stage's copies: once MMA(i - kASlots) is
+        // done, so is MMA(i - kStages), whose dequant saw the copy slot's
+        // previous phase complete, so this parity wait cannot pass a phase
+        // early (several groups share a copy slot when kStages is not a
+        // multiple of kGroups, and a parity wait cannot tell a phase still
+        // pending from the one before it).
         const int as = i % kASlots;
+        bool go = !*abort_flag;
         if (go && i >= kASlots)
           go = waited(tc::mbar_wait_abortable(afree_bar(as), ((i / kASlots) - 1) & 1, abort_flag),
                       kRoleCompute);
+        go = go && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag), kRoleCompute);
         if (!__all_sync(0xffffffffu, go)) continue;
         const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
         uint8_t* arow = smem + C::kOffA + as * C::kAStageBytes + ao;
-        uint32_t v[32];
-        if constexpr (kInt8) {
-          // row rr's chunks 4 h .. 4 h + 3 of 128 bytes, 128-byte swizzle
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const uint4 w =
-                *reinterpret_cast<const uint4*>(cst + rr * 128 + 16 * ((4 * h + cc) ^ (rr & 7)));
-            dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
+        for (int k = 0; k < kHalves; ++k) {
+          const int hf = half0 + k;                   // columns 32 hf .. + 31 of the run
+          uint32_t v[16];
+          if constexpr (kInt8) {
+            // row rr's chunks 4 h + 2 hf, + 1 of 128 bytes, 128-byte swizzle
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const uint4 w = *reinterpret_cast<const uint4*>(
+                  cst + rr * 128 + 16 * ((4 * h + 2 * hf + cc) ^ (rr & 7)));
+              dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
+            }
+          } else {
+            // row rr's chunk 2 h + hf of 64 bytes, 64-byte swizzle
+            const int csw = (rr >> 1) & 3;
+            dequant16_4bit<kF16, C::kLutShift>(
+                *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw)), tab,
+                ahat2, v);
           }
-        } else {
-          // row rr's chunks 2 h, 2 h + 1 of 64 bytes, 64-byte swizzle
-          const int csw = (rr >> 1) & 3;
+          // columns 32 hf + 8 j .. + 7 form chunk 4 hf + j of the atom row
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const uint4 w =
-                *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw));
-            uint32_t part[16];
-            dequant16_4bit<kF16>(w, tab, ahat2, part);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[16 * hf + e] = part[e];
-          }
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(arow + 16 * ((4 * hf + j) ^ asw)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
-        // columns 8 j .. 8 j + 7 form chunk j of the atom row
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(arow + 16 * (j ^ asw)) =
-              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         tc::fence_proxy_async();   // the MMA reads the tile through the async proxy
         __syncwarp();
         if (lane == 0) arrive_dq(as);
       }
     }
 
-    // epilogue: accumulator lanes are tile rows, columns are tokens; the
-    // groups share out the 16-column chunks
+    // epilogue: accumulator lanes are tile rows, columns are tokens
     if (!*abort_flag) waited(tc::mbar_wait_abortable(accum_bar, 0, abort_flag), kRoleEpilogue);
     tc::fence_after_sync();
     if (!*abort_flag) {
       const int64_t rg = r0 + tile_row;
       const int64_t nd = kDx ? p.K : p.N;
       const bool vrow = rg < nd;
-      for (int c = 16 * grp; c < p.bn; c += 16 * kGroups) {
+      // the four warps of each lane quarter share out the 16-column chunks
+      for (int c = 16 * ((warp - 2) >> 2); c < p.bn; c += 64) {
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
         tc::tmem_wait_ld();
