@@ -8,20 +8,28 @@
 // then enters the MMA in the same type); outputs fp32 or bf16, overwritten or
 // added to ("bitsandbytes", quantized-GEMM and 4-bit paragraphs).
 //
-// One CTA computes a 128 x BN tile of D = A * B^T with the weight as the
-// 128-row A operand and the tokens as the BN-column B operand (BN = 64, 128 or
-// 256; 256 on CTA pairs that share one 256 x 256 MMA), looping over the
-// reduction in stages of 64:
+// The kernel is persistent: a CTA (or CTA pair) takes the output tile units
+// c, c + G, c + 2G, ... of the launch (G = the number of CTAs or pairs, at
+// most one per SM). A unit is a 128 x BN tile of D = A * B^T with the weight
+// as the 128-row A operand and the tokens as the BN-column B operand (BN =
+// 64, 128 or 256; 256 on CTA pairs that share one 256 x 256 MMA) over one
+// reduction range, walked in stages of 64. One stage counter runs across the
+// units, so the copy ring, the A slots and the dequant groups never restart:
 //   * warp 0 TMA-loads the stage's activation tile (16-bit, 128-byte swizzle,
 //     the K-major B operand) and its code tile from one elected lane;
-//   * the dequant warps, in four groups of four that take the stages in
-//     turn, dequantize the codes (level * dequantized absmax, rounded to the
+//   * warps 2-17, in four groups of four that take the stages in turn,
+//     dequantize the codes (level * dequantized absmax, rounded to the
 //     activation type) into the stage's A operand;
 //   * warp 1 issues tcgen05.mma (128 x BN x 16) from one elected lane into
-//     an fp32 accumulator in tensor memory and commits each stage back to the
-//     producer;
-//   * the dequant warps then read the accumulator with tcgen05.ld and store
-//     the outputs (32 consecutive outputs of one token per warp store).
+//     an fp32 accumulator in tensor memory, commits each stage back to the
+//     producer and each unit to the epilogue;
+//   * warps 18-21 read a finished accumulator with tcgen05.ld and store the
+//     outputs while the MMAs of the next unit run into the other of two
+//     accumulator buffers. Where there is one accumulator only (the forward
+//     at BN = 256, whose A operand slots take the other half of tensor
+//     memory, and BN = 64, whose short units leave 4 warps too little time),
+//     the dequant warps drain it between units instead, as the copies of the
+//     next unit are already under way.
 //
 // Both directions walk the weight along its rows, one thread per (row, 64
 // columns) run, which is one absmax block. A 4-bit code byte gives both
@@ -43,7 +51,7 @@
 // between lanes.
 //
 // When the output tiles alone cannot fill the GPU and the output is fp32,
-// the reduction is split across CTAs and summed with atomics into a zeroed
+// the reduction is split across units and summed with atomics into a zeroed
 // (or, accumulating, the caller's) output. A bf16 output is never split.
 //
 // Every mbarrier wait is bounded; a CTA that gives up records a timeout in the
@@ -59,56 +67,33 @@
 namespace nf4 {
 namespace {
 
-#ifndef NF4_TC_FWD_GROUPS
-#define NF4_TC_FWD_GROUPS 4
-#endif
-#ifndef NF4_TC_DX_GROUPS
-#define NF4_TC_DX_GROUPS 4
-#endif
-#ifndef NF4_TC_DX_STAGES
-#define NF4_TC_DX_STAGES 6
-#endif
-#ifndef NF4_TC_DX_ASLOTS
-#define NF4_TC_DX_ASLOTS 4
-#endif
-#ifndef NF4_TC_DX_LUT_COPIES
-#define NF4_TC_DX_LUT_COPIES 32
-#endif
-
 constexpr int kTileRows = 128;               // MMA M
 constexpr uint32_t kTmemCols = 512;
 
 // Per-direction, per-token-tile and per-format configuration and shared-memory
 // layout. The token tile BN (MMA N) sets the stage size; smaller tiles get
 // deeper rings, so that enough code bytes are in flight per SM to cover the
-// memory latency. Tensor memory holds the BN fp32 accumulator columns, then
-// (forward) one 32-column A-operand slot per stage.
+// memory latency. Tensor memory holds the accumulator buffers (BN fp32
+// columns each), then (forward) one 32-column A-operand slot per stage.
 //
 // The BN = 256 tiles run on CTA pairs (cta_group::2): the two CTAs of a
 // cluster hold 128 weight rows (columns) each, and half of the token tile
 // each; the MMA warp of the even CTA issues 256 x 256 x 16 MMAs over both
 // SMs. Each SM then stages and reads only half of the activation tile, which
-// is most of the shared-memory traffic of a stage. The dequant warps of both
-// CTAs arrive on the issuing CTA's stage barrier. The arrival takes the
-// instruction's default (CTA-scope) release: by then the warp's tensor-memory
-// stores have retired (tcgen05.wait::st) and the stage's copies have been
-// seen complete, and a cluster-scope release was measured to stall the
-// arriving thread for 1-2.5K cycles on a busy SM, enough to halve the MMA rate.
+// is most of the shared-memory traffic of a stage. The dequant and epilogue
+// warps of both CTAs arrive on the issuing CTA's barriers. The arrival takes
+// the instruction's default (CTA-scope) release: by then the warp's
+// tensor-memory accesses have retired and the stage's copies have been seen
+// complete, and a cluster-scope release was measured to stall the arriving
+// thread for 1-2.5K cycles on a busy SM, enough to halve the MMA rate.
 template <bool kDx, int kBN, bool kInt8>
 struct Cfg {
   static constexpr bool kPair = kBN == 256;
   static constexpr int kCg = kPair ? 2 : 1;          // tcgen05 cta_group
-  // 16 dequant warps in kGroups groups that take the stages in turn; a
-  // group's kGroupWarps warps split a stage, each thread taking kPartCols of
-  // a 64-weight run. Fewer, larger groups finish a stage sooner (the latency
-  // the pipeline must cover) at the same throughput.
+  // 16 dequant warps in 4 groups of 4 that take the stages in turn (measured:
+  // 2 groups of 8 splitting each stage, 8-12% slower)
   static constexpr int kDqWarps = 16;
-  static constexpr int kGroups = kDx ? NF4_TC_DX_GROUPS : NF4_TC_FWD_GROUPS;
-  static constexpr int kGroupWarps = kDqWarps / kGroups;
-  static constexpr int kParts = kGroupWarps / 4;          // threads per 64-weight run
-  static constexpr int kPartCols = 64 / kParts;           // weights a thread dequantizes
-  static_assert(kGroups == 2 || kGroups == 4, "dequant groups");
-  static constexpr int kThreads = 64 + 32 * kDqWarps;
+  static constexpr int kGroups = 4;
   // code bytes of a stage: 128 weight rows (forward) or 64 weight rows of 128
   // columns (input gradient) x 64 weights, at 4 or 8 bits
   static constexpr int kCodesStageBytes = kInt8 ? 8192 : 4096;
@@ -117,26 +102,36 @@ struct Cfg {
   // the copies run further ahead (a shared 5-deep ring left the MMA waiting
   // on copy latency plus dequant every stage).
   static constexpr int kAStageBytes = kDx ? kTileRows * 64 * 2 : 0;
-  static constexpr int kStages = kDx ? (kBN == 64 ? 8 : (kInt8 ? 6 : NF4_TC_DX_STAGES))
-                                     : (kBN == 64 ? 12 : 8);
-  static constexpr int kASlots = kDx ? NF4_TC_DX_ASLOTS : kStages;   // forward: the TMEM slot of the stage
-  // lane-private copies of the level pair table: 32 make every lookup of a
-  // warp conflict-free; 16 halve the table at a two-way conflict
-  static constexpr int kLutCopies = kDx ? NF4_TC_DX_LUT_COPIES : 32;
-  static constexpr int kLutShift = kLutCopies == 32 ? 7 : 6;   // log2 bytes per table entry
+  static constexpr int kStages = kDx ? (kBN == 64 ? 8 : 6) : (kBN == 64 ? 12 : 8);
+  static constexpr int kASlots = kDx ? 4 : kStages;   // forward: the TMEM slot of the stage
   static constexpr int kBRows = kPair ? kBN / 2 : kBN;   // tokens staged per CTA
   static constexpr int kActStageBytes = kBRows * 128;    // 64 16-bit values per token row
-  static constexpr uint32_t kTmemA0 = kBN;
-  // the forward's A slots follow the accumulator; the input gradient holds
-  // only the accumulator (BN columns, a power of two >= 32)
-  static constexpr uint32_t kTmemAlloc = kDx ? static_cast<uint32_t>(kBN) : kTmemCols;
-  static constexpr int kLutBytes = kInt8 ? 0 : 256 * kLutCopies * 4;
+  // Two accumulator buffers where they fit next to the forward's A slots,
+  // and where a unit is long enough for 4 epilogue warps to drain one while
+  // the next fills the other: at BN = 64 (short, often split units whose
+  // outputs go out as atomics) the 16 dequant warps drain a single buffer
+  // between units instead (4 epilogue warps there measured 13% slower).
+  static constexpr int kAccBufs = kBN >= 128 && 2 * kBN + (kDx ? 0 : 32 * kStages) <= 512 ? 2 : 1;
+  // With two buffers, 4 epilogue warps, one per tensor-memory lane quarter
+  // (22 warps leave 80 registers a thread; 18, without them, 96).
+  static constexpr int kEpiWarps = kAccBufs == 2 ? 4 : 0;
+  static constexpr int kFirstEpiWarp = 2 + kDqWarps;
+  static constexpr int kThreads = 32 * (2 + kDqWarps + kEpiWarps);
+  static constexpr uint32_t kTmemA0 = kAccBufs * kBN;
+  // the input gradient holds only the accumulators (a power of two >= 32)
+  static constexpr uint32_t kTmemAlloc = kDx ? static_cast<uint32_t>(kAccBufs * kBN) : kTmemCols;
+  // arrivals that free an accumulator buffer: the epilogue warps, or with a
+  // single buffer the dequant warps that drain it, of both CTAs of a pair
+  static constexpr int kDrainWarps = kAccBufs == 2 ? kEpiWarps : kDqWarps;
+  static constexpr int kLutBytes = kInt8 ? 0 : kHalfPairTableBytes;
   static constexpr int kOffAct = 0;
   static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
   static constexpr int kOffCodes = kOffA + kASlots * kAStageBytes;
   static constexpr int kOffLut = kOffCodes + kStages * kCodesStageBytes;
   static constexpr int kOffBars = kOffLut + kLutBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2;
+  // full, empty per stage; dq, afree per A slot; accumulator full, empty per
+  // buffer; the level table; the final drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   static_assert(kDx || kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
@@ -162,8 +157,11 @@ struct TcArgs {
   int nblk;                // K / 64
   int bn;                  // token tile
   int fmt;                 // 4-bit table: kFmtNf4 or kFmtFp4
-  int stages_total;
+  int stages_total;        // reduction stages of the whole product
   int stages_per_split;
+  int row_units;           // tile units along the rows (one per CTA or pair)
+  int m_tiles;             // token tiles
+  int units;               // row_units * m_tiles * splits
   int atomic_out;
   int out_bf16;
   int accumulate;
@@ -171,24 +169,16 @@ struct TcArgs {
   int* status;
 };
 
-// Level pair tables of the 4-bit formats (fp16 levels, layout in common.cuh),
-// and the same with 16 lane copies: entry b of copy l at word 16 b + l.
-__device__ __align__(128) const HalfPairTable kHalfPairsNf4 = make_half_pair_table(kFmtNf4);
-__device__ __align__(128) const HalfPairTable kHalfPairsFp4 = make_half_pair_table(kFmtFp4);
-
-struct HalfPairTable16 {
-  uint32_t w[256 * 16];
+// One tile unit as a CTA sees it.
+struct Unit {
+  int64_t r0;              // first tile row (weight row or column) of this CTA
+  int64_t m0;              // first token
+  int s_begin, nst;        // reduction stages
 };
 
-constexpr HalfPairTable16 make_half_pair_table16(int fmt) {
-  HalfPairTable16 t{};
-  const HalfPairTable full = make_half_pair_table(fmt);
-  for (int b = 0; b < 256; ++b)
-    for (int l = 0; l < 16; ++l) t.w[16 * b + l] = full.w[32 * b + l];
-  return t;
-}
-__device__ __align__(128) const HalfPairTable16 kHalfPairs16Nf4 = make_half_pair_table16(kFmtNf4);
-__device__ __align__(128) const HalfPairTable16 kHalfPairs16Fp4 = make_half_pair_table16(kFmtFp4);
+// Level pair tables of the 4-bit formats (fp16 levels, layout in common.cuh).
+__device__ __align__(128) const HalfPairTable kHalfPairsNf4 = make_half_pair_table(kFmtNf4);
+__device__ __align__(128) const HalfPairTable kHalfPairsFp4 = make_half_pair_table(kFmtFp4);
 
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
@@ -212,8 +202,8 @@ __device__ __forceinline__ uint32_t pack_operand(float lo, float hi) {
 }
 
 // 16 code bytes of a 4-bit format (32 weights) -> 16 packed operand words.
-// tab is this lane's copy of the level pair table, entries 2^kShift bytes apart.
-template <bool kF16, int kShift = 7>
+// tab is this lane's copy of the level pair table (entries 128 bytes apart).
+template <bool kF16>
 __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab, float2 ahat2,
                                                uint32_t (&v)[16]) {
   const uint32_t words[4] = {c.x, c.y, c.z, c.w};
@@ -222,7 +212,7 @@ __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
-      const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << kShift));
+      const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
       const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
       v[4 * j + b] = pack_operand<kF16>(lv.x, lv.y);
     }
@@ -262,7 +252,7 @@ __device__ __forceinline__ void store_out(void* out, int64_t i, float v, int out
 
 // The first nm of 16 consecutive tokens' outputs of one tile row (stride nd),
 // bf16 or accumulating. Kept out of line: its registers would otherwise
-// count against the whole kernel's budget of 96 a thread.
+// count against the whole kernel's budget of 80 or 96 a thread.
 __device__ __noinline__ void store_out16(void* out, int64_t i0, int64_t nd, int nm, uint4 a,
                                          uint4 b, uint4 c, uint4 d, int out_bf16,
                                          int accumulate) {
@@ -281,7 +271,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   constexpr bool kPair = C::kPair;
   constexpr int kCg = C::kCg;
   constexpr int kStages = C::kStages;
+  constexpr int kASlots = C::kASlots;
   constexpr int kGroups = C::kGroups;
+  constexpr int kAccBufs = C::kAccBufs;
   constexpr int kActStageBytes = C::kActStageBytes;
   constexpr int kCodesStageBytes = C::kCodesStageBytes;
   constexpr uint32_t kTmemA0 = C::kTmemA0;
@@ -289,26 +281,37 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t bars = tc::smem_addr(smem + C::kOffBars);
-  constexpr int kASlots = C::kASlots;
   // copy ring: full / empty per stage slot; A ring: dq (written) / afree
-  // (read by the MMAs; input gradient only) per A slot
+  // (read by the MMAs; input gradient only) per A slot; accumulator buffers:
+  // accf (all MMAs of a unit done) / acce (drained by the epilogue)
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto dq_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
   auto afree_bar = [&](int a) { return bars + 8u * (2 * kStages + kASlots + a); };
-  const uint32_t accum_bar = bars + 8u * (2 * kStages + 2 * kASlots);
-  const uint32_t lut_bar = accum_bar + 8u;
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 * kASlots + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 * kASlots + 2 + b); };
+  const uint32_t lut_bar = bars + 8u * (2 * kStages + 2 * kASlots + 4);
+  const uint32_t drain_bar = lut_bar + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // A pair is the cluster (2, 1, 1): CTA 2p + rank holds rows 128 (2p + rank),
-  // the token half rank of the tile, and rank 0 issues the pair's MMAs.
+  // A pair is the cluster (2, 1, 1): its CTAs hold rows 128 (2 r + rank) of
+  // a unit's 256, the token half rank of the tile, and rank 0 issues the MMAs.
   const uint32_t rank = kPair ? tc::cluster_ctarank() : 0u;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * p.bn;
-  const int s_begin = blockIdx.z * p.stages_per_split;
-  const int nst = min(p.stages_per_split, p.stages_total - s_begin);
+  const int cid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ncl = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // unit u: row unit fastest, then token tile, then reduction split
+  auto unit_at = [&](int u) {
+    Unit t;
+    const int rt = u % p.row_units, rest = u / p.row_units;
+    const int mt = rest % p.m_tiles, sp = rest / p.m_tiles;
+    t.r0 = (static_cast<int64_t>(rt) * kCg + rank) * kTileRows;
+    t.m0 = static_cast<int64_t>(mt) * p.bn;
+    t.s_begin = sp * p.stages_per_split;
+    t.nst = min(p.stages_per_split, p.stages_total - t.s_begin);
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -317,17 +320,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
     for (int a = 0; a < kASlots; ++a) {
       // one arrival per warp of the stage's group, in both CTAs of a pair
-      tc::mbar_init(dq_bar(a), C::kGroupWarps * kCg);
+      tc::mbar_init(dq_bar(a), 4 * kCg);
       tc::mbar_init(afree_bar(a), 1);
     }
-    tc::mbar_init(accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(accf_bar(b), 1);
+      tc::mbar_init(acce_bar(b), C::kDrainWarps * kCg);
+    }
     tc::mbar_init(lut_bar, 1);
+    tc::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
     if constexpr (!kInt8) {
-      const void* lut;
-      if constexpr (C::kLutCopies == 32) lut = p.fmt == kFmtFp4 ? &kHalfPairsFp4 : &kHalfPairsNf4;
-      else lut = p.fmt == kFmtFp4 ? &kHalfPairs16Fp4 : &kHalfPairs16Nf4;
+      const HalfPairTable* lut = p.fmt == kFmtFp4 ? &kHalfPairsFp4 : &kHalfPairsNf4;
       tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
       bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), lut, C::kLutBytes, lut_bar);
     }
@@ -358,55 +363,98 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     if (r == tc::kWaitTimeout) fail(role);
     return r == tc::kWaitDone;
   };
+  // an arrival that frees accumulator buffer b (on the issuing CTA of a pair)
+  auto arrive_acce = [&](int b) {
+    if constexpr (kPair) tc::mbar_arrive_remote(tc::mapa(acce_bar(b), 0));
+    else tc::mbar_arrive(acce_bar(b));
+  };
+  const int q = warp & 3;                      // TMEM lane quarter of this warp
+  const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+  // tile row (forward: weight row; input gradient: weight column) held by
+  // this thread's accumulator lane
+  const int tile_row = 32 * q + lane;
+
+  // Drain accumulator buffer b of unit t (16-column chunks c0, c0 + step, ...
+  // of this warp's lane quarter) into the outputs.
+  auto drain = [&](const Unit& t, int b, int c0, int step) {
+    const int64_t rg = t.r0 + tile_row;
+    const int64_t nd = kDx ? p.K : p.N;
+    const bool vrow = rg < nd;
+    for (int c = c0; c < p.bn; c += step) {
+      uint32_t v[16];
+      tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(b * kBN + c), v);
+      tc::tmem_wait_ld();
+      // one output mode per launch: the branch stays outside the stores
+      const int nm = vrow ? static_cast<int>(min(static_cast<int64_t>(16), p.M - (t.m0 + c))) : 0;
+      float* of = reinterpret_cast<float*>(p.out) + (t.m0 + c) * nd + rg;
+      if (p.atomic_out) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < nm) atomicAdd(of + j * nd, __uint_as_float(v[j]));
+      } else if (!p.out_bf16 && !p.accumulate) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < nm) of[j * nd] = __uint_as_float(v[j]);
+      } else {
+        store_out16(p.out, (t.m0 + c) * nd + rg, nd, nm, make_uint4(v[0], v[1], v[2], v[3]),
+                    make_uint4(v[4], v[5], v[6], v[7]), make_uint4(v[8], v[9], v[10], v[11]),
+                    make_uint4(v[12], v[13], v[14], v[15]), p.out_bf16, p.accumulate);
+      }
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     // Like the MMA loop, the whole warp runs it on warp-uniform values and
     // one elected lane issues the copies: from a one-thread branch a stage's
     // expect_tx and two tensor copies took ~500 cycles, which paced the whole
-    // pipeline.
+    // pipeline. The ring runs on across units.
     const uint32_t tx = static_cast<uint32_t>(kActStageBytes + kCodesStageBytes);
-    const int32_t m_load = static_cast<int32_t>(m0) + static_cast<int32_t>(rank) * C::kBRows;
-    int issued = 0;
-    for (int i = 0; i < nst; ++i) {
-      // one vote, so that the lanes leave together
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int slot = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      // every lane waits (a wait in lane 0 alone, the others parked at the
-      // shuffle, was measured 4% slower on the prefill forward: the warp
-      // reconverged late after each stage), then lane 0's outcome decides
-      int r = tc::mbar_wait_abortable(empty_bar(slot), ph ^ 1, abort_flag);
-      r = __shfl_sync(0xffffffffu, r, 0);
-      if (r != tc::kWaitDone) {
-        if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleProducer);
-        break;
-      }
-      const int s = s_begin + i;
-      const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
-      const uint32_t cod = tc::smem_addr(smem + C::kOffCodes + slot * kCodesStageBytes);
-      if (tc::elect_one()) {
-        tc::mbar_arrive_expect_tx(full_bar(slot), tx);
-        tc::tma_load_2d(act, &tm_act, s * 64, m_load, full_bar(slot));
-        if (!kDx) {
-          // 128 rows x 32 (4-bit) or 64 (int8) bytes
-          tc::tma_load_2d(cod, &tm_codes, s * (kInt8 ? 64 : 32), static_cast<int32_t>(r0),
-                          full_bar(slot));
-        } else {
-          // 128 columns x 64 rows: 64 bytes with the 64-byte swizzle (4-bit,
-          // row r's 16-byte chunk c at r * 64 + 16 * (c ^ ((r >> 1) & 3))) or
-          // 128 bytes with the 128-byte swizzle (int8, chunk c at
-          // r * 128 + 16 * (c ^ (r & 7)))
-          tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(kInt8 ? r0 : r0 / 2), s * 64,
-                          full_bar(slot));
+    int gs = 0;                    // stages issued (across units)
+    bool stop = false;
+    for (int u = cid; u < p.units && !stop; u += ncl) {
+      const Unit t = unit_at(u);
+      const int32_t m_load = static_cast<int32_t>(t.m0) + static_cast<int32_t>(rank) * C::kBRows;
+      for (int i = 0; i < t.nst; ++i, ++gs) {
+        // one vote, so that the lanes leave together
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { stop = true; break; }
+        const int slot = gs % kStages;
+        const uint32_t ph = (gs / kStages) & 1;
+        // every lane waits (a wait in lane 0 alone, the others parked at the
+        // shuffle, was measured 4% slower on the prefill forward: the warp
+        // reconverged late after each stage), then lane 0's outcome decides
+        int r = tc::mbar_wait_abortable(empty_bar(slot), ph ^ 1, abort_flag);
+        r = __shfl_sync(0xffffffffu, r, 0);
+        if (r != tc::kWaitDone) {
+          if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleProducer);
+          stop = true;
+          break;
         }
+        const int s = t.s_begin + i;
+        const uint32_t act = tc::smem_addr(smem + C::kOffAct + slot * kActStageBytes);
+        const uint32_t cod = tc::smem_addr(smem + C::kOffCodes + slot * kCodesStageBytes);
+        if (tc::elect_one()) {
+          tc::mbar_arrive_expect_tx(full_bar(slot), tx);
+          tc::tma_load_2d(act, &tm_act, s * 64, m_load, full_bar(slot));
+          if (!kDx) {
+            // 128 rows x 32 (4-bit) or 64 (int8) bytes
+            tc::tma_load_2d(cod, &tm_codes, s * (kInt8 ? 64 : 32), static_cast<int32_t>(t.r0),
+                            full_bar(slot));
+          } else {
+            // 128 columns x 64 rows: 64 bytes with the 64-byte swizzle (4-bit,
+            // row r's 16-byte chunk c at r * 64 + 16 * (c ^ ((r >> 1) & 3))) or
+            // 128 bytes with the 128-byte swizzle (int8, chunk c at
+            // r * 128 + 16 * (c ^ (r & 7)))
+            tc::tma_load_2d(cod, &tm_codes, static_cast<int32_t>(kInt8 ? t.r0 : t.r0 / 2), s * 64,
+                            full_bar(slot));
+          }
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      ++issued;
     }
     if (*abort_flag && lane == 0) {  // let copies in flight land before the CTA exits
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        tc::mbar_wait(full_bar(i % kStages), (i / kStages) & 1);
+      for (int g = max(0, gs - kStages); g < gs; ++g)
+        tc::mbar_wait(full_bar(g % kStages), (g / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
@@ -414,13 +462,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     // lane issues, which lets the MMA operands stay uniform (a loop inside a
     // one-thread branch issued ~60% slower). The dequant warps arrive on
     // dq_bar only after they have seen the stage's copies land on full_bar,
-    // so its completion orders both the tensor-memory A operand and the
-    // shared-memory B tile before the MMAs; a failure elsewhere surfaces here
-    // through the abort flag. The wait is a spin on the non-blocking test: a
-    // suspending try_wait on the issuing warp lets the MMAs already queued
-    // drain (about 380 idle tensor cycles per wait, as measured). On a pair
-    // the peer's dequant warps arrive here too, once they have stored the
-    // stage and seen their own copies land.
+    // so its completion orders both the A operand and the shared-memory B
+    // tile before the MMAs; a failure elsewhere surfaces here through the
+    // abort flag. The waits spin on the non-blocking test: a suspending
+    // try_wait on the issuing warp lets the MMAs already queued drain (about
+    // 380 idle tensor cycles per wait, as measured).
     if (rank == 0) {
       const uint32_t idesc =
           tc::idesc_f16kind_f32(kTileRows * kCg, static_cast<uint32_t>(p.bn), kDx, kF16);
@@ -428,54 +474,70 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       // input gradient: A tile atoms (column half h, row group g) at
       // (2 g + h) KB, i.e. 1 KB apart along M and 2 KB along K
       const uint64_t adesc0 = tc::sw128_mnmajor_desc(tc::smem_addr(smem + C::kOffA), 1024, 2048);
-      for (int i = 0; i < nst; ++i) {
-        const int sl = i % kStages;
-        const int as = i % kASlots;
-        int r = tc::mbar_spin_abortable<kPair>(dq_bar(as), (i / kASlots) & 1, abort_flag,
-                                               p.mma_wait_limit);
+      int gs = 0, k = 0;
+      bool stop = false;
+      for (int u = cid; u < p.units && !stop; u += ncl, ++k) {
+        const Unit t = unit_at(u);
+        const int b = k % kAccBufs;
+        const uint32_t acc = tmem + static_cast<uint32_t>(b * kBN);
+        // the buffer's previous unit (k - kAccBufs) has been drained
+        int r = tc::mbar_spin_abortable<kPair>(acce_bar(b), ((k / kAccBufs) & 1) ^ 1, abort_flag,
+                                               1ll << 31);
         r = __shfl_sync(0xffffffffu, r, 0);
         if (r != tc::kWaitDone) {
           if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleMma);
           break;
         }
         tc::fence_after_sync();
-        const uint32_t a = tmem + kTmemA0 + 32u * sl;
-        // the descriptor's start-address field counts 16-byte units
-        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
-        const uint64_t adesc = adesc0 + static_cast<uint64_t>(as * (C::kAStageBytes >> 4));
-        if (tc::elect_one()) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if constexpr (kDx)   // K rows 16 j .. 16 j + 15: row groups 2 j, 2 j + 1
-              tc::mma_bf16_ss<kCg>(tmem, adesc + 256u * j, bdesc + 2u * j, idesc,
-                                   (i | j) != 0 ? 1u : 0u);
-            else
-              tc::mma_bf16_tmem_a<kCg>(tmem, a + 8u * j, bdesc + 2u * j, idesc,
-                                       (i | j) != 0 ? 1u : 0u);
+        for (int i = 0; i < t.nst; ++i, ++gs) {
+          const int sl = gs % kStages;
+          const int as = gs % kASlots;
+          r = tc::mbar_spin_abortable<kPair>(dq_bar(as), (gs / kASlots) & 1, abort_flag,
+                                             p.mma_wait_limit);
+          r = __shfl_sync(0xffffffffu, r, 0);
+          if (r != tc::kWaitDone) {
+            if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleMma);
+            stop = true;
+            break;
           }
-          tc::mma_commit<kCg>(empty_bar(sl));
-          if constexpr (kDx) tc::mma_commit<kCg>(afree_bar(as));
+          tc::fence_after_sync();
+          const uint32_t a = tmem + kTmemA0 + 32u * sl;
+          // the descriptor's start-address field counts 16-byte units
+          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(sl * (kActStageBytes >> 4));
+          const uint64_t adesc = adesc0 + static_cast<uint64_t>(as * (C::kAStageBytes >> 4));
+          if (tc::elect_one()) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if constexpr (kDx)   // K rows 16 j .. 16 j + 15: row groups 2 j, 2 j + 1
+                tc::mma_bf16_ss<kCg>(acc, adesc + 256u * j, bdesc + 2u * j, idesc,
+                                     (i | j) != 0 ? 1u : 0u);
+              else
+                tc::mma_bf16_tmem_a<kCg>(acc, a + 8u * j, bdesc + 2u * j, idesc,
+                                         (i | j) != 0 ? 1u : 0u);
+            }
+            tc::mma_commit<kCg>(empty_bar(sl));
+            if constexpr (kDx) tc::mma_commit<kCg>(afree_bar(as));
+          }
+          __syncwarp();
         }
+        if (stop) break;
+        if (tc::elect_one()) tc::mma_commit<kCg>(accf_bar(b));   // the unit's accumulator is done
         __syncwarp();
       }
-      if (tc::elect_one()) tc::mma_commit<kCg>(accum_bar);
+      if (tc::elect_one()) tc::mma_commit<kCg>(drain_bar);
       __syncwarp();
       // all MMAs done before teardown (a drain: full limit, no abort exit)
-      if (lane == 0 && !tc::mbar_wait(accum_bar, 0)) fail(kRoleMma);
+      if (lane == 0 && !tc::mbar_wait(drain_bar, 0)) fail(kRoleMma);
     }
-  } else {
-    // ---------------------------------------------------- dequant + store --
+  } else if (warp < C::kFirstEpiWarp) {
+    // ------------------------------------------------------------ dequant --
     // the stage's A slot is written: tell the pair's MMA thread
     auto arrive_dq = [&](int a) {
       if constexpr (kPair) tc::mbar_arrive_remote(tc::mapa(dq_bar(a), 0));
       else tc::mbar_arrive(dq_bar(a));
     };
-    const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int grp = (warp - 2) / C::kGroupWarps;   // takes the stages i % kGroups == grp
-    const int gw = (warp - 2) % C::kGroupWarps;    // warp within the group
-    constexpr int kHalves = 2 / C::kParts;          // 32-weight halves of a run per thread
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const uint8_t* tab = smem + C::kOffLut + 4 * (lane % C::kLutCopies);
+    const int grp = (warp - 2) >> 2;        // takes the stages gs % kGroups == grp
+    const uint8_t* tab = smem + C::kOffLut + 4 * lane;
     // block scale: 4-bit ahat = fl32(fl32(a8 s2) / 255); int8 absmax / 127
     auto block_scale = [&](uint32_t a8v, float sv) {
       return kInt8 ? __fdiv_rn(sv, 127.0f) : dequant_absmax(a8v, sv);
@@ -492,171 +554,170 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     // (no copy may still be landing in this CTA's shared memory when it
     // exits), after the first scale loads have gone out so that their latency
     // overlaps the copy's.
+    bool lut_ready = kInt8;
     auto wait_lut = [&] {
-      if constexpr (!kInt8) {
+      if (!lut_ready) {
         if (!tc::mbar_wait(lut_bar, 0)) fail(kRoleCompute);
+        lut_ready = true;
       }
     };
-    // tile row (forward: weight row; input gradient: weight column) held by
-    // this thread's accumulator lane
-    const int tile_row = 32 * q + lane;
-    if (!kDx) {
-      const int64_t n = r0 + tile_row;      // this thread's weight row
-      const bool vrow = n < p.N;
+    // input gradient: thread t of the group dequantizes weight row t % 64 of
+    // the stage over the tile's columns 64 (t / 64) .. + 63, one absmax
+    // block, as the forward walks a row. The 64 results are one 128-byte row
+    // of a 128-byte-swizzled MN-major atom of the A tile (64 weight columns
+    // along M x 8 weight rows along K per 1 KB atom; atom (column half h, row
+    // group g) at (2 g + h) KB).
+    const int t4 = ((warp - 2) & 3) * 32 + lane;
+    const int rr = t4 & 63, h = t4 >> 6;
+    const int ao = (2 * (rr >> 3) + h) * 1024 + (rr & 7) * 128;
+    const int asw = rr & 7;
+    int gs = 0, k = 0;
+    for (int u = cid; u < p.units; u += ncl, ++k) {
+      if (*abort_flag) break;
+      const Unit t = unit_at(u);
+      // this thread's block of stage i of the unit: forward (weight row n,
+      // block s_begin + i); input gradient (weight row (s_begin + i) 64 + rr,
+      // block r0 / 64 + h)
+      const int64_t n_fwd = t.r0 + tile_row;
+      const int64_t kb = (t.r0 >> 6) + h;
+      auto block_of = [&](int i, int64_t& bi) {
+        if constexpr (kDx) {
+          const int64_t n = static_cast<int64_t>(t.s_begin + i) * 64 + rr;
+          bi = n * p.nblk + kb;
+          return kb < p.nblk && n < p.N;
+        } else {
+          bi = n_fwd * p.nblk + t.s_begin + i;
+          return n_fwd < p.N;
+        }
+      };
       uint32_t a8v = 0;
       float sv = 0.0f;
+      bool ok = false;
       auto load_scale = [&](int i) {
-        if (vrow && i < nst) load_block(n * p.nblk + s_begin + i, a8v, sv);
+        if (i >= t.nst) return;
+        int64_t bi;
+        ok = block_of(i, bi);
+        if (ok) load_block(bi, a8v, sv);
       };
-      load_scale(grp);
+      int i = ((grp - gs % kGroups) + kGroups) % kGroups;   // this group's first stage of the unit
+      load_scale(i);
       wait_lut();
-      for (int i = grp; i < nst; i += kGroups) {
-        const int slot = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        const float ahat = vrow ? block_scale(a8v, sv) : 0.0f;
+      for (; i < t.nst; i += kGroups) {
+        const int g = gs + i;                 // the stage's index across units
+        const int slot = g % kStages;
+        const uint32_t ph = (g / kStages) & 1;
+        const float ahat = ok ? block_scale(a8v, sv) : 0.0f;
         const float2 ahat2 = make_float2(ahat, ahat);
         load_scale(i + kGroups);
-        // warp-uniform: the stage is done by all lanes or by none (the
-        // arrival below follows a __syncwarp)
-        bool go = !*abort_flag && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag),
-                                         kRoleCompute);
-        if (!__all_sync(0xffffffffu, go)) continue;
-        const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
-        const uint32_t dst = tmem + lane_base + kTmemA0 + 32u * slot;
-        // this thread's 32-weight halves of the row's 64: hf = half0 ..
-        const int half0 = (gw >> 2) * kHalves;
+        if constexpr (!kDx) {
+          // warp-uniform: the stage is done by all lanes or by none (the
+          // arrival below follows a __syncwarp)
+          const bool go = !*abort_flag &&
+                          waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag),
+                                 kRoleCompute);
+          if (!__all_sync(0xffffffffu, go)) continue;
+          const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
+          const uint32_t dst = tmem + lane_base + kTmemA0 + 32u * slot;
 #pragma unroll
-        for (int k = 0; k < kHalves; ++k) {
-          const int hf = half0 + k;
-          uint32_t v[16];
-          if constexpr (kInt8) {
-            // row tile_row's 64 bytes, 64-byte swizzle
-            const int sw = (tile_row >> 1) & 3;
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[16];
+            if constexpr (kInt8) {
+              // row tile_row's 64 bytes, 64-byte swizzle
+              const int sw = (tile_row >> 1) & 3;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int c = 2 * hf + cc;
-              const uint4 w = *reinterpret_cast<const uint4*>(cst + tile_row * 64 + 16 * (c ^ sw));
-              dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
+              for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * hf + cc;
+                const uint4 w =
+                    *reinterpret_cast<const uint4*>(cst + tile_row * 64 + 16 * (c ^ sw));
+                dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
+              }
+            } else {
+              dequant16_4bit<kF16>(
+                  *reinterpret_cast<const uint4*>(cst + tile_row * 32 + 16 * hf), tab, ahat2, v);
             }
-          } else {
-            const uint8_t* crow = cst + tile_row * 32;
-            dequant16_4bit<kF16, C::kLutShift>(*reinterpret_cast<const uint4*>(crow + 16 * hf), tab, ahat2, v);
+            tc::tmem_st16(dst + 16u * hf, v);
           }
-          tc::tmem_st16(dst + 16u * hf, v);
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) arrive_dq(slot);
+        } else {
+          // First the A slot: its previous tile (stage g - kASlots) has been
+          // read by its MMAs. Only then the stage's copies: once MMA(g -
+          // kASlots) is done, so is MMA(g - kStages), whose dequant saw the
+          // copy slot's previous phase complete, so this parity wait cannot
+          // pass a phase early (the copy slots are shared between groups, and
+          // a parity wait cannot tell a phase still pending from the one
+          // before it).
+          const int as = g % kASlots;
+          bool go = !*abort_flag;
+          if (go && g >= kASlots)
+            go = waited(tc::mbar_wait_abortable(afree_bar(as), ((g / kASlots) - 1) & 1, abort_flag),
+                        kRoleCompute);
+          go = go && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag), kRoleCompute);
+          if (!__all_sync(0xffffffffu, go)) continue;
+          const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
+          uint8_t* arow = smem + C::kOffA + as * C::kAStageBytes + ao;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {        // columns 32 hf .. + 31 of the run
+            uint32_t v[16];
+            if constexpr (kInt8) {
+              // row rr's chunks 4 h + 2 hf, + 1 of 128 bytes, 128-byte swizzle
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const uint4 w = *reinterpret_cast<const uint4*>(
+                    cst + rr * 128 + 16 * ((4 * h + 2 * hf + cc) ^ (rr & 7)));
+                dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
+              }
+            } else {
+              // row rr's chunk 2 h + hf of 64 bytes, 64-byte swizzle
+              const int csw = (rr >> 1) & 3;
+              dequant16_4bit<kF16>(
+                  *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw)), tab,
+                  ahat2, v);
+            }
+            // columns 32 hf + 8 j .. + 7 form chunk 4 hf + j of the atom row
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(arow + 16 * ((4 * hf + j) ^ asw)) =
+                  make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+          tc::fence_proxy_async();   // the MMA reads the tile through the async proxy
+          __syncwarp();
+          if (lane == 0) arrive_dq(as);
         }
-        tc::tmem_wait_st();
+      }
+      gs += t.nst;
+      if constexpr (kAccBufs == 1) {
+        // The only accumulator buffer: these warps drain it (the four warps
+        // of each lane quarter share out its 16-column chunks) before they go
+        // on to the next unit, whose copies are already under way.
+        if (*abort_flag) break;
+        if (!waited(tc::mbar_wait_abortable(accf_bar(0), k & 1, abort_flag), kRoleEpilogue)) break;
+        tc::fence_after_sync();
+        drain(t, 0, 16 * ((warp - 2) >> 2), 64);
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) arrive_dq(slot);
-      }
-    } else {
-      // Thread t of the group dequantizes weight row t % 64 of the stage over
-      // kPartCols of the tile's columns 64 h .. 64 h + 63, one absmax block,
-      // as the forward walks a row. A run of 64 results is one 128-byte row of
-      // a 128-byte-swizzled MN-major atom of the A tile (64 weight columns
-      // along M x 8 weight rows along K per 1 KB atom; atom (column half h,
-      // row group g) at (2 g + h) KB).
-      const int t = gw * 32 + lane;
-      const int rr = t & 63, part = t >> 6;
-      const int h = part / C::kParts;                 // 64-column block of the tile
-      const int half0 = (part % C::kParts) * kHalves; // first 32-column half of the run
-      const int64_t kb = (r0 >> 6) + h;
-      const bool kb_ok = kb < p.nblk;
-      const int ao = (2 * (rr >> 3) + h) * 1024 + (rr & 7) * 128;
-      const int asw = rr & 7;
-      uint32_t a8v = 0;
-      float sv = 0.0f;
-      bool rok = false;
-      auto load_scale = [&](int i) {
-        if (i >= nst) return;
-        const int64_t n = static_cast<int64_t>(s_begin + i) * 64 + rr;
-        rok = kb_ok && n < p.N;
-        if (rok) load_block(n * p.nblk + kb, a8v, sv);
-      };
-      load_scale(grp);
-      wait_lut();
-      for (int i = grp; i < nst; i += kGroups) {
-        const int slot = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        const float ahat = rok ? block_scale(a8v, sv) : 0.0f;
-        const float2 ahat2 = make_float2(ahat, ahat);
-        load_scale(i + kGroups);
-        // First the A slot: its previous tile (stage i - kASlots) has been read
-        // by its MMAs. Only then the stage's copies: once MMA(i - kASlots) is
-        // done, so is MMA(i - kStages), whose dequant saw the copy slot's
-        // previous phase complete, so this parity wait cannot pass a phase
-        // early (several groups share a copy slot when kStages is not a
-        // multiple of kGroups, and a parity wait cannot tell a phase still
-        // pending from the one before it).
-        const int as = i % kASlots;
-        bool go = !*abort_flag;
-        if (go && i >= kASlots)
-          go = waited(tc::mbar_wait_abortable(afree_bar(as), ((i / kASlots) - 1) & 1, abort_flag),
-                      kRoleCompute);
-        go = go && waited(tc::mbar_wait_abortable(full_bar(slot), ph, abort_flag), kRoleCompute);
-        if (!__all_sync(0xffffffffu, go)) continue;
-        const uint8_t* cst = smem + C::kOffCodes + slot * kCodesStageBytes;
-        uint8_t* arow = smem + C::kOffA + as * C::kAStageBytes + ao;
-#pragma unroll
-        for (int k = 0; k < kHalves; ++k) {
-          const int hf = half0 + k;                   // columns 32 hf .. + 31 of the run
-          uint32_t v[16];
-          if constexpr (kInt8) {
-            // row rr's chunks 4 h + 2 hf, + 1 of 128 bytes, 128-byte swizzle
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const uint4 w = *reinterpret_cast<const uint4*>(
-                  cst + rr * 128 + 16 * ((4 * h + 2 * hf + cc) ^ (rr & 7)));
-              dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
-            }
-          } else {
-            // row rr's chunk 2 h + hf of 64 bytes, 64-byte swizzle
-            const int csw = (rr >> 1) & 3;
-            dequant16_4bit<kF16, C::kLutShift>(
-                *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw)), tab,
-                ahat2, v);
-          }
-          // columns 32 hf + 8 j .. + 7 form chunk 4 hf + j of the atom row
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(arow + 16 * ((4 * hf + j) ^ asw)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
-        tc::fence_proxy_async();   // the MMA reads the tile through the async proxy
-        __syncwarp();
-        if (lane == 0) arrive_dq(as);
+        if (lane == 0) arrive_acce(0);
       }
     }
-
-    // epilogue: accumulator lanes are tile rows, columns are tokens
-    if (!*abort_flag) waited(tc::mbar_wait_abortable(accum_bar, 0, abort_flag), kRoleEpilogue);
-    tc::fence_after_sync();
-    if (!*abort_flag) {
-      const int64_t rg = r0 + tile_row;
-      const int64_t nd = kDx ? p.K : p.N;
-      const bool vrow = rg < nd;
-      // the four warps of each lane quarter share out the 16-column chunks
-      for (int c = 16 * ((warp - 2) >> 2); c < p.bn; c += 64) {
-        uint32_t v[16];
-        tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
-        tc::tmem_wait_ld();
-        // one output mode per launch: the branch stays outside the stores
-        const int nm = vrow ? static_cast<int>(min(static_cast<int64_t>(16), p.M - (m0 + c))) : 0;
-        float* of = reinterpret_cast<float*>(p.out) + (m0 + c) * nd + rg;
-        if (p.atomic_out) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (j < nm) atomicAdd(of + j * nd, __uint_as_float(v[j]));
-        } else if (!p.out_bf16 && !p.accumulate) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (j < nm) of[j * nd] = __uint_as_float(v[j]);
-        } else {
-          store_out16(p.out, (m0 + c) * nd + rg, nd, nm, make_uint4(v[0], v[1], v[2], v[3]),
-                      make_uint4(v[4], v[5], v[6], v[7]), make_uint4(v[8], v[9], v[10], v[11]),
-                      make_uint4(v[12], v[13], v[14], v[15]), p.out_bf16, p.accumulate);
-        }
-      }
+    wait_lut();   // a CTA with no unit still lets the table copy land
+  } else if constexpr (kAccBufs == 2) {
+    // ----------------------------------------------------------- epilogue --
+    // Unit k's accumulator (buffer k % 2) goes out while the MMAs of unit
+    // k + 1 fill the other buffer.
+    int k = 0;
+    for (int u = cid; u < p.units; u += ncl, ++k) {
+      const Unit t = unit_at(u);
+      const int b = k & 1;
+      if (*abort_flag) break;
+      if (!waited(tc::mbar_wait_abortable(accf_bar(b), (k >> 1) & 1, abort_flag), kRoleEpilogue))
+        break;
+      tc::fence_after_sync();
+      drain(t, b, 0, 16);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_acce(b);
     }
   }
 
@@ -691,13 +752,12 @@ cudaError_t launch_tc(const MatmulCall& c) {
   a.mma_wait_limit = c.wait_limit;
   const int64_t nd = kDx ? K : N;            // tile-row dimension
   const int64_t red = kDx ? N : K;           // reduction dimension
-  // a pair's two CTAs take consecutive 128-row tiles
-  const int64_t tile_rows = kTileRows * C::kCg;
-  const int64_t row_tiles = (nd + tile_rows - 1) / tile_rows * C::kCg;
+  // a unit covers 128 rows per CTA of a pair
+  const int64_t row_units = (nd + kTileRows * C::kCg - 1) / (kTileRows * C::kCg);
   const int64_t m_tiles = (M + a.bn - 1) / a.bn;
   a.stages_total = static_cast<int>((red + 63) / 64);
   int splits = 1;
-  const int64_t ctas = row_tiles * m_tiles;
+  const int64_t ctas = row_units * C::kCg * m_tiles;
   if (ctas < c.num_sms && !c.out_bf16) {   // each split fills the ring at least once
     splits = static_cast<int>(std::max<int64_t>(
         1, std::min<int64_t>(c.num_sms / ctas, a.stages_total / C::kStages)));
@@ -705,6 +765,12 @@ cudaError_t launch_tc(const MatmulCall& c) {
   a.stages_per_split = (a.stages_total + splits - 1) / splits;
   splits = (a.stages_total + a.stages_per_split - 1) / a.stages_per_split;
   a.atomic_out = splits > 1 ? 1 : 0;
+  a.row_units = static_cast<int>(row_units);
+  a.m_tiles = static_cast<int>(m_tiles);
+  const int64_t units = row_units * m_tiles * splits;
+  a.units = static_cast<int>(units);
+  // persistent: at most one CTA (or pair) per SM, each taking units in turn
+  const int64_t groups = std::min<int64_t>(units, std::max(1, c.num_sms / C::kCg));
 
   CUtensorMap tm_act, tm_codes;
   // activations: [M, red] 16-bit, box 64 (reduction) x the tokens one CTA
@@ -736,8 +802,7 @@ cudaError_t launch_tc(const MatmulCall& c) {
     cudaError_t e = cudaMemsetAsync(c.out, 0, static_cast<size_t>(M) * nd * sizeof(float), c.st);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>(m_tiles),
-            static_cast<unsigned>(splits));
+  const dim3 grid(static_cast<unsigned>(groups * C::kCg));
   if constexpr (C::kPair) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

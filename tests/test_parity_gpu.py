@@ -376,3 +376,29 @@ def test_dx_small_shapes(rows, cols, M):
     _, dX = run_dx(W, dY)
     Wh = o.dequantize(*o.quantize(W), rows, cols)
     assert_tol(dX, o.matmul_bwd_dx(dY.float().numpy(), Wh), f"dX {rows}x{cols} M={M}")
+
+
+@pytest.mark.parametrize("M", [50, 100, 300])
+def test_persistent_units_with_ragged_tails(M):
+    """Many more tile units than SMs (each CTA or pair walks several, its
+    copy ring and accumulator buffers running on across them), with a ragged
+    last row tile and a ragged last token tile, through the 64-, 128- and
+    256-token tiles; compared in full with the oracle, both directions and
+    both output types."""
+    rows, cols = 38920, 192            # 304 row tiles of 128, the last one ragged
+    W = weight_np(rows, cols, 41)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    Wh = o.dequantize(*o.quantize(W), rows, cols)
+    X = wl.activations(M, cols, seed=M + 42)
+    Y = nf4.nf4_matmul_fwd(X.to(DEV), q)
+    Y_ref = o.matmul_fwd(X.float().numpy(), Wh)
+    assert_tol(Y.cpu().numpy(), Y_ref, f"persistent fwd M={M}")
+    Yb = nf4.nf4_matmul_fwd(X.to(DEV), q, out_dtype=torch.bfloat16)
+    assert torch.equal(Yb, Y.to(torch.bfloat16))     # no split: the same sums, rounded
+    Wd = weight_np(192, 38912, 43)    # 304 column tiles, a short reduction
+    qd = nf4.nf4_quantize(torch.from_numpy(Wd).to(DEV))
+    dY = wl.activations(M, 192, std=0.01, seed=M + 44)
+    dX = nf4.nf4_matmul_bwd_dx(dY.to(DEV), qd).cpu().numpy()
+    dX_ref = o.matmul_bwd_dx(dY.float().numpy(), o.dequantize(*o.quantize(Wd), 192, 38912))
+    assert_tol(dX, dX_ref, f"persistent dX M={M}")
+    assert nf4.nf4_poll_device_status() == 0
