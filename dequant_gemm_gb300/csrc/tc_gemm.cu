@@ -395,6 +395,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           if (j < nm) of[j * nd] = __uint_as_float(v[j]);
+      } else if (!p.accumulate) {
+        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) + (t.m0 + c) * nd + rg;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < nm) ob[j * nd] = __float2bfloat16_rn(__uint_as_float(v[j]));
       } else {
         store_out16(p.out, (t.m0 + c) * nd + rg, nd, nm, make_uint4(v[0], v[1], v[2], v[3]),
                     make_uint4(v[4], v[5], v[6], v[7]), make_uint4(v[8], v[9], v[10], v[11]),
