@@ -139,9 +139,24 @@ __device__ inline void report_status(int* status, int code, uint32_t kernel, uin
 constexpr uint32_t kSiteGemv = 1, kSiteTcFwd = 2, kSiteTcDx = 3;
 constexpr uint32_t kRoleProducer = 1, kRoleMma = 2, kRoleCompute = 3, kRoleEpilogue = 4;
 
+// x / D rounded to nearest for the constant divisors D = 255 and 127:
+// q = RN(x r) with r = RN(1/D) is within one ulp of x / D, the remainder
+// x - q D is exact in one FMA, and RN(q + rem r) is then the correctly
+// rounded quotient (Markstein's theorem on division by reciprocal and
+// remainder correction). For D = 255 and D = 127 this was also checked
+// against the exact quotient for every positive fp32 x, subnormals
+// included; the sign is symmetric. Three instructions, no division.
+template <int D>
+__device__ __forceinline__ float div_by_const(float x) {
+  constexpr float r = 1.0f / static_cast<float>(D);
+  const float q = __fmul_rn(x, r);
+  const float rem = __fmaf_rn(-q, static_cast<float>(D), x);
+  return __fmaf_rn(rem, r, q);
+}
+
 // Second-level dequant: ahat = fl32(fl32(a8 * s2) / 255), both IEEE RN.
 __device__ __forceinline__ float dequant_absmax(uint32_t a8, float s2) {
-  return __fdiv_rn(__fmul_rn(static_cast<float>(a8), s2), 255.0f);
+  return div_by_const<255>(__fmul_rn(static_cast<float>(a8), s2));
 }
 
 // Element types of activations and outputs (the nf4_elem values of the C ABI).

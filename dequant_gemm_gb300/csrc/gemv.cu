@@ -35,7 +35,11 @@
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
 //    that every lookup of a warp hits 32 distinct banks. Each CTA lays the
-//    copies out itself, by shuffles from levels held in registers. Int8
+//    copies out itself, by shuffles from levels held in registers. With one
+//    n-tile (up to 8 tokens) the table rows are 256 bytes apart, so that a
+//    single byte permute of the code word and the lane number gives the
+//    address of a lookup (a permute and a load per two weights); that CTA
+//    takes an SM of its own and may use up to 128 registers a thread. Int8
 //    weights need no table: two bytes become an f16x2 of 1024 + (q + 128)
 //    by one byte permute with the fp16 exponent of 1024, less 1152, which is
 //    q exactly; the block scale absmax / 127 is applied after the MMA like
@@ -43,6 +47,8 @@
 //  * Within a block the 4 threads of an MMA quad each own 16 contiguous k
 //    (8 code bytes); the reduction order over k is permuted consistently in A
 //    and B, which leaves the sum unchanged.
+//  * The activation slice is staged by all 16 warps at once (one global round
+//    trip), then scaled to fp16 in place after a block-wide max.
 //  * Launched with programmatic stream serialization: the CTAs of the next
 //    kernel in the stream can be resident and do their set-up while this one
 //    drains. Before griddepcontrol.wait a CTA only prefetches its code boxes
@@ -178,19 +184,34 @@ __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
   return (nblk * s) / slices;
 }
 
-// Shared memory (offsets from a 1024-byte aligned base): level table, code
-// slots (per warp, 1024-byte aligned for the swizzle; after the main loop a
+// Shared memory. The level table comes in two layouts. Narrow (one n-tile
+// of 16 tokens, or int8 without a table): rows of 128 bytes, one 4-byte copy
+// per lane, at the start of the 1024-byte aligned region. Wide (4-bit
+// formats with one n-tile of 8 tokens, the decode case): rows of 256 bytes
+// at the very start of the dynamic window, before the aligned region, so
+// that the address of a lookup, (code byte) * 256 + lane * 4, is what one
+// byte permute returns and the window offset folds into the load; the upper
+// 128 bytes of each row stay unused. Then, from the aligned base: code slots
+// (per warp, 1024-byte aligned for the swizzle; after the main loop a
 // second-K-half warp's first slot carries its sums to the first K-half),
-// mbarriers, token scales, the cluster reduction inbox and the fp16
-// activation slice (rows of max_nb * 128 + 8 bytes: the 8 keeps the B
-// fragment loads of 8 token rows on distinct banks).
-constexpr int kOffSlots = kTabBytes;
-constexpr int kOffBars = kOffSlots + kGemvWarps * kWarpSlots * kBoxBytes;
-constexpr int kOffXinv = kOffBars + kGemvWarps * kWarpSlots * 8;
-constexpr int kOffInbox = kOffXinv + 16 * 4;
-__host__ __device__ constexpr int gemv_off_inbox(int) { return kOffInbox; }
-__host__ __device__ constexpr int gemv_off_xs(int nt) { return gemv_off_inbox(nt) + 8 * nt * kGemvRows * 4; }
+// mbarriers, token scales, per-warp max |x|, the cluster reduction inbox and
+// the fp16 activation slice (rows of max_nb * 128 + 8 bytes: the 8 keeps the
+// B fragment loads of 8 token rows on distinct banks).
+constexpr int kWideTabBytes = 256 * 256;
+__host__ __device__ constexpr int gemv_lead(bool wide) { return wide ? kWideTabBytes : 0; }
+__host__ __device__ constexpr int gemv_off_slots(bool wide) { return wide ? 0 : kTabBytes; }
+__host__ __device__ constexpr int gemv_off_bars(bool wide) {
+  return gemv_off_slots(wide) + kGemvWarps * kWarpSlots * kBoxBytes;
+}
+__host__ __device__ constexpr int gemv_off_xinv(bool wide) { return gemv_off_bars(wide) + kGemvWarps * kWarpSlots * 8; }
+__host__ __device__ constexpr int gemv_off_wmax(bool wide) { return gemv_off_xinv(wide) + 16 * 4; }
+__host__ __device__ constexpr int gemv_off_inbox(bool wide) { return gemv_off_wmax(wide) + kGemvWarps * 4; }
+__host__ __device__ constexpr int gemv_off_xs(int nt, bool wide) {
+  return gemv_off_inbox(wide) + 8 * nt * kGemvRows * 4;
+}
 __host__ __device__ constexpr int gemv_xstride(int max_nb) { return max_nb * 128 + 8; }
+// The wide table serves one n-tile of a 4-bit format.
+__host__ __device__ constexpr bool gemv_wide(int nt, int fmt) { return nt == 1 && fmt != kFmtInt8; }
 
 // Per-format constants of the small-M forward: 64-weight blocks per 128-byte
 // code box row (four of 32 bytes, or two of 64 for int8).
@@ -202,18 +223,20 @@ struct GemvFmt {
 };
 
 template <int NT, int kFmt, bool kF16>
-__global__ void __launch_bounds__(kGemvThreads, 2)
+__global__ void __launch_bounds__(kGemvThreads, gemv_wide(NT, kFmt) ? 1 : 2)
 gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) {
   constexpr bool kInt8 = GemvFmt<kFmt>::kInt8;
   constexpr int kBoxBlocks = GemvFmt<kFmt>::kBoxBlocks;
   constexpr int kBlockBytes = GemvFmt<kFmt>::kBlockBytes;
-  extern __shared__ uint8_t smem_raw[];
+  constexpr bool kWide = gemv_wide(NT, kFmt);
+  extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
-  float* xinv = reinterpret_cast<float*>(smem + kOffXinv);    // [16]
-  float* inbox = reinterpret_cast<float*>(smem + gemv_off_inbox(NT));
-  uint8_t* xs = smem + gemv_off_xs(NT);
+      (reinterpret_cast<uintptr_t>(smem_raw + gemv_lead(kWide)) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint32_t* tab = reinterpret_cast<uint32_t*>(kWide ? smem_raw : smem);
+  float* xinv = reinterpret_cast<float*>(smem + gemv_off_xinv(kWide));    // [16]
+  float* wmax = reinterpret_cast<float*>(smem + gemv_off_wmax(kWide));    // [kGemvWarps]
+  float* inbox = reinterpret_cast<float*>(smem + gemv_off_inbox(kWide));
+  uint8_t* xs = smem + gemv_off_xs(NT, kWide);
   const int xstride = gemv_xstride(p.max_nb);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -221,7 +244,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   const int rgp = warp & (kRowGroups - 1), kh = warp / kRowGroups;
   // K-half hand-off of row group rgp: the first slot of warp rgp + 8, free
   // once that warp has consumed its last box
-  float* red = reinterpret_cast<float*>(smem + kOffSlots + (rgp + kRowGroups) * kWarpSlots * kBoxBytes);
+  float* red = reinterpret_cast<float*>(smem + gemv_off_slots(kWide) +
+                                       (rgp + kRowGroups) * kWarpSlots * kBoxBytes);
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kGemvRows;
   const int slice = blockIdx.y;
   const int kb0 = slice_begin(p.nblk, p.slices, slice);
@@ -230,8 +254,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
   const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
   // this warp's code slots and their mbarriers; it takes boxes kh, kh + 2, ...
-  const uint32_t slots = tc::smem_addr(smem + kOffSlots) + warp * kWarpSlots * kBoxBytes;
-  const uint32_t bars = tc::smem_addr(smem + kOffBars) + warp * kWarpSlots * 8;
+  const uint32_t slots = tc::smem_addr(smem + gemv_off_slots(kWide)) + warp * kWarpSlots * kBoxBytes;
+  const uint32_t bars = tc::smem_addr(smem + gemv_off_bars(kWide)) + warp * kWarpSlots * 8;
 
   // Programmatic dependent launch: the next kernel in the stream may start its
   // own set-up now; this one reads no global memory before the previous
@@ -242,7 +266,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   // the point of coherence, so the loads after griddepcontrol.wait still see
   // everything the previous kernel wrote.
   {
-    // Only for short slices (at most the two boxes a warp keeps in flight),
+    // Only for short slices (at most the boxes a warp keeps in flight),
     // where the launch is latency-bound: on long slices the prefetch competes
     // with demand loads and was measured slower (35 MB weights, 4% slower
     // even with the first four boxes only).
@@ -264,14 +288,15 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       }
     }
   }
-  // level table: entry e, copy l at word 32 e + l (one conflict-free store per
-  // entry and warp); lane l holds level l & 15, entries come by shuffles
+  // level table: entry e, copy l at word (32 or 64) e + l (one
+  // conflict-free store per entry and warp); lane l holds level l & 15,
+  // entries come by shuffles
   if constexpr (!kInt8) {
     const uint32_t lev = level_f16<kFmt, 0, 16>(lane & 15);
     for (int e = warp; e < 256; e += kGemvWarps) {
       const uint32_t hi = __shfl_sync(0xffffffffu, lev, e >> 4);
       const uint32_t lo = __shfl_sync(0xffffffffu, lev, e & 15);
-      tab[e * 32 + lane] = hi | (lo << 16);
+      tab[e * (kWide ? 64 : 32) + lane] = hi | (lo << 16);
     }
   }
   if (lane == 0) {
@@ -287,9 +312,11 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   if (p.slices > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // Activations first, ahead of the code stream: warp w copies token w of
-  // the tile, as bf16, into its staging row and takes its max |x| on the way
-  // (one global round trip); the conversion to fp16 happens in place below.
+  // Activations first, ahead of the code stream: every warp takes part.
+  // Token xm = warp % mt of the tile is copied, as bf16, into its staging row
+  // by the xparts = 16 / mt warps with that token, interleaved by 32 lanes,
+  // each taking its max |x| on the way (one global round trip for short
+  // slices); the conversion to fp16 happens in place below.
   auto to_f2 = [](uint32_t w) {
     if constexpr (kF16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
     else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
@@ -299,20 +326,22 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     return fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
   };
   const int nkv4 = nb * (kBlock / 4);      // uint2 (4 bf16) per token row
-  uint2* xo = reinterpret_cast<uint2*>(xs + warp * xstride);
+  const int xparts = kGemvWarps / mt, xm = warp % mt, xp = warp / mt;
+  const bool xw = xp < xparts;             // warps past xparts * mt stage nothing
+  uint2* xo = reinterpret_cast<uint2*>(xs + xm * xstride);
   float xmax = 0.0f;
-  if (warp < mt) {
-    const uint2* xrow = reinterpret_cast<const uint2*>(p.X + (m0 + warp) * p.K +
+  if (xw) {
+    const uint2* xrow = reinterpret_cast<const uint2*>(p.X + (m0 + xm) * p.K +
                                                        static_cast<int64_t>(kb0) * kBlock);
-#pragma unroll 8
-    for (int i = lane; i < nkv4; i += 32) {
+#pragma unroll 4
+    for (int i = xp * 32 + lane; i < nkv4; i += xparts * 32) {
       const uint2 v = __ldg(xrow + i);
       xo[i] = v;
       xmax = fmaxf(xmax, amax4(v));
     }
   }
 
-  // Box i of this warp (the slice's box kh + 2 i) goes into slot i % 2, by
+  // Box i of this warp (the slice's box kh + 2 i) goes into slot i % kWarpSlots, by
   // TMA; its absmax codes and scales travel alongside: lane e loads those of
   // row pair (e & 7, (e & 7) + 8) of block e >> 3 of the box.
   const int nmine = (nboxes - kh + 1) / 2;   // boxes of this warp
@@ -349,22 +378,27 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   float sa0, sb0, sa1, sb1;
   load_scales(0, qa0, qb0, sa0, sb0);
   load_scales(1, qa1, qb1, sa1, sb1);
-  if (nmine > 0) issue_box(0);
-  if (nmine > 1) issue_box(1);
+  for (int i = 0; i < kWarpSlots && i < nmine; ++i) issue_box(i);
 
   // max |x| over the slice -> power-of-two scale into [2^14, 2^15) -> fp16
   // (bit-preserving down to fp16's normal range, see the file comment)
-  if (warp < mt) {
+  if (xw) {
     float mx = xmax;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) wmax[warp] = mx;
+  }
+  __syncthreads();
+  if (xw) {
+    float mx = 0.0f;
+    for (int q = 0; q < xparts; ++q) mx = fmaxf(mx, wmax[xm + q * mt]);
     int e = 0;
     if (mx > 0.0f) {
       const int E = max(1, static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu));
       e = min(141 - E, 126);
     }
     const float scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-    if (lane == 0) xinv[warp] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    if (xp == 0 && lane == 0) xinv[xm] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
     auto convert = [&](uint2 v) {
       const float2 f0 = to_f2(v.x), f1 = to_f2(v.y);
       const __half2 h0 = __floats2half2_rn(f0.x * scale, f0.y * scale);
@@ -372,7 +406,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
       return make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
                         *reinterpret_cast<const uint32_t*>(&h1));
     };
-    for (int i = lane; i < nkv4; i += 32) xo[i] = convert(xo[i]);   // each lane its own entries
+    for (int i = xp * 32 + lane; i < nkv4; i += xparts * 32) xo[i] = convert(xo[i]);   // own entries
   }
   __syncthreads();
 
@@ -383,16 +417,23 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-  const uint8_t* tabl = smem + lane * 4;                 // this lane's table copy
+  const uint8_t* tabl = smem + lane * 4;                 // this lane's narrow table copy
+  const uint32_t lane_sel = static_cast<uint32_t>(lane) * 4u;   // byte 0: lane * 4, rest 0
   const uint8_t* xsl = xs + g * xstride + t * 32;        // token g, this lane's 16 k
   bool tok_ok[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < mt;
   auto lut = [&](uint32_t w, int b) {
-    return *reinterpret_cast<const uint32_t*>(tabl + (__byte_perm(w, 0u, 0x4440u + b) << 7));
+    if constexpr (kWide) {
+      // bytes (lane * 4, code byte b, 0, 0): the entry's offset in the window
+      const uint32_t off = __byte_perm(w, lane_sel, 0x7604u + (static_cast<uint32_t>(b) << 4));
+      return *reinterpret_cast<const uint32_t*>(smem_raw + off);
+    } else {
+      return *reinterpret_cast<const uint32_t*>(tabl + (__byte_perm(w, 0u, 0x4440u + b) << 7));
+    }
   };
   // rows g and g + 8 of the box; 16-byte chunk c of row r sits at c ^ (r & 7)
-  const uint8_t* slot_g = smem + kOffSlots + warp * kWarpSlots * kBoxBytes + g * 128 +
+  const uint8_t* slot_g = smem + gemv_off_slots(kWide) + warp * kWarpSlots * kBoxBytes + g * 128 +
                           (kInt8 ? 0 : (t & 1) * 8);
   bool ok = true;
   int waited = 0;
@@ -402,8 +443,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     const int sl = i % kWarpSlots;
     float aha, ahb;
     if constexpr (kInt8) {   // scale of the raw integer sums
-      aha = __fdiv_rn(sa, 127.0f);
-      ahb = __fdiv_rn(sb, 127.0f);
+      aha = div_by_const<127>(sa);
+      ahb = div_by_const<127>(sb);
     } else {
       aha = dequant_absmax(qa, sa);
       ahb = dequant_absmax(qb, sb);
@@ -534,7 +575,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   }
   if (p.slices == 1) {
     // stage [8 NT tokens x 128 rows] over the level table, then float4 stores
-    float* out_s = reinterpret_cast<float*>(smem);
+    float* out_s = reinterpret_cast<float*>(tab);
     if (kh == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -592,8 +633,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
 }  // namespace
 
 // Dynamic shared memory of one GEMV CTA (plus 1 KB to align the base).
-constexpr size_t gemv_smem_bytes(int nt, int max_nb, int xrows) {
-  return static_cast<size_t>(gemv_off_xs(nt)) +
+constexpr size_t gemv_smem_bytes(int nt, int max_nb, int xrows, bool wide) {
+  return static_cast<size_t>(gemv_lead(wide)) + static_cast<size_t>(gemv_off_xs(nt, wide)) +
          static_cast<size_t>(xrows) * gemv_xstride(max_nb) + 1024;
 }
 constexpr size_t kGemvSmemTwoPerSm = 112 * 1024;   // two CTAs per SM
@@ -639,7 +680,7 @@ cudaError_t launch_gemv_fwd(const MatmulCall& c) {
   // measured faster than filling every SM with smaller ones), else the most
   // busy SMs; then two n-tiles over one.
   const int64_t row_ctas = (N + kGemvRows - 1) / kGemvRows;
-  const int nt_max = M <= 8 ? 1 : 2;
+  const int fmt = c.fmt;
   struct Shape { int s, nt; int64_t ctas, waves, busy; size_t smem; };
   Shape best{0, 0, 0, 0, 0, 0};
   const int64_t enough = (7 * static_cast<int64_t>(num_sms)) / 10;
@@ -651,24 +692,31 @@ cudaError_t launch_gemv_fwd(const MatmulCall& c) {
     if (!ce && c.busy != best.busy) return c.busy > best.busy;
     return c.nt > best.nt;
   };
-  for (int sl = kMaxCluster; sl >= 1; sl /= 2) {
-    if (sl > a.nblk) continue;
-    const int nb = (a.nblk + sl - 1) / sl;
-    if (nb > kMaxSliceBlocks) continue;
-    for (int n = nt_max; n >= 1; --n) {
-      const size_t b = gemv_smem_bytes(n, nb, static_cast<int>(std::min<int64_t>(M, 8 * n)));
-      if (b > kGemvSmemLimit) continue;
-      Shape c;
-      c.s = sl;
-      c.nt = n;
-      c.smem = b;
-      c.ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
-      const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
-      c.waves = (c.ctas + cap - 1) / cap;
-      c.busy = std::min(c.ctas, static_cast<int64_t>(num_sms));
-      if (better(c)) best = c;
+  auto search = [&](int nt_lo, int nt_hi) {
+    for (int sl = kMaxCluster; sl >= 1; sl /= 2) {
+      if (sl > a.nblk) continue;
+      const int nb = (a.nblk + sl - 1) / sl;
+      if (nb > kMaxSliceBlocks) continue;
+      for (int n = nt_hi; n >= nt_lo; --n) {
+        const size_t b = gemv_smem_bytes(n, nb, static_cast<int>(std::min<int64_t>(M, 8 * n)),
+                                         gemv_wide(n, fmt));
+        if (b > kGemvSmemLimit) continue;
+        Shape sh;
+        sh.s = sl;
+        sh.nt = n;
+        sh.smem = b;
+        sh.ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
+        const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
+        sh.waves = (sh.ctas + cap - 1) / cap;
+        sh.busy = std::min(sh.ctas, static_cast<int64_t>(num_sms));
+        if (better(sh)) best = sh;
+      }
     }
-  }
+  };
+  // Up to 8 tokens take one n-tile (the wide table for 4-bit codes); when its
+  // shared memory does not fit (8 tokens of the longest slices), two n-tiles.
+  search(1, M <= 8 ? 1 : 2);
+  if (best.s == 0 && M <= 8) search(2, 2);
   const int best_s = best.s, best_nt = best.nt;
   const size_t best_smem = best.smem;
   if (best_s == 0) return cudaErrorInvalidValue;

@@ -313,7 +313,7 @@ dequantize_int8_kernel(const int8_t* __restrict__ q, const float* __restrict__ a
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int v = static_cast<int8_t>((words[j] >> (8 * e)) & 0xffu);
-      r[e] = __fdiv_rn(__fmul_rn(static_cast<float>(v), a), 127.0f);
+      r[e] = div_by_const<127>(__fmul_rn(static_cast<float>(v), a));
     }
     __stcs(o + j, make_float4(r[0], r[1], r[2], r[3]));
   }

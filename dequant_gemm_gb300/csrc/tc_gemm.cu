@@ -545,7 +545,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     const uint8_t* tab = smem + C::kOffLut + 4 * lane;
     // block scale: 4-bit ahat = fl32(fl32(a8 s2) / 255); int8 absmax / 127
     auto block_scale = [&](uint32_t a8v, float sv) {
-      return kInt8 ? __fdiv_rn(sv, 127.0f) : dequant_absmax(a8v, sv);
+      return kInt8 ? div_by_const<127>(sv) : dequant_absmax(a8v, sv);
     };
     auto load_block = [&](int64_t bi, uint32_t& a8v, float& sv) {
       if constexpr (kInt8) {
