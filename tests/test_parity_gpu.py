@@ -402,3 +402,19 @@ def test_persistent_units_with_ragged_tails(M):
     dX_ref = o.matmul_bwd_dx(dY.float().numpy(), o.dequantize(*o.quantize(Wd), 192, 38912))
     assert_tol(dX, dX_ref, f"persistent dX M={M}")
     assert nf4.nf4_poll_device_status() == 0
+
+
+@pytest.mark.parametrize("rows,cols,M", [
+    (40, 24576, 1), (40, 24576, 16), (520, 7168, 3), (520, 7168, 12), (2056, 1024, 8),
+    (2056, 7168, 1), (264, 49152, 8), (1544, 3584, 16), (4104, 4096, 5), (1032, 8192, 1),
+    (8200, 1024, 1)])
+def test_fwd_small_m_launch_shapes(rows, cols, M):
+    """The small-M forward over its launch shapes: 16 to 128 rows per CTA
+    with 16 to 2 K-parts reducing in shared memory, with and without a
+    cluster of K-slices, one or two token tiles, the wide and the narrow
+    level table, ragged last row tiles and token tiles; compared in full."""
+    W = weight_np(rows, cols, 51)
+    X = wl.activations(M, cols, seed=rows + cols + M)
+    _, Y = run_fwd(W, X)
+    Wh = o.dequantize(*o.quantize(W), rows, cols)
+    assert_tol(Y, o.matmul_fwd(X.float().numpy(), Wh), f"fwd {rows}x{cols} M={M}")
