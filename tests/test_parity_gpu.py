@@ -409,10 +409,10 @@ def test_persistent_units_with_ragged_tails(M):
     (2056, 7168, 1), (264, 49152, 8), (1544, 3584, 16), (4104, 4096, 5), (1032, 8192, 1),
     (8200, 1024, 1)])
 def test_fwd_small_m_launch_shapes(rows, cols, M):
-    """The small-M forward over its launch shapes: 16 to 128 rows per CTA
-    with 16 to 2 K-parts reducing in shared memory, with and without a
-    cluster of K-slices, one or two token tiles, the wide and the narrow
-    level table, ragged last row tiles and token tiles; compared in full."""
+    """The small-M forward over its launch shapes: with and without a
+    cluster of K-slices (1 to 8), one or two n-tiles, one or two token
+    tiles, the wide and the narrow level table, rows that end inside a
+    row group and short or long slices; compared in full."""
     W = weight_np(rows, cols, 51)
     X = wl.activations(M, cols, seed=rows + cols + M)
     _, Y = run_fwd(W, X)
