@@ -96,6 +96,10 @@ def packed_bytes(rows, cols, wdtype="nf4"):
     return n // 2 + nb + 4 * ((nb + 255) // 256)
 
 
+SMALL_M = 16    # forwards up to this many tokens take the streaming small-M kernel
+GROUP_SMALL_M = True   # projections sharing an input take one grouped small-M launch
+
+
 def fwd_work(p, M, w=None):
     """(flop, algorithmic bytes) of Y = X W^T: packed W + X in + Y out."""
     wd, a, o = (w.wdtype, w.act, w.out) if w else ("nf4", "bf16", "f32")
@@ -279,6 +283,7 @@ class Step:
                                                           dtype=act_dt).to(device)
                 self.dx[(i, M)] = torch.empty(M, p.cols, dtype=out_dt, device=device)
         self.quantize_in_step = True
+        self.group_small_m = GROUP_SMALL_M
         self.calls = self._calls()
         self.side = []
         self.graphs = None
@@ -302,6 +307,19 @@ class Step:
         for M in sorted(self.w.fwd_m, reverse=True):
             for r in range(self.rotate):
                 for gi, g in enumerate(groups):
+                    if M <= SMALL_M and len(g) > 1 and self.group_small_m:
+                        # projections sharing their input: one grouped launch;
+                        # X counted once in the algorithmic bytes
+                        ps = [P[i] for i in g]
+                        f = sum(fwd_work(p, M, self.w)[0] for p in ps)
+                        b = sum(fwd_work(p, M, self.w)[1] for p in ps) - \
+                            (len(ps) - 1) * ELEM_BYTES[self.w.act] * M * ps[0].cols
+                        calls.append((f"fwd_M{M}", f, b, 1,
+                                      lambda r=r, g=g, M=M, K=ps[0].cols: nf4.nf4_matmul_fwd_group(
+                                          self.x[(K, M)], [self.q[r][i] for i in g],
+                                          outs=[self.y[(i, M)] for i in g]),
+                                      (f"fwd_M{M}", r, gi), tuple(g)))
+                        continue
                     for i in g:
                         p = P[i]
                         f, b = fwd_work(p, M, self.w)
@@ -433,21 +451,34 @@ class Step:
                     ev_w[i] = torch.cuda.Event()
                     ev_w[i].record(cin)
         main.wait_event(ev_act)
-        for i in order:
+        # a call runs once every weight it reads has landed (a grouped call
+        # reads several); each output goes back right after the call that
+        # writes it
+        pos = {i: n for n, i in enumerate(order)}
+        projs = [c[6] if isinstance(c[6], tuple) else (c[6],) for c in self.calls]
+        turn = [max(pos[j] for j in js) for js in projs]
+        out_turn = {}
+        for c, js, t in zip(self.calls, projs, turn):
+            for kind in ("fwd", "dx"):
+                if c[0].startswith(kind + "_M"):
+                    M = int(c[0][len(kind) + 2:])
+                    for j in js:
+                        out_turn[(kind, j, M)] = t
+        for n, i in enumerate(order):
             if ev_w:
                 main.wait_event(ev_w[i])
-            for c in self.calls:
-                if c[6] == i:
+            for c, t in zip(self.calls, turn):
+                if t == n:
                     c[4]()
             done = torch.cuda.Event()
             done.record(main)
             cout.wait_event(done)
             with torch.cuda.stream(cout):
                 for (j, M), v in self.y.items():
-                    if j == i:
+                    if out_turn.get(("fwd", j, M)) == n:
                         self.h_y[(j, M)].copy_(v, non_blocking=True)
                 for (j, M), v in self.dx.items():
-                    if j == i:
+                    if out_turn.get(("dx", j, M)) == n:
                         self.h_dx[(j, M)].copy_(v, non_blocking=True)
         main.wait_stream(cout)
 
@@ -749,7 +780,12 @@ def main():
                     help="skip the per-workload records (decode, prefill + quantize, dX)")
     ap.add_argument("--naive", action="store_true",
                     help="time the fused forward against dequantize + cuBLAS instead")
+    ap.add_argument("--no-group", action="store_true",
+                    help="small-M forwards of projections sharing an input as separate launches "
+                         "on parallel streams instead of one grouped launch")
     args = ap.parse_args()
+    global GROUP_SMALL_M
+    GROUP_SMALL_M = not args.no_group
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -803,6 +839,9 @@ def main():
                    "quantize_in_step": step.quantize_in_step,
                    "l2": main_run["l2"],
                    "timing": "CUDA graph per kernel class, CUDA events between graphs",
+                   "issue": ("projections sharing an input: one grouped launch at M <= 16, "
+                             "parallel graph branches otherwise" if GROUP_SMALL_M else
+                             "projections sharing an input on parallel graph branches"),
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": step.launches() * args.steps,
         "roofline": roof,

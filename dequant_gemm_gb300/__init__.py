@@ -30,7 +30,7 @@ STATUS = {
 
 # Every symbol the header declares, for load checks.
 EXPORTS = ("nf4_quantize", "nf4_quantize_ex", "nf4_dequantize", "nf4_matmul_fwd",
-           "nf4_matmul_bwd_dx", "nf4_matmul_fwd_ex", "nf4_matmul_bwd_dx_ex",
+           "nf4_matmul_bwd_dx", "nf4_matmul_fwd_ex", "nf4_matmul_bwd_dx_ex", "nf4_matmul_fwd_group",
            "nf4_poll_device_status", "nf4_poll_device_status_site", "nf4_codebook",
            "nf4_codebook_of", "nf4_set_mma_wait_limit", "nf4_last_cuda_error",
            "nf4_status_string")
@@ -39,6 +39,7 @@ EXPORTS = ("nf4_quantize", "nf4_quantize_ex", "nf4_dequantize", "nf4_matmul_fwd"
 DTYPES = {"nf4": 0, "fp4": 1, "int8": 2}
 ELEM = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 ACCUMULATE = 1
+GROUP_MAX = 4          # NF4_GROUP_MAX
 
 
 class NF4Error(RuntimeError):
@@ -81,6 +82,7 @@ def lib() -> ctypes.CDLL:
                 "nf4_matmul_bwd_dx": [vp, i64, W, vp, vp],
                 "nf4_matmul_fwd_ex": [vp, i32, i64, W, vp, i32, i32, vp],
                 "nf4_matmul_bwd_dx_ex": [vp, i32, i64, W, vp, i32, i32, vp],
+                "nf4_matmul_fwd_group": [vp, i32, i64, W, i32, vp, i32, i32, vp],
                 "nf4_poll_device_status": [vp],
                 "nf4_poll_device_status_site": [vp, vp],
                 "nf4_codebook": [vp],
@@ -290,6 +292,53 @@ def nf4_matmul_fwd(X: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = Non
     """Y = X * dequant(W)^T (+ out when accumulate): X bf16 or fp16 [M, cols]
     -> Y fp32 or bf16 [M, rows]."""
     return _matmul("X", "nf4_matmul_fwd_ex", X, w, w.cols, w.rows, out, out_dtype, accumulate)
+
+
+def nf4_matmul_fwd_group(X: torch.Tensor, ws, outs=None, out_dtype: torch.dtype = torch.float32,
+                         accumulate: bool = False) -> list:
+    """Y_i = X * dequant(W_i)^T (+ outs[i] when accumulate) for up to
+    GROUP_MAX weights that share X (same cols and data type, rows may
+    differ); one launch of the small-M kernel for M <= 16. Returns the
+    outputs, fp32 or bf16 [M, rows_i]."""
+    ws = list(ws)
+    if not 1 <= len(ws) <= GROUP_MAX:
+        raise ValueError(f"a group has 1 to {GROUP_MAX} weights, got {len(ws)}")
+    if not isinstance(X, torch.Tensor) or X.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"X must be bfloat16 or float16, got {getattr(X, 'dtype', type(X))}")
+    _require(X, "X", X.dtype)
+    K = ws[0].cols
+    if X.dim() != 2 or X.shape[1] != K:
+        raise ValueError(f"X must be [M, {K}]")
+    M = X.shape[0]
+    for w in ws:
+        if w.cols != K or w.dtype != ws[0].dtype:
+            raise ValueError("the weights of a group must share cols and dtype")
+        _check_weight(w, X.device)
+    if outs is not None:
+        outs = list(outs)
+        if len(outs) != len(ws):
+            raise ValueError("one output per weight")
+        out_dtype = outs[0].dtype
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"the output must be float32 or bfloat16, got {out_dtype}")
+    if outs is not None:
+        for o, w in zip(outs, ws):
+            _require(o, "out", out_dtype, shape=(M, w.rows))
+            _same_device(X.device, out=o)
+    elif accumulate:
+        raise ValueError("accumulate=True needs the output tensors to add to (outs=)")
+    _require_cuda_device(X.device)
+    if outs is None:
+        outs = [torch.empty(M, w.rows, dtype=out_dtype, device=X.device) for w in ws]
+    structs = (nf4_weight * len(ws))(*[w.c_struct() for w in ws])
+    ptrs = (ctypes.c_void_p * len(ws))(*[o.data_ptr() for o in outs])
+    with torch.cuda.device(X.device):
+        _check("nf4_matmul_fwd_group",
+               lib().nf4_matmul_fwd_group(_ptr(X), ELEM[X.dtype], M, structs, len(ws),
+                                          ctypes.cast(ptrs, ctypes.c_void_p),
+                                          ELEM[out_dtype], ACCUMULATE if accumulate else 0,
+                                          _stream(X.device)))
+    return outs
 
 
 def nf4_matmul_bwd_dx(dY: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None,

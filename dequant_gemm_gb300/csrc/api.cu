@@ -95,9 +95,10 @@ nf4_status launched(cudaError_t e) {
 
 size_t elem_bytes(int32_t e) { return e == NF4_F32 ? 4 : 2; }
 
-// The shared body of the fused forward and input gradient.
-nf4_status matmul(bool dx, const void* act, int32_t act_elem, int64_t M, const nf4_weight* w,
-                  void* out, int32_t out_elem, int32_t flags, void* stream) {
+// Validates one fused call without launching anything (the checks of
+// matmul below, in its order).
+nf4_status check_call(bool dx, const void* act, int32_t act_elem, int64_t M, const nf4_weight* w,
+                      const void* out, int32_t out_elem, int32_t flags) {
   if (nf4_status s = check_weight(w)) return s;
   if (act_elem != NF4_BF16 && act_elem != NF4_F16) return NF4_ERR_SHAPE;
   if (out_elem != NF4_F32 && out_elem != NF4_BF16) return NF4_ERR_SHAPE;
@@ -105,19 +106,17 @@ nf4_status matmul(bool dx, const void* act, int32_t act_elem, int64_t M, const n
   if (M < 0 || (w->rows % 8) != 0) return NF4_ERR_SHAPE;
   const int64_t out_cols = dx ? w->cols : w->rows, red = dx ? w->rows : w->cols;
   if (M == 0 || out_cols == 0) return NF4_OK;
-  const bool accumulate = (flags & NF4_ACCUMULATE) != 0;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (red == 0) {  // an empty reduction: the output is 0 (or unchanged when accumulating)
-    if (!out) return NF4_ERR_NULL;
-    if (accumulate) return NF4_OK;
-    return launched(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * out_cols * elem_bytes(out_elem),
-                                    st));
-  }
+  if (red == 0) return out ? NF4_OK : NF4_ERR_NULL;
   if (nf4_status s = check_weight_ptrs(w)) return s;
   if (!act || !out) return NF4_ERR_NULL;
   if (!aligned16(act) || !aligned16(out)) return NF4_ERR_ALIGN;
-  DeviceInfo* d = nullptr;
-  if (nf4_status s = current_device(&d)) return s;
+  return NF4_OK;
+}
+
+// One fused call as the launchers take it (after check_call).
+nf4::MatmulCall make_call(const void* act, int32_t act_elem, int64_t M, const nf4_weight* w,
+                          void* out, int32_t out_elem, int32_t flags, const DeviceInfo* d,
+                          cudaStream_t st) {
   nf4::MatmulCall c;
   c.act = act;
   c.act_f16 = act_elem == NF4_F16;
@@ -130,14 +129,65 @@ nf4_status matmul(bool dx, const void* act, int32_t act_elem, int64_t M, const n
   c.scale = w->absmax_scale;
   c.out = out;
   c.out_bf16 = out_elem == NF4_BF16;
-  c.accumulate = accumulate;
+  c.accumulate = (flags & NF4_ACCUMULATE) != 0;
   c.num_sms = d->num_sms;
   c.status = d->status;
   c.wait_limit = g_mma_wait_limit.load(std::memory_order_relaxed);
   c.st = st;
+  return c;
+}
+
+// The shared body of the fused forward and input gradient.
+nf4_status matmul(bool dx, const void* act, int32_t act_elem, int64_t M, const nf4_weight* w,
+                  void* out, int32_t out_elem, int32_t flags, void* stream) {
+  if (nf4_status s = check_call(dx, act, act_elem, M, w, out, out_elem, flags)) return s;
+  const int64_t out_cols = dx ? w->cols : w->rows, red = dx ? w->rows : w->cols;
+  if (M == 0 || out_cols == 0) return NF4_OK;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (red == 0) {  // an empty reduction: the output is 0 (or unchanged when accumulating)
+    if ((flags & NF4_ACCUMULATE) != 0) return NF4_OK;
+    return launched(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * out_cols * elem_bytes(out_elem),
+                                    st));
+  }
+  DeviceInfo* d = nullptr;
+  if (nf4_status s = current_device(&d)) return s;
+  const nf4::MatmulCall c = make_call(act, act_elem, M, w, out, out_elem, flags, d, st);
   if (!dx && M <= kSmallMFwd && w->cols <= nf4::kGemvMaxCols)
     return launched(nf4::launch_gemv_fwd(c));
   return launched(dx ? nf4::launch_tc_dx(c) : nf4::launch_tc_fwd(c));
+}
+
+// Forwards of several weights sharing the activations: one small-M launch
+// over all their row tiles, else one call per weight.
+nf4_status matmul_group(const void* act, int32_t act_elem, int64_t M, const nf4_weight* ws,
+                        int32_t count, void* const* outs, int32_t out_elem, int32_t flags,
+                        void* stream) {
+  if (!ws || !outs) return NF4_ERR_NULL;
+  if (count < 1 || count > NF4_GROUP_MAX) return NF4_ERR_SHAPE;
+  for (int i = 0; i < count; ++i) {
+    if (nf4_status s = check_weight(&ws[i])) return s;
+    if (ws[i].cols != ws[0].cols || ws[i].dtype != ws[0].dtype) return NF4_ERR_SHAPE;
+  }
+  for (int i = 0; i < count; ++i)
+    if (nf4_status s = check_call(false, act, act_elem, M, &ws[i], outs[i], out_elem, flags))
+      return s;
+  const int64_t K = ws[0].cols;
+  if (M == 0) return NF4_OK;
+  if (M > kSmallMFwd || K == 0 || K > nf4::kGemvMaxCols) {
+    for (int i = 0; i < count; ++i)
+      if (nf4_status s = matmul(false, act, act_elem, M, &ws[i], outs[i], out_elem, flags, stream))
+        return s;
+    return NF4_OK;
+  }
+  DeviceInfo* d = nullptr;
+  if (nf4_status s = current_device(&d)) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  nf4::MatmulCall cs[NF4_GROUP_MAX];
+  int n = 0;
+  for (int i = 0; i < count; ++i)   // weights without rows have nothing to write
+    if (ws[i].rows > 0) cs[n++] = make_call(act, act_elem, M, &ws[i], outs[i], out_elem, flags, d, st);
+  if (n == 0) return NF4_OK;
+  return launched(nf4::launch_gemv_group(cs, n));
 }
 
 nf4_status quantize(const void* W, int32_t w_elem, int64_t rows, int64_t cols, int32_t blocksize,
@@ -194,6 +244,12 @@ nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, flo
 nf4_status nf4_matmul_bwd_dx(const uint16_t* dY, int64_t M, const nf4_weight* w, float* dX,
                              void* stream) {
   return matmul(true, dY, NF4_BF16, M, w, dX, NF4_F32, 0, stream);
+}
+
+nf4_status nf4_matmul_fwd_group(const void* X, int32_t x_elem, int64_t M, const nf4_weight* ws,
+                                int32_t count, void* const* Ys, int32_t y_elem, int32_t flags,
+                                void* stream) {
+  return matmul_group(X, x_elem, M, ws, count, Ys, y_elem, flags, stream);
 }
 
 nf4_status nf4_matmul_fwd_ex(const void* X, int32_t x_elem, int64_t M, const nf4_weight* w,

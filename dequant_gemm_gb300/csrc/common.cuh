@@ -18,6 +18,8 @@ constexpr int kGroupElems = kBlock * kGroup;  // 16384 weights per group
 // portable cluster size) of at most 96 blocks each. Longer rows go to the
 // tensor-core kernel.
 constexpr int64_t kGemvMaxCols = 8 * 96 * kBlock;
+// Most weights a grouped small-M forward takes in one launch.
+constexpr int kGemvGroupMax = NF4_GROUP_MAX;
 
 // The 16 NF4 levels: standard-normal quantiles at evenly spaced probabilities
 // (8 on the positive side from delta = (1 - 1/30 + 1 - 1/32) / 2 to 1/2,
@@ -199,6 +201,10 @@ cudaError_t launch_quantize(const void* W, bool w_bf16, int fmt, int64_t n_elems
 cudaError_t launch_dequantize(int fmt, const uint8_t* codes, const uint8_t* a8, const float* s2,
                               int64_t n_elems, float* out, cudaStream_t st);
 cudaError_t launch_gemv_fwd(const MatmulCall& c);
+// One launch for `count` (1 .. kGemvGroupMax) weights that share the
+// activations, K, the data type, the element types, the flags and the
+// stream; each call gives its own weight, N and output.
+cudaError_t launch_gemv_group(const MatmulCall* cs, int count);
 cudaError_t launch_tc_fwd(const MatmulCall& c);
 cudaError_t launch_tc_dx(const MatmulCall& c);
 cudaError_t launch_simt_dx(const MatmulCall& c);

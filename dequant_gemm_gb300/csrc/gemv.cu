@@ -128,12 +128,21 @@ __device__ __forceinline__ void st_dsmem(float* local, uint32_t rank, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+// Up to kGemvGroupMax weights that share the activations (and K and the
+// data type) run in one launch: the row tiles of weight i are blocks
+// [tile0[i], tile0[i + 1]) of the grid's x dimension.
+struct GemvMaps {
+  CUtensorMap m[kGemvGroupMax];   // the codes of each weight
+};
 struct GemvArgs {
-  const uint16_t* X;     // bf16 or fp16 [M, K]
-  const uint8_t* a8;     // 4-bit formats: [N*K/64]
-  const float* scale;    // 4-bit formats: s2 [groups]; int8: absmax [N*K/64]
-  void* Y;               // fp32 or bf16 [M, N]
-  int64_t M, N, K;
+  const uint16_t* X;                   // bf16 or fp16 [M, K]
+  const uint8_t* a8[kGemvGroupMax];    // 4-bit formats: [N*K/64]
+  const float* scale[kGemvGroupMax];   // 4-bit formats: s2 [groups]; int8: absmax [N*K/64]
+  void* Y[kGemvGroupMax];              // fp32 or bf16 [M, N]
+  int64_t N[kGemvGroupMax];
+  int tile0[kGemvGroupMax + 1];
+  int count;
+  int64_t M, K;
   int nblk;              // K / 64
   int slices;            // K-slices = cluster size along y
   int max_nb;            // largest slice, in blocks
@@ -224,7 +233,7 @@ struct GemvFmt {
 
 template <int NT, int kFmt, bool kF16>
 __global__ void __launch_bounds__(kGemvThreads, gemv_wide(NT, kFmt) ? 1 : 2)
-gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) {
+gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs p) {
   constexpr bool kInt8 = GemvFmt<kFmt>::kInt8;
   constexpr int kBoxBlocks = GemvFmt<kFmt>::kBoxBlocks;
   constexpr int kBlockBytes = GemvFmt<kFmt>::kBlockBytes;
@@ -246,7 +255,29 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   // once that warp has consumed its last box
   float* red = reinterpret_cast<float*>(smem + gemv_off_slots(kWide) +
                                        (rgp + kRowGroups) * kWarpSlots * kBoxBytes);
-  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kGemvRows;
+  // this CTA's weight of the group (selects on static indices, so the
+  // parameter arrays stay in parameter space)
+  int gi = 0;
+#pragma unroll
+  for (int q = 1; q < kGemvGroupMax; ++q)
+    gi += (q < p.count && static_cast<int>(blockIdx.x) >= p.tile0[q]) ? 1 : 0;
+  auto pick = [&](auto const (&arr)[kGemvGroupMax]) {
+    auto v = arr[0];
+#pragma unroll
+    for (int q = 1; q < kGemvGroupMax; ++q)
+      if (gi == q) v = arr[q];
+    return v;
+  };
+  const int64_t N = pick(p.N);
+  const uint8_t* const a8 = pick(p.a8);
+  const float* const scale = pick(p.scale);
+  void* const Y = pick(p.Y);
+  const CUtensorMap* const tm_codes = &maps.m[gi];
+  int tile_first = p.tile0[0];
+#pragma unroll
+  for (int q = 1; q < kGemvGroupMax; ++q)
+    if (gi == q) tile_first = p.tile0[q];
+  const int64_t row0 = static_cast<int64_t>(static_cast<int>(blockIdx.x) - tile_first) * kGemvRows;
   const int slice = blockIdx.y;
   const int kb0 = slice_begin(p.nblk, p.slices, slice);
   const int nb = slice_begin(p.nblk, p.slices, slice + 1) - kb0;
@@ -271,20 +302,20 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     // with demand loads and was measured slower (35 MB weights, 4% slower
     // even with the first four boxes only).
     const int nmine_pf = (nboxes - kh + 1) / 2;
-    if (lane == 0 && nmine_pf <= kWarpSlots && row0 + rgp * 16 < p.N)   // boxes inside the weight
+    if (lane == 0 && nmine_pf <= kWarpSlots && row0 + rgp * 16 < N)   // boxes inside the weight
       for (int i = 0; i < nmine_pf; ++i)
-        tma_prefetch_2d(&tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * kBlockBytes,
+        tma_prefetch_2d(tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * kBlockBytes,
                             static_cast<int32_t>(row0 + rgp * 16));
     const int64_t pr = row0 + rgp * 16 + lane;
-    if (kh == 0 && lane < 16 && pr < p.N && nb > 0 && nmine_pf <= kWarpSlots) {
+    if (kh == 0 && lane < 16 && pr < N && nb > 0 && nmine_pf <= kWarpSlots) {
       const int64_t ia = pr * p.nblk + kb0;
       if constexpr (kInt8) {
-        prefetch_l2(p.scale + ia);
-        prefetch_l2(p.scale + ia + nb - 1);
+        prefetch_l2(scale + ia);
+        prefetch_l2(scale + ia + nb - 1);
       } else {
-        prefetch_l2(p.a8 + ia);
-        prefetch_l2(p.a8 + ia + nb - 1);
-        prefetch_l2(p.scale + (ia >> 8));
+        prefetch_l2(a8 + ia);
+        prefetch_l2(a8 + ia + nb - 1);
+        prefetch_l2(scale + (ia >> 8));
       }
     }
   }
@@ -302,7 +333,7 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   if (lane == 0) {
     for (int s = 0; s < kWarpSlots; ++s) tc::mbar_init(bars + 8u * s, 1);
     tc::fence_barrier_init();
-    tc::prefetch_tensormap(&tm_codes);
+    tc::prefetch_tensormap(tm_codes);
   }
   __syncwarp();
   // First half of a split cluster barrier: the CTAs of a cluster store into
@@ -346,13 +377,13 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
   // row pair (e & 7, (e & 7) + 8) of block e >> 3 of the box.
   const int nmine = (nboxes - kh + 1) / 2;   // boxes of this warp
   const int64_t ar = row0 + rgp * 16 + (lane & 7);
-  const bool ar_ok = ar < p.N, br_ok = ar + 8 < p.N;
+  const bool ar_ok = ar < N, br_ok = ar + 8 < N;
   auto issue_box = [&](int i) {
     if (lane == 0) {
       const int b = kh + 2 * i;
       const uint32_t bar = bars + 8u * (i % kWarpSlots);
       tc::mbar_arrive_expect_tx(bar, kBoxBytes);
-      tc::tma_load_2d(slots + (i % kWarpSlots) * kBoxBytes, &tm_codes,
+      tc::tma_load_2d(slots + (i % kWarpSlots) * kBoxBytes, tm_codes,
                       (kb0 + kBoxBlocks * b) * kBlockBytes, static_cast<int32_t>(row0 + rgp * 16),
                       bar);
     }
@@ -365,13 +396,13 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     const int64_t ia = ar * p.nblk + kb0 + j, ib = ia + 8 * p.nblk;
     if constexpr (kInt8) {
       qa = qb = 0u;
-      sa = (in && ar_ok) ? __ldg(p.scale + ia) : 0.0f;
-      sb = (in && br_ok) ? __ldg(p.scale + ib) : 0.0f;
+      sa = (in && ar_ok) ? __ldg(scale + ia) : 0.0f;
+      sb = (in && br_ok) ? __ldg(scale + ib) : 0.0f;
     } else {
-      qa = (in && ar_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ia)) : 0u;
-      qb = (in && br_ok) ? static_cast<uint32_t>(__ldg(p.a8 + ib)) : 0u;
-      sa = (in && ar_ok) ? __ldg(p.scale + (ia >> 8)) : 0.0f;
-      sb = (in && br_ok) ? __ldg(p.scale + (ib >> 8)) : 0.0f;
+      qa = (in && ar_ok) ? static_cast<uint32_t>(__ldg(a8 + ia)) : 0u;
+      qb = (in && br_ok) ? static_cast<uint32_t>(__ldg(a8 + ib)) : 0u;
+      sa = (in && ar_ok) ? __ldg(scale + (ia >> 8)) : 0.0f;
+      sb = (in && br_ok) ? __ldg(scale + (ib >> 8)) : 0.0f;
     }
   };
   uint32_t qa0, qb0, qa1, qb1;
@@ -590,8 +621,8 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     __syncthreads();
     for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
       const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
-      if (tk < mt && row0 + r4 < p.N)
-        store_out4(p.Y, (m0 + tk) * p.N + row0 + r4,
+      if (tk < mt && row0 + r4 < N)
+        store_out4(Y, (m0 + tk) * N + row0 + r4,
                    *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4), p.out_bf16,
                    p.accumulate);
     }
@@ -621,10 +652,10 @@ gemv_fwd_kernel(const __grid_constant__ CUtensorMap tm_codes, const GemvArgs p) 
     const int rank = static_cast<int>(tc::cluster_ctarank());
     for (int i = tid; i < 8 * NT * rpc; i += kGemvThreads) {
       const int tk = i >> rpc_shift, rl = i & (rpc - 1), r = rank * rpc + rl;
-      if (tk < mt && row0 + r < p.N) {
+      if (tk < mt && row0 + r < N) {
         float v = 0.0f;
         for (int c = 0; c < p.slices; ++c) v += inbox[((c * 8 * NT + tk) << rpc_shift) + rl];
-        store_out(p.Y, (m0 + tk) * p.N + row0 + r, v, p.out_bf16, p.accumulate);
+        store_out(Y, (m0 + tk) * N + row0 + r, v, p.out_bf16, p.accumulate);
       }
     }
   }
@@ -647,7 +678,7 @@ void set_smem_limit() {
 }
 
 template <int kFmt, bool kF16>
-cudaError_t launch_gemv_as(int nt, const cudaLaunchConfig_t& cfg, const CUtensorMap& tm,
+cudaError_t launch_gemv_as(int nt, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
                            const GemvArgs& a) {
   static std::once_flag once;
   std::call_once(once, [] {
@@ -658,16 +689,27 @@ cudaError_t launch_gemv_as(int nt, const cudaLaunchConfig_t& cfg, const CUtensor
                  : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16>, tm, a);
 }
 
-cudaError_t launch_gemv_fwd(const MatmulCall& c) {
-  const int64_t M = c.M, N = c.N, K = c.K;
+cudaError_t launch_gemv_fwd(const MatmulCall& c) { return launch_gemv_group(&c, 1); }
+
+cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
+  if (count < 1 || count > kGemvGroupMax) return cudaErrorInvalidValue;
+  const MatmulCall& c = cs[0];   // activations, M, K, formats, flags and stream are shared
+  const int64_t M = c.M, K = c.K;
   const int num_sms = c.num_sms;
-  GemvArgs a;
+  GemvArgs a = {};
   a.X = static_cast<const uint16_t*>(c.act);
-  a.a8 = c.a8;
-  a.scale = c.scale;
-  a.Y = c.out;
+  a.count = count;
+  a.tile0[0] = 0;
+  for (int i = 0; i < kGemvGroupMax; ++i) {
+    const MatmulCall& ci = cs[i < count ? i : 0];
+    a.a8[i] = ci.a8;
+    a.scale[i] = ci.scale;
+    a.Y[i] = ci.out;
+    a.N[i] = ci.N;
+    const int64_t tiles = i < count ? (ci.N + kGemvRows - 1) / kGemvRows : 0;
+    a.tile0[i + 1] = a.tile0[i] + static_cast<int>(tiles);
+  }
   a.M = M;
-  a.N = N;
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
   a.out_bf16 = c.out_bf16 ? 1 : 0;
@@ -679,7 +721,7 @@ cudaError_t launch_gemv_fwd(const MatmulCall& c) {
   // busy (bigger CTAs pay the prologue and the cluster barrier less often;
   // measured faster than filling every SM with smaller ones), else the most
   // busy SMs; then two n-tiles over one.
-  const int64_t row_ctas = (N + kGemvRows - 1) / kGemvRows;
+  const int64_t row_ctas = a.tile0[count];   // row tiles of all weights
   const int fmt = c.fmt;
   struct Shape { int s, nt; int64_t ctas, waves, busy; size_t smem; };
   Shape best{0, 0, 0, 0, 0, 0};
@@ -730,12 +772,15 @@ cudaError_t launch_gemv_fwd(const MatmulCall& c) {
   // others stay idle.
   const size_t smem = best.ctas <= num_sms ? std::max(best_smem, kGemvSmemTwoPerSm + 4096) : best_smem;
   // codes [N, row bytes] (K/2 packed 4-bit, K int8), box 128 B x 16 rows,
-  // 128-byte swizzle
+  // 128-byte swizzle; one map per weight (unused entries repeat the first)
   const uint64_t row_bytes = static_cast<uint64_t>(c.fmt == kFmtInt8 ? K : K / 2);
-  CUtensorMap tm;
-  if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.codes, row_bytes, static_cast<uint64_t>(N),
-                 row_bytes, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  GemvMaps tm;
+  for (int i = 0; i < kGemvGroupMax; ++i) {
+    const MatmulCall& ci = cs[i < count ? i : 0];
+    if (!encode_2d(&tm.m[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, ci.codes, row_bytes,
+                   static_cast<uint64_t>(ci.N), row_bytes, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(row_ctas), static_cast<unsigned>(a.slices),
                      static_cast<unsigned>(mtiles));

@@ -101,6 +101,9 @@ typedef enum nf4_elem {
 /* Flags of the fused matmuls. */
 #define NF4_ACCUMULATE 1       /* add the product to the output's contents */
 
+/* Most weights one nf4_matmul_fwd_group call takes. */
+#define NF4_GROUP_MAX 4
+
 /* A quantized weight (the QuantState of the bitsandbytes page, reduced to
  * plain device pointers). All arrays are device pointers owned by the
  * caller, in the storage format of `dtype` above. A zero-initialised dtype
@@ -202,6 +205,30 @@ nf4_status nf4_matmul_fwd_ex(const void* X, int32_t x_elem, int64_t M, const nf4
  *   NF4_F32 or NF4_BF16), flags NF4_ACCUMULATE: dX += dY * dequant(W). */
 nf4_status nf4_matmul_bwd_dx_ex(const void* dY, int32_t dy_elem, int64_t M, const nf4_weight* w,
                                 void* dX, int32_t dx_elem, int32_t flags, void* stream);
+
+/* The fused forward of up to NF4_GROUP_MAX weights that read the same
+ * activations (the q, k and v projections of an attention layer, or the gate
+ * and up projections of an MLP): Y_i = X * dequant(W_i)^T for i < count.
+ * The method is nf4_matmul_fwd_ex's ("Zenbit", zenbit.pallas_nf4 bullet);
+ * putting the weights in one launch is this library's choice, so that a
+ * decode step pays the launch latency once per shared input.
+ *   X      device [M, cols], x_elem NF4_BF16 or NF4_F16
+ *   ws     host array of `count` weights, 1 <= count <= NF4_GROUP_MAX, all
+ *          with the same cols and dtype (rows may differ)
+ *   Ys     host array of `count` device outputs; Ys[i] is [M, ws[i].rows]
+ *          of y_elem (NF4_F32 or NF4_BF16)
+ *   flags  NF4_ACCUMULATE or 0, as nf4_matmul_fwd_ex
+ * With M <= 16 and cols <= 49152 every weight runs in one launch of the
+ * small-M kernel, one grid over all their row tiles; otherwise each weight
+ * is one tensor-core launch, in order, on `stream`. The results are those of
+ * count nf4_matmul_fwd_ex calls, up to the order of the fp32 sums (the
+ * accuracy statement is the same). Every weight and output is validated as
+ * nf4_matmul_fwd_ex does before anything is launched; ws or Ys NULL is
+ * NF4_ERR_NULL; count out of range, or weights that differ in cols or dtype,
+ * NF4_ERR_SHAPE. */
+nf4_status nf4_matmul_fwd_group(const void* X, int32_t x_elem, int64_t M, const nf4_weight* ws,
+                                int32_t count, void* const* Ys, int32_t y_elem, int32_t flags,
+                                void* stream);
 
 /* Synchronizes `stream`, then reports and clears the device status word of
  * the current device: NF4_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran

@@ -170,3 +170,33 @@ def test_valid_ex_calls_without_device_report_device_error():
     i8 = nf4.nf4_weight(P, None, P, 8, 64, 64, 0, 2)
     assert L.nf4_matmul_fwd_ex(P, 2, 4, ctypes.byref(i8), P, 1, 1, None) == 5
     assert L.nf4_quantize_ex(P, 1, 8, 64, 64, 2, P, None, P, None) == 5
+
+
+def test_matmul_group_validation():
+    L = nf4.lib()
+    a = nf4.nf4_weight(P, P, P, 8, 64, 64, 256, 0)
+    b = nf4.nf4_weight(P, P, P, 24, 64, 64, 256, 0)
+    ws = (nf4.nf4_weight * 2)(a, b)
+    outs = (ctypes.c_void_p * 2)(P, P)
+    g = L.nf4_matmul_fwd_group
+    assert g(P, 1, 4, None, 2, outs, 0, 0, None) == 1                 # no weights
+    assert g(P, 1, 4, ws, 2, None, 0, 0, None) == 1                   # no outputs
+    assert g(P, 1, 4, ws, 0, outs, 0, 0, None) == 2                   # empty group
+    assert g(P, 1, 4, (nf4.nf4_weight * 5)(*([a] * 5)), 5,
+             (ctypes.c_void_p * 5)(*([P] * 5)), 0, 0, None) == 2      # above NF4_GROUP_MAX
+    other_cols = (nf4.nf4_weight * 2)(a, nf4.nf4_weight(P, P, P, 8, 128, 64, 256, 0))
+    assert g(P, 1, 4, other_cols, 2, outs, 0, 0, None) == 2
+    other_dtype = (nf4.nf4_weight * 2)(a, nf4.nf4_weight(P, P, P, 8, 64, 64, 256, 1))
+    assert g(P, 1, 4, other_dtype, 2, outs, 0, 0, None) == 2
+    assert g(P, 0, 4, ws, 2, outs, 0, 0, None) == 2                   # fp32 activations
+    assert g(P, 1, 4, ws, 2, (ctypes.c_void_p * 2)(P, P + 4), 0, 0, None) == 3
+    assert g(P, 1, 4, ws, 2, (ctypes.c_void_p * 2)(P, None), 0, 0, None) == 1
+    assert g(P, 1, 0, ws, 2, outs, 0, 0, None) == 0                   # M = 0: nothing to do
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_group_call_without_device_reports_device_error():
+    a = nf4.nf4_weight(P, P, P, 8, 64, 64, 256, 0)
+    ws = (nf4.nf4_weight * 2)(a, a)
+    assert nf4.lib().nf4_matmul_fwd_group(P, 1, 4, ws, 2, (ctypes.c_void_p * 2)(P, P), 0, 0,
+                                          None) == 5

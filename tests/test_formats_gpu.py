@@ -276,3 +276,47 @@ def test_accumulate_adds_to_the_output(M):
     dref = o.matmul_bwd_dx(dY.float().cpu().numpy(), oracle_dequant(W, "nf4"))
     assert_tol((dX.double() - dX0.double()).cpu().numpy(), dref, f"accumulate dX M={M}")
     assert nf4.nf4_poll_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["nf4", "fp4", "int8"])
+@pytest.mark.parametrize("M", [1, 6, 16, 40])
+def test_fwd_group_matches_the_oracle(dtype, M):
+    """Weights that share X (rows 520, 136 and 1032 over K = 3584, like a
+    q/k/v group) in one small-M launch (M <= 16) or one tensor-core launch
+    each (M = 40); every output against the oracle."""
+    shapes = [(520, 3584), (136, 3584), (1032, 3584)]
+    Ws = [weight_np(r, c, 60 + i) for i, (r, c) in enumerate(shapes)]
+    qs = [nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype) for W in Ws]
+    X = wl.activations(M, 3584, seed=M + 61)
+    Ys = nf4.nf4_matmul_fwd_group(X.to(DEV), qs)
+    for W, Y, (r, c) in zip(Ws, Ys, shapes):
+        ref = o.matmul_fwd(X.float().numpy(), oracle_dequant(W, dtype))
+        assert_tol(Y.cpu().numpy(), ref, f"group {dtype} {r}x{c} M={M}")
+
+
+@pytest.mark.parametrize("M", [3, 16])
+def test_fwd_group_bf16_accumulate_fp16_activations(M):
+    """A gate/up-like pair with fp16 activations, adding into bf16 outputs:
+    each output is its starting value plus the product, rounded once."""
+    shapes = [(264, 2048), (72, 2048)]
+    Ws = [weight_np(r, c, 70 + i) for i, (r, c) in enumerate(shapes)]
+    qs = [nf4.nf4_quantize(torch.from_numpy(W).to(DEV)) for W in Ws]
+    X = wl.activations(M, 2048, seed=M + 71, dtype=torch.float16)
+    start = [wl.activations(M, r, seed=M + 72 + i).float() for i, (r, _) in enumerate(shapes)]
+    outs = [s.to(torch.bfloat16).to(DEV) for s in start]
+    nf4.nf4_matmul_fwd_group(X.to(DEV), qs, outs=outs, accumulate=True)
+    for W, Y, s0 in zip(Ws, outs, start):
+        ref = o.matmul_fwd(X.float().numpy(), oracle_dequant(W, "nf4")) + \
+            s0.to(torch.bfloat16).float().numpy()
+        assert_tol(Y.float().cpu().numpy(), ref, f"group accumulate M={M}",
+                   rel=REL_FRO + BF16_U * (1 + REL_FRO), mx=MAX_REL + BF16_U * (1 + MAX_REL))
+
+
+def test_fwd_group_of_one_equals_the_single_call():
+    """A group of one weight runs the same launch as nf4_matmul_fwd: the
+    outputs are bitwise equal."""
+    W = weight_np(4096, 4096, 80)
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    X = wl.activations(4, 4096, seed=81).to(DEV)
+    (Yg,) = nf4.nf4_matmul_fwd_group(X, [q])
+    assert torch.equal(Yg, nf4.nf4_matmul_fwd(X, q))
