@@ -98,6 +98,7 @@ def packed_bytes(rows, cols, wdtype="nf4"):
 
 SMALL_M = 16    # forwards up to this many tokens take the streaming small-M kernel
 GROUP_SMALL_M = True   # projections sharing an input take one grouped small-M launch
+PARALLEL_TC = True     # tensor-core calls of projections sharing an input on parallel streams
 
 
 def fwd_work(p, M, w=None):
@@ -284,9 +285,17 @@ class Step:
                 self.dx[(i, M)] = torch.empty(M, p.cols, dtype=out_dt, device=device)
         self.quantize_in_step = True
         self.group_small_m = GROUP_SMALL_M
+        self.parallel_tc = PARALLEL_TC
         self.calls = self._calls()
         self.side = []
         self.graphs = None
+
+    def parallel(self, M):
+        """Whether the calls of one input group at M tokens go out on
+        parallel streams: the small-M kernel's separate launches (when not
+        grouped) and the tensor-core launches (measured faster than one after
+        another at 64 and 2048 tokens: the small projections' grids overlap)."""
+        return (M <= SMALL_M and not self.group_small_m) or (M > SMALL_M and self.parallel_tc)
 
     def _calls(self):
         """List of (category, flop, bytes, launches, fn, group, projection) in
@@ -323,20 +332,22 @@ class Step:
                     for i in g:
                         p = P[i]
                         f, b = fwd_work(p, M, self.w)
+                        tag = (f"fwd_M{M}", r, gi) if self.parallel(M) else (f"fwd_M{M}", r, gi, i)
                         calls.append((f"fwd_M{M}", f, b, 1,
                                       lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_fwd(
                                           self.x[(p.cols, M)], self.q[r][i], out=self.y[(i, M)]),
-                                      (f"fwd_M{M}", r, gi), i))
+                                      tag, i))
         for M in self.w.dx_m:
             for r in range(self.rotate):
                 for gi, g in enumerate(groups):
                     for i in g:
                         p = P[i]
                         f, b = dx_work(p, M, self.w)
+                        tag = (f"dx_M{M}", r, gi) if self.parallel(M) else (f"dx_M{M}", r, gi, i)
                         calls.append((f"dx_M{M}", f, b, 1,
                                       lambda r=r, i=i, M=M, p=p: nf4.nf4_matmul_bwd_dx(
                                           self.dy[(p.rows, M)], self.q[r][i], out=self.dx[(i, M)]),
-                                      (f"dx_M{M}", r, gi), i))
+                                      tag, i))
         return calls
 
     def issue(self, idx):
@@ -780,12 +791,16 @@ def main():
                     help="skip the per-workload records (decode, prefill + quantize, dX)")
     ap.add_argument("--naive", action="store_true",
                     help="time the fused forward against dequantize + cuBLAS instead")
+    ap.add_argument("--serial-tc", action="store_true",
+                    help="tensor-core calls of projections sharing an input one after another "
+                         "instead of on parallel streams")
     ap.add_argument("--no-group", action="store_true",
                     help="small-M forwards of projections sharing an input as separate launches "
                          "on parallel streams instead of one grouped launch")
     args = ap.parse_args()
-    global GROUP_SMALL_M
+    global GROUP_SMALL_M, PARALLEL_TC
     GROUP_SMALL_M = not args.no_group
+    PARALLEL_TC = not args.serial_tc
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -839,9 +854,11 @@ def main():
                    "quantize_in_step": step.quantize_in_step,
                    "l2": main_run["l2"],
                    "timing": "CUDA graph per kernel class, CUDA events between graphs",
-                   "issue": ("projections sharing an input: one grouped launch at M <= 16, "
-                             "parallel graph branches otherwise" if GROUP_SMALL_M else
-                             "projections sharing an input on parallel graph branches"),
+                   "issue": ("projections sharing an input: "
+                             + ("one grouped launch at M <= 16" if GROUP_SMALL_M else
+                                "parallel graph branches at M <= 16")
+                             + (", parallel graph branches above" if PARALLEL_TC else
+                                ", one after another above")),
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": step.launches() * args.steps,
         "roofline": roof,

@@ -50,9 +50,12 @@
 // an MN-major descriptor: no transposition and no per-row scale exchange
 // between lanes.
 //
-// When the output tiles alone cannot fill the GPU and the output is fp32,
-// the reduction is split across units and summed with atomics into a zeroed
-// (or, accumulating, the caller's) output. A bf16 output is never split.
+// When the output tiles alone cannot fill the GPU, or (forward) leave the
+// persistent grid a partial last round (112 tiles on 76 pairs run two
+// rounds, the second 47% full; split in two, 224 half-length units run three
+// full ones), and the output is fp32, the reduction is split across units
+// and summed with atomics into a zeroed (or, accumulating, the caller's)
+// output. A bf16 output is never split.
 //
 // Every mbarrier wait is bounded; a CTA that gives up records a timeout in the
 // device status word and raises an abort flag (its own and, on a pair, the
@@ -761,11 +764,40 @@ cudaError_t launch_tc(const MatmulCall& c) {
   const int64_t row_units = (nd + kTileRows * C::kCg - 1) / (kTileRows * C::kCg);
   const int64_t m_tiles = (M + a.bn - 1) / a.bn;
   a.stages_total = static_cast<int>((red + 63) / 64);
+  // Splits of the reduction, summed with atomics into the output (fp32 only):
+  // when the tiles alone leave SMs idle, or (forward) leave the persistent
+  // grid a partial last round. The estimate is the makespan in stages:
+  // rounds of the grid x (stages a split + a unit's fixed cost). The fixed
+  // cost, about 30 stages, was fitted to single launches of the
+  // decoder-layer shapes at 2048 tokens, split and unsplit (3584 x 18944
+  // forward 201 -> 168 us split in two, while 3584 x 3584 lost 2-7%). Each
+  // split covers at least one ring of stages; a split is taken only when it
+  // gains at least 10% (it adds the zeroing pass and atomic stores). The
+  // input gradient splits only grids smaller than the GPU: splitting the
+  // 18944 x 3584 gradient in two was 19% faster alone but slower inside the
+  // decoder-layer step, where its output's atomics compete with the other
+  // projections' traffic.
+  const int64_t groups_max = std::max(1, c.num_sms / C::kCg);
+  const int64_t tiles = row_units * m_tiles;
   int splits = 1;
-  const int64_t ctas = row_units * C::kCg * m_tiles;
-  if (ctas < c.num_sms && !c.out_bf16) {   // each split fills the ring at least once
-    splits = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>(c.num_sms / ctas, a.stages_total / C::kStages)));
+  if (kDx) {
+    const int64_t ctas = tiles * C::kCg;
+    if (ctas < c.num_sms && !c.out_bf16)   // each split fills the ring at least once
+      splits = static_cast<int>(std::max<int64_t>(
+          1, std::min<int64_t>(c.num_sms / ctas, a.stages_total / C::kStages)));
+  } else if (!c.out_bf16) {
+    const int64_t smax = std::max<int64_t>(1, std::min<int64_t>(a.stages_total / C::kStages, 16));
+    const int64_t ovh = 32;
+    auto cost = [&](int64_t s) {
+      return ((tiles * s + groups_max - 1) / groups_max) * ((a.stages_total + s - 1) / s + ovh);
+    };
+    int64_t best = cost(1), best_s = 1;
+    for (int64_t s = 2; s <= smax; ++s)
+      if (cost(s) < best) {
+        best = cost(s);
+        best_s = s;
+      }
+    if (best * 10 <= cost(1) * 9) splits = static_cast<int>(best_s);
   }
   a.stages_per_split = (a.stages_total + splits - 1) / splits;
   splits = (a.stages_total + a.stages_per_split - 1) / a.stages_per_split;
@@ -775,7 +807,7 @@ cudaError_t launch_tc(const MatmulCall& c) {
   const int64_t units = row_units * m_tiles * splits;
   a.units = static_cast<int>(units);
   // persistent: at most one CTA (or pair) per SM, each taking units in turn
-  const int64_t groups = std::min<int64_t>(units, std::max(1, c.num_sms / C::kCg));
+  const int64_t groups = std::min<int64_t>(units, groups_max);
 
   CUtensorMap tm_act, tm_codes;
   // activations: [M, red] 16-bit, box 64 (reduction) x the tokens one CTA

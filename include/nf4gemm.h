@@ -164,11 +164,12 @@ nf4_status nf4_dequantize(const nf4_weight* w, float* W_out, void* stream);
  * dequantize-then-multiply: relative Frobenius error <= 2e-3 and max error
  * <= 5e-3 * max|Y_ref| (weights enter the tensor cores as bf16, or as fp16
  * levels with the block scale applied in fp32 on the small-M kernel).
- * Determinism: when the output tiles alone cannot fill the GPU the reduction
- * is split across CTAs and the partial sums are added into Y with fp32
- * atomics, in an order that varies between runs, so the low bits of Y can
- * differ between identical calls. The small-M kernel reduces its splits in
- * a fixed order and is bitwise repeatable. */
+ * Determinism: when the output tiles alone cannot fill the GPU, or would
+ * leave its last round of tiles partly idle, the reduction is split across
+ * CTAs and the partial sums are added into Y with fp32 atomics, in an order
+ * that varies between runs, so the low bits of Y can differ between
+ * identical calls. The small-M kernel reduces its splits in a fixed order
+ * and is bitwise repeatable. */
 nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, float* Y,
                           void* stream);
 
@@ -178,8 +179,8 @@ nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, flo
  *   dY device bf16 (raw uint16 bits) [M, rows]
  *   dX device fp32 [M, cols] (output, overwritten)
  * Requires rows % 8 == 0. Same accuracy statement as nf4_matmul_fwd, and
- * the same determinism note: split reductions (small grids, and M <= 16)
- * add partial sums with atomics. */
+ * the same determinism note: split reductions add partial sums with
+ * atomics. */
 nf4_status nf4_matmul_bwd_dx(const uint16_t* dY, int64_t M, const nf4_weight* w, float* dX,
                              void* stream);
 
