@@ -35,11 +35,12 @@
 //  * One packed byte (two adjacent weights) becomes one f16x2 fragment
 //    register through a 256-entry table held in 32 copies, one per lane, so
 //    that every lookup of a warp hits 32 distinct banks. Each CTA lays the
-//    copies out itself, by shuffles from levels held in registers. With one
-//    n-tile (up to 8 tokens) the table rows are 256 bytes apart, so that a
-//    single byte permute of the code word and the lane number gives the
-//    address of a lookup (a permute and a load per two weights); that CTA
-//    takes an SM of its own and may use up to 128 registers a thread. Int8
+//    copies out itself, by shuffles from levels held in registers. Where the
+//    shared memory allows (4-bit codes; the launcher decides) the table rows
+//    are 256 bytes apart, so that a single byte permute of the code word and
+//    the lane number gives the address of a lookup (a permute and a load per
+//    two weights); that CTA takes an SM of its own and may use up to 128
+//    registers a thread. Int8
 //    weights need no table: two bytes become an f16x2 of 1024 + (q + 128)
 //    by one byte permute with the fp16 exponent of 1024, less 1152, which is
 //    q exactly; the block scale absmax / 127 is applied after the MMA like
@@ -193,10 +194,10 @@ __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
   return (nblk * s) / slices;
 }
 
-// Shared memory. The level table comes in two layouts. Narrow (one n-tile
-// of 16 tokens, or int8 without a table): rows of 128 bytes, one 4-byte copy
-// per lane, at the start of the 1024-byte aligned region. Wide (4-bit
-// formats with one n-tile of 8 tokens, the decode case): rows of 256 bytes
+// Shared memory. The level table comes in two layouts. Narrow (where the
+// wide one does not fit, or int8 without a table): rows of 128 bytes, one
+// 4-byte copy per lane, at the start of the 1024-byte aligned region. Wide
+// (4-bit formats, when the launcher finds room): rows of 256 bytes
 // at the very start of the dynamic window, before the aligned region, so
 // that the address of a lookup, (code byte) * 256 + lane * 4, is what one
 // byte permute returns and the window offset folds into the load; the upper
@@ -220,7 +221,7 @@ __host__ __device__ constexpr int gemv_off_xs(int nt, bool wide) {
 }
 __host__ __device__ constexpr int gemv_xstride(int max_nb) { return max_nb * 128 + 8; }
 // The wide table serves one n-tile of a 4-bit format.
-__host__ __device__ constexpr bool gemv_wide(int nt, int fmt) { return nt == 1 && fmt != kFmtInt8; }
+__host__ __device__ constexpr bool gemv_wide(int nt, int fmt) { return nt <= 2 && fmt != kFmtInt8; }
 
 // Per-format constants of the small-M forward: 64-weight blocks per 128-byte
 // code box row (four of 32 bytes, or two of 64 for int8).
@@ -231,13 +232,13 @@ struct GemvFmt {
   static constexpr int kBlockBytes = kInt8 ? 64 : 32;   // code bytes of one block row
 };
 
-template <int NT, int kFmt, bool kF16>
-__global__ void __launch_bounds__(kGemvThreads, gemv_wide(NT, kFmt) ? 1 : 2)
+template <int NT, int kFmt, bool kF16, bool kWide>
+__global__ void __launch_bounds__(kGemvThreads, kWide ? 1 : 2)
 gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs p) {
   constexpr bool kInt8 = GemvFmt<kFmt>::kInt8;
   constexpr int kBoxBlocks = GemvFmt<kFmt>::kBoxBlocks;
   constexpr int kBlockBytes = GemvFmt<kFmt>::kBlockBytes;
-  constexpr bool kWide = gemv_wide(NT, kFmt);
+  static_assert(!kWide || gemv_wide(NT, kFmt), "the wide table serves the 4-bit formats");
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw + gemv_lead(kWide)) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -671,22 +672,35 @@ constexpr size_t gemv_smem_bytes(int nt, int max_nb, int xrows, bool wide) {
 constexpr size_t kGemvSmemTwoPerSm = 112 * 1024;   // two CTAs per SM
 constexpr size_t kGemvSmemLimit = 220 * 1024;
 
-template <int NT, int kFmt, bool kF16>
+// The longest slices (96 blocks) of 8 tokens always fit one narrow n-tile:
+// the small-M kernel has a launch shape for every K up to kGemvMaxCols.
+static_assert(gemv_smem_bytes(1, kMaxSliceBlocks, 8, false) <= kGemvSmemLimit, "K limit shape");
+
+template <int NT, int kFmt, bool kF16, bool kWide>
 void set_smem_limit() {
-  cudaFuncSetAttribute(gemv_fwd_kernel<NT, kFmt, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(kGemvSmemLimit));
+  cudaFuncSetAttribute(gemv_fwd_kernel<NT, kFmt, kF16, kWide>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGemvSmemLimit));
 }
 
 template <int kFmt, bool kF16>
-cudaError_t launch_gemv_as(int nt, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
+cudaError_t launch_gemv_as(int nt, bool wide, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
                            const GemvArgs& a) {
   static std::once_flag once;
   std::call_once(once, [] {
-    set_smem_limit<1, kFmt, kF16>();
-    set_smem_limit<2, kFmt, kF16>();
+    set_smem_limit<1, kFmt, kF16, false>();
+    set_smem_limit<2, kFmt, kF16, false>();
+    if constexpr (kFmt != kFmtInt8) {
+      set_smem_limit<1, kFmt, kF16, true>();
+      set_smem_limit<2, kFmt, kF16, true>();
+    }
   });
-  return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1, kFmt, kF16>, tm, a)
-                 : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16>, tm, a);
+  if constexpr (kFmt != kFmtInt8) {
+    if (wide)
+      return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1, kFmt, kF16, true>, tm, a)
+                     : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16, true>, tm, a);
+  }
+  return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1, kFmt, kF16, false>, tm, a)
+                 : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16, false>, tm, a);
 }
 
 cudaError_t launch_gemv_fwd(const MatmulCall& c) { return launch_gemv_group(&c, 1); }
@@ -715,16 +729,17 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
   a.out_bf16 = c.out_bf16 ? 1 : 0;
   a.accumulate = c.accumulate ? 1 : 0;
   a.status = c.status;
-  // Launch shape: K-slices (cluster size, a power of two <= 8) and n-tiles
-  // per CTA. Fewest waves (two CTAs per SM when they fit in shared memory,
-  // else one); among those, the fewest CTAs that still keep 70% of the SMs
-  // busy (bigger CTAs pay the prologue and the cluster barrier less often;
-  // measured faster than filling every SM with smaller ones), else the most
-  // busy SMs; then two n-tiles over one.
+  // Launch shape: K-slices (cluster size, a power of two <= 8), n-tiles per
+  // CTA and the table layout (the wide one, for 4-bit codes, when its
+  // shared memory fits, else the narrow one). Fewest waves (two CTAs per SM
+  // when they fit in shared memory, else one); among those, the fewest CTAs
+  // that still keep 70% of the SMs busy (bigger CTAs pay the prologue and the
+  // cluster barrier less often; measured faster than filling every SM with
+  // smaller ones), else the most busy SMs; then two n-tiles over one.
   const int64_t row_ctas = a.tile0[count];   // row tiles of all weights
   const int fmt = c.fmt;
-  struct Shape { int s, nt; int64_t ctas, waves, busy; size_t smem; };
-  Shape best{0, 0, 0, 0, 0, 0};
+  struct Shape { int s, nt; bool wide; int64_t ctas, waves, busy; size_t smem; };
+  Shape best{0, 0, false, 0, 0, 0, 0};
   const int64_t enough = (7 * static_cast<int64_t>(num_sms)) / 10;
   auto better = [&](const Shape& c) {
     if (best.s == 0 || c.waves != best.waves) return best.s == 0 || c.waves < best.waves;
@@ -740,23 +755,32 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
       const int nb = (a.nblk + sl - 1) / sl;
       if (nb > kMaxSliceBlocks) continue;
       for (int n = nt_hi; n >= nt_lo; --n) {
-        const size_t b = gemv_smem_bytes(n, nb, static_cast<int>(std::min<int64_t>(M, 8 * n)),
-                                         gemv_wide(n, fmt));
-        if (b > kGemvSmemLimit) continue;
-        Shape sh;
-        sh.s = sl;
-        sh.nt = n;
-        sh.smem = b;
-        sh.ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
-        const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
-        sh.waves = (sh.ctas + cap - 1) / cap;
-        sh.busy = std::min(sh.ctas, static_cast<int64_t>(num_sms));
-        if (better(sh)) best = sh;
+        // the wide table whenever it fits (two narrow CTAs sharing an SM
+        // were measured slower than wide ones one after the other)
+        bool wide_fits = false;
+        for (int w = 1; w >= 0; --w) {
+          const bool wide = w == 1;
+          if (wide && !gemv_wide(n, fmt)) continue;
+          if (!wide && wide_fits) continue;
+          const size_t b = gemv_smem_bytes(n, nb, static_cast<int>(std::min<int64_t>(M, 8 * n)),
+                                           wide);
+          if (b > kGemvSmemLimit) continue;
+          wide_fits = wide;
+          Shape sh;
+          sh.s = sl;
+          sh.nt = n;
+          sh.wide = wide;
+          sh.smem = b;
+          sh.ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
+          const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
+          sh.waves = (sh.ctas + cap - 1) / cap;
+          sh.busy = std::min(sh.ctas, static_cast<int64_t>(num_sms));
+          if (better(sh)) best = sh;
+        }
       }
     }
   };
-  // Up to 8 tokens take one n-tile (the wide table for 4-bit codes); when its
-  // shared memory does not fit (8 tokens of the longest slices), two n-tiles.
+  // Up to 8 tokens take one n-tile; if no shape fits, two.
   search(1, M <= 8 ? 1 : 2);
   if (best.s == 0 && M <= 8) search(2, 2);
   const int best_s = best.s, best_nt = best.nt;
@@ -797,12 +821,12 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   switch (c.fmt * 2 + (c.act_f16 ? 1 : 0)) {
-    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, cfg, tm, a);
-    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, cfg, tm, a);
-    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, cfg, tm, a);
-    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, cfg, tm, a);
-    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, cfg, tm, a);
-    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, cfg, tm, a);
+    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, best.wide, cfg, tm, a);
+    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, best.wide, cfg, tm, a);
+    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, best.wide, cfg, tm, a);
+    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, best.wide, cfg, tm, a);
+    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, best.wide, cfg, tm, a);
+    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, best.wide, cfg, tm, a);
   }
   return cudaErrorInvalidValue;
 }

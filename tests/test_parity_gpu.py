@@ -407,7 +407,7 @@ def test_persistent_units_with_ragged_tails(M):
 @pytest.mark.parametrize("rows,cols,M", [
     (40, 24576, 1), (40, 24576, 16), (520, 7168, 3), (520, 7168, 12), (2056, 1024, 8),
     (2056, 7168, 1), (264, 49152, 8), (1544, 3584, 16), (4104, 4096, 5), (1032, 8192, 1),
-    (8200, 1024, 1)])
+    (8200, 1024, 1), (264, 49152, 16), (136, 45056, 12), (4104, 4096, 16), (520, 4096, 9)])
 def test_fwd_small_m_launch_shapes(rows, cols, M):
     """The small-M forward over its launch shapes: with and without a
     cluster of K-slices (1 to 8), one or two n-tiles, one or two token
