@@ -433,6 +433,24 @@ class Step:
                   list(self.h_y.values()) + list(self.h_dx.values()))
         return h2d, d2h
 
+    def e2e_schedule(self, order):
+        """For weights landing in `order`: the turn (index into order) at
+        which each call runs, once every weight it reads has landed (a
+        grouped call reads several), and the turn at which each output
+        ("fwd" or "dx", projection, M) goes back: right after the call that
+        writes it."""
+        pos = {i: n for n, i in enumerate(order)}
+        projs = [c[6] if isinstance(c[6], tuple) else (c[6],) for c in self.calls]
+        turn = [max(pos[j] for j in js) for js in projs]
+        out_turn = {}
+        for c, js, t in zip(self.calls, projs, turn):
+            for kind in ("fwd", "dx"):
+                if c[0].startswith(kind + "_M"):
+                    M = int(c[0][len(kind) + 2:])
+                    for j in js:
+                        out_turn[(kind, j, M)] = t
+        return turn, out_turn
+
     def run_e2e(self):
         """One step from host inputs to host outputs, streamed by projection:
         the activations and then each weight go in on a copy stream; a
@@ -462,19 +480,7 @@ class Step:
                     ev_w[i] = torch.cuda.Event()
                     ev_w[i].record(cin)
         main.wait_event(ev_act)
-        # a call runs once every weight it reads has landed (a grouped call
-        # reads several); each output goes back right after the call that
-        # writes it
-        pos = {i: n for n, i in enumerate(order)}
-        projs = [c[6] if isinstance(c[6], tuple) else (c[6],) for c in self.calls]
-        turn = [max(pos[j] for j in js) for js in projs]
-        out_turn = {}
-        for c, js, t in zip(self.calls, projs, turn):
-            for kind in ("fwd", "dx"):
-                if c[0].startswith(kind + "_M"):
-                    M = int(c[0][len(kind) + 2:])
-                    for j in js:
-                        out_turn[(kind, j, M)] = t
+        turn, out_turn = self.e2e_schedule(order)
         for n, i in enumerate(order):
             if ev_w:
                 main.wait_event(ev_w[i])

@@ -96,3 +96,56 @@ def test_class_record_roofline():
     # memory-bound: 8 GB in 2 ms at 8000 GB/s peak is half the copy bandwidth
     r = bench.class_record(1e9, 8e9, 2e-3, pk)
     assert r["bound"] == "hbm" and abs(r["hbm_frac"] - 0.5) < 1e-12 and abs(r["roofline_frac"] - 0.5) < 1e-12
+
+
+def _call_list(name, group=True, parallel_tc=True):
+    """The call list of a workload's step without device buffers."""
+    from dequant_gemm_gb300 import workloads as wl
+    st = object.__new__(bench.Step)
+    st.nf4 = None
+    st.w = wl.WORKLOADS[name]
+    st.rotate = 1
+    st.group_small_m = group
+    st.parallel_tc = parallel_tc
+    st.x, st.y, st.dy, st.dx, st.q, st.wcopies = {}, {}, {}, {}, [[None] * 7], [[None] * 7]
+    st.calls = st._calls()
+    return st
+
+
+def test_layer_step_groups_small_m_forwards_and_counts_x_once():
+    st = _call_list("qwen2.5_7b_layer")
+    P = st.w.projections
+    m1 = [c for c in st.calls if c[0] == "fwd_M1"]
+    assert [c[6] for c in m1] == [(0, 1, 2), 3, (4, 5), 6]
+    for c in m1:
+        js = c[6] if isinstance(c[6], tuple) else (c[6],)
+        f = sum(bench.fwd_work(P[j], 1, st.w)[0] for j in js)
+        b = sum(bench.fwd_work(P[j], 1, st.w)[1] for j in js) - (len(js) - 1) * 2 * P[js[0]].cols
+        assert (c[1], c[2]) == (f, b)
+    # the same work either way
+    sep = _call_list("qwen2.5_7b_layer", group=False)
+    assert sum(c[1] for c in st.calls) == sum(c[1] for c in sep.calls)
+    assert len([c for c in sep.calls if c[0] == "fwd_M1"]) == 7
+    # tensor-core calls of an input group share a stream group tag only when parallel
+    tags = {c[5] for c in st.calls if c[0] == "fwd_M2048"}
+    serial = {c[5] for c in _call_list("qwen2.5_7b_layer", parallel_tc=False).calls
+              if c[0] == "fwd_M2048"}
+    assert len(tags) == 4 and len(serial) == 7
+
+
+def test_end_to_end_schedule_copies_every_output_once_after_its_writer():
+    st = _call_list("qwen2.5_7b_layer")
+    P = st.w.projections
+    order = sorted(range(len(P)), key=lambda i: -P[i].rows * P[i].cols)
+    turn, out_turn = st.e2e_schedule(order)
+    pos = {i: n for n, i in enumerate(order)}
+    expected = {(k, j, M) for j in range(len(P)) for k, ms in (("fwd", st.w.fwd_m), ("dx", st.w.dx_m))
+                for M in ms}
+    assert set(out_turn) == expected
+    for c, t in zip(st.calls, turn):
+        js = c[6] if isinstance(c[6], tuple) else (c[6],)
+        assert t == max(pos[j] for j in js)          # after every weight it reads has landed
+        for kind in ("fwd", "dx"):
+            if c[0].startswith(kind + "_M"):
+                for j in js:
+                    assert out_turn[(kind, j, int(c[0][len(kind) + 2:]))] >= t
