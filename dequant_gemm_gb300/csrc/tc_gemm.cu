@@ -136,7 +136,13 @@ struct Cfg {
   // buffer; the level table; the final drain
   static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+  // epilogue staging: one 16-token x 32-row fp32 box per draining warp,
+  // written out by TMA (not at 64 tokens, whose drains stay plain stores:
+  // the boxes' 32 KB there cost more than the copy engine gained, 1.5%)
+  static constexpr int kStageWarps = kBN == 64 ? 0 : kAccBufs == 2 ? kEpiWarps : kDqWarps;
+  static constexpr int kStageBoxBytes = 16 * 32 * 4;
+  static constexpr int kOffStage = (kOffMisc + 16 + 127) & ~127;
+  static constexpr int kSmemBytes = kOffStage + kStageWarps * kStageBoxBytes + 1024;   // + slack
   static_assert(kDx || kTmemA0 + 32 * kStages <= kTmemCols, "tensor memory columns");
   static_assert(kOffA % 1024 == 0 && kOffCodes % 1024 == 0, "swizzled tiles");
   static_assert(kBN == 64 || kBN == 128 || kBN == 256, "token tile");
@@ -168,6 +174,7 @@ struct TcArgs {
   int atomic_out;
   int out_bf16;
   int accumulate;
+  int out_mode;            // 0: TMA store; 1: TMA add (fp32, split or accumulating); 2: plain stores
   long long mma_wait_limit;
   int* status;
 };
@@ -269,7 +276,7 @@ __device__ __noinline__ void store_out16(void* out, int64_t i0, int64_t nd, int 
 template <bool kDx, int kBN, bool kF16, bool kInt8>
 __global__ void __launch_bounds__(Cfg<kDx, kBN, kInt8>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
-               const TcArgs p) {
+               const __grid_constant__ CUtensorMap tm_out, const TcArgs p) {
   using C = Cfg<kDx, kBN, kInt8>;
   constexpr bool kPair = C::kPair;
   constexpr int kCg = C::kCg;
@@ -378,7 +385,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
   const int tile_row = 32 * q + lane;
 
   // Drain accumulator buffer b of unit t (16-column chunks c0, c0 + step, ...
-  // of this warp's lane quarter) into the outputs.
+  // of this warp's lane quarter) into the outputs. The TMA modes stage each
+  // chunk (16 tokens x the quarter's 32 rows) in the warp's shared-memory
+  // box and let one lane store (or add) it: the warp goes on while the copy
+  // engine writes, rather than holding its stores in flight, and rows or
+  // tokens past the output's end are dropped by the copy.
+  const int stage_slot =
+      C::kStageWarps > 0 ? max(0, warp - (kAccBufs == 2 ? C::kFirstEpiWarp : 2)) % C::kStageWarps : 0;
+  uint8_t* stage_box = smem + C::kOffStage + stage_slot * C::kStageBoxBytes;
+  const uint32_t stage_addr = tc::smem_addr(stage_box);
   auto drain = [&](const Unit& t, int b, int c0, int step) {
     const int64_t rg = t.r0 + tile_row;
     const int64_t nd = kDx ? p.K : p.N;
@@ -387,6 +402,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       uint32_t v[16];
       tc::tmem_ld16(tmem + lane_base + static_cast<uint32_t>(b * kBN + c), v);
       tc::tmem_wait_ld();
+      if (p.out_mode != 2) {
+        // the box's previous contents have been read by their copy
+        if (lane == 0) tc::bulk_wait_read_all();
+        __syncwarp();
+        if (p.out_bf16) {
+          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_box);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        } else {
+          float* sf = reinterpret_cast<float*>(stage_box);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sf[j * 32 + lane] = __uint_as_float(v[j]);
+        }
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t x = static_cast<int32_t>(t.r0 + 32 * q);
+          const int32_t y = static_cast<int32_t>(t.m0 + c);
+          if (p.out_mode == 0) tc::tma_store_2d(&tm_out, stage_addr, x, y);
+          else tc::tma_reduce_add_2d(&tm_out, stage_addr, x, y);
+          tc::bulk_commit();
+        }
+        continue;
+      }
       // one output mode per launch: the branch stays outside the stores
       const int nm = vrow ? static_cast<int>(min(static_cast<int64_t>(16), p.M - (t.m0 + c))) : 0;
       float* of = reinterpret_cast<float*>(p.out) + (t.m0 + c) * nd + rg;
@@ -729,6 +768,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     }
   }
 
+  // The epilogue's output copies have landed before the CTA leaves.
+  if (lane == 0) tc::bulk_wait_all();
   // On a pair, neither CTA frees its tensor memory or leaves (its barriers
   // take the peer's arrivals) before both are done.
   tc::fence_before_sync();
@@ -802,6 +843,11 @@ cudaError_t launch_tc(const MatmulCall& c) {
   a.stages_per_split = (a.stages_total + splits - 1) / splits;
   splits = (a.stages_total + a.stages_per_split - 1) / a.stages_per_split;
   a.atomic_out = splits > 1 ? 1 : 0;
+  // outputs: TMA store, or TMA add (fp32) into a zeroed output for splits and
+  // into the caller's for accumulate (2-5% faster than plain stores at 128
+  // and 256 tokens); a bf16 output that accumulates keeps plain
+  // read-modify-write stores, and so do 64-token tiles (no staging boxes)
+  a.out_mode = C::kStageWarps == 0 ? 2 : (a.atomic_out || c.accumulate) ? (c.out_bf16 ? 2 : 1) : 0;
   a.row_units = static_cast<int>(row_units);
   a.m_tiles = static_cast<int>(m_tiles);
   const int64_t units = row_units * m_tiles * splits;
@@ -829,6 +875,13 @@ cudaError_t launch_tc(const MatmulCall& c) {
   if (!encode_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.codes, row_bytes,
                  static_cast<uint64_t>(N), row_bytes, box_x, box_y, sw))
     return cudaErrorInvalidValue;
+  // outputs: [M, nd] fp32 or bf16, box 32 tile rows x 16 tokens, no swizzle
+  CUtensorMap tm_out;
+  const uint64_t out_elem = c.out_bf16 ? 2 : 4;
+  if (!encode_2d(&tm_out, c.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                 c.out, static_cast<uint64_t>(nd), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(nd) * out_elem, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
 
   static std::once_flag once;
   std::call_once(once, [] {
@@ -853,10 +906,11 @@ cudaError_t launch_tc(const MatmulCall& c) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kDx, kBN, kF16, kInt8>, tm_act, tm_codes, a);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kDx, kBN, kF16, kInt8>, tm_act, tm_codes, tm_out,
+                              a);
   } else {
-    tc_gemm_kernel<kDx, kBN, kF16, kInt8><<<grid, C::kThreads, C::kSmemBytes, c.st>>>(tm_act,
-                                                                                   tm_codes, a);
+    tc_gemm_kernel<kDx, kBN, kF16, kInt8><<<grid, C::kThreads, C::kSmemBytes, c.st>>>(
+        tm_act, tm_codes, tm_out, a);
     return cudaGetLastError();
   }
 }
