@@ -619,6 +619,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     const int ao = (2 * (rr >> 3) + h) * 1024 + (rr & 7) * 128;
     const int asw = rr & 7;
     int gs = 0, k = 0;
+    // With a single accumulator buffer these warps drain it, the four warps
+    // of each lane quarter sharing out its 16-column chunks. Unit k's drain
+    // waits until each group has dequantized its first stage of unit k + 1
+    // (or found it has none): the MMAs of unit k + 1 then find four stages
+    // ready when the buffer is free, instead of waiting for the dequant to
+    // restart after the drain. Safe to defer: a group's first stage of a
+    // unit needs only copies and slots freed by earlier units' MMAs.
+    bool pend = false;
+    Unit pend_t{};
+    int pend_k = 0;
+    auto drain_pending = [&]() {
+      pend = false;
+      if (*abort_flag) return false;
+      if (!waited(tc::mbar_wait_abortable(accf_bar(0), pend_k & 1, abort_flag), kRoleEpilogue))
+        return false;
+      tc::fence_after_sync();
+      drain(pend_t, 0, 16 * ((warp - 2) >> 2), 64);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_acce(0);
+      return true;
+    };
+    bool drained_ok = true;
     for (int u = cid; u < p.units; u += ncl, ++k) {
       if (*abort_flag) break;
       const Unit t = unit_at(u);
@@ -649,7 +672,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       int i = ((grp - gs % kGroups) + kGroups) % kGroups;   // this group's first stage of the unit
       load_scale(i);
       wait_lut();
+      bool first = true;
       for (; i < t.nst; i += kGroups) {
+        if constexpr (kAccBufs == 1) {
+          if (!first && pend && !(drained_ok = drain_pending())) break;
+          first = false;
+        }
         const int g = gs + i;                 // the stage's index across units
         const int slot = g % kStages;
         const uint32_t ph = (g / kStages) & 1;
@@ -736,18 +764,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       }
       gs += t.nst;
       if constexpr (kAccBufs == 1) {
-        // The only accumulator buffer: these warps drain it (the four warps
-        // of each lane quarter share out its 16-column chunks) before they go
-        // on to the next unit, whose copies are already under way.
-        if (*abort_flag) break;
-        if (!waited(tc::mbar_wait_abortable(accf_bar(0), k & 1, abort_flag), kRoleEpilogue)) break;
-        tc::fence_after_sync();
-        drain(t, 0, 16 * ((warp - 2) >> 2), 64);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) arrive_acce(0);
+        if (!drained_ok || (pend && !drain_pending())) break;   // fewer than two stages here
+        pend = true;
+        pend_t = t;
+        pend_k = k;
       }
     }
+    if constexpr (kAccBufs == 1)
+      if (drained_ok && pend) drain_pending();   // the last unit
     wait_lut();   // a CTA with no unit still lets the table copy land
   } else if constexpr (kAccBufs == 2) {
     // ----------------------------------------------------------- epilogue --
