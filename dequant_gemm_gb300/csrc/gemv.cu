@@ -63,16 +63,15 @@
 namespace nf4 {
 namespace {
 
-constexpr int kGemvRows = 128;                  // weight rows per CTA
-constexpr int kRowGroups = 8;                   // 16 rows each
-constexpr int kGemvWarps = 2 * kRowGroups;      // two K-halves per row group
+constexpr int kGemvWarps = 16;                  // row groups x K-parts
+constexpr int kMaxRowGroups = 8;                // of 16 rows each
+constexpr int kGemvRows = 16 * kMaxRowGroups;   // most weight rows per CTA
 constexpr int kGemvThreads = 32 * kGemvWarps;
 constexpr int kBoxBytes = 16 * 128;             // 16 rows x 128 bytes
 constexpr int kWarpSlots = 2;                   // code boxes in flight per warp
 constexpr int kTabBytes = kHalfPairTableBytes;
 constexpr int kMaxSliceBlocks = 96;
 constexpr int kMaxCluster = 8;
-constexpr int kOutStride = kGemvRows + 4;       // floats, keeps rows 16-byte aligned
 static_assert(kMaxCluster * kMaxSliceBlocks * kBlock == kGemvMaxCols, "K limit");
 
 // fp16 bits of level i (0 <= i < 16) of a 4-bit format as a select tree
@@ -232,7 +231,7 @@ struct GemvFmt {
   static constexpr int kBlockBytes = kInt8 ? 64 : 32;   // code bytes of one block row
 };
 
-template <int NT, int kFmt, bool kF16, bool kWide>
+template <int NT, int kFmt, bool kF16, bool kWide, int kR>
 __global__ void __launch_bounds__(kGemvThreads, kWide ? 1 : 2)
 gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs p) {
   constexpr bool kInt8 = GemvFmt<kFmt>::kInt8;
@@ -251,11 +250,14 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int rgp = warp & (kRowGroups - 1), kh = warp / kRowGroups;
-  // K-half hand-off of row group rgp: the first slot of warp rgp + 8, free
-  // once that warp has consumed its last box
-  float* red = reinterpret_cast<float*>(smem + gemv_off_slots(kWide) +
-                                       (rgp + kRowGroups) * kWarpSlots * kBoxBytes);
+  // warp = row group rgp of kR (16 rows each) x K-part kp of kP = 16 / kR
+  constexpr int kP = kGemvWarps / kR, kRowsCta = 16 * kR;
+  const int rgp = warp % kR, kp = warp / kR;
+  // K-part hand-off: warp w's partial sums go through its own first code
+  // slot, free once it has consumed its last box
+  auto red_of = [&](int w) {
+    return reinterpret_cast<float*>(smem + gemv_off_slots(kWide) + w * kWarpSlots * kBoxBytes);
+  };
   // this CTA's weight of the group (selects on static indices, so the
   // parameter arrays stay in parameter space)
   int gi = 0;
@@ -278,14 +280,14 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
 #pragma unroll
   for (int q = 1; q < kGemvGroupMax; ++q)
     if (gi == q) tile_first = p.tile0[q];
-  const int64_t row0 = static_cast<int64_t>(static_cast<int>(blockIdx.x) - tile_first) * kGemvRows;
+  const int64_t row0 = static_cast<int64_t>(static_cast<int>(blockIdx.x) - tile_first) * kRowsCta;
   const int slice = blockIdx.y;
   const int kb0 = slice_begin(p.nblk, p.slices, slice);
   const int nb = slice_begin(p.nblk, p.slices, slice + 1) - kb0;
   const int nboxes = (nb + kBoxBlocks - 1) / kBoxBlocks;
   const int64_t m0 = static_cast<int64_t>(blockIdx.z) * 8 * NT;
   const int mt = static_cast<int>(min(static_cast<int64_t>(8 * NT), p.M - m0));
-  // this warp's code slots and their mbarriers; it takes boxes kh, kh + 2, ...
+  // this warp's code slots and their mbarriers; it takes boxes kp, kp + kP, ...
   const uint32_t slots = tc::smem_addr(smem + gemv_off_slots(kWide)) + warp * kWarpSlots * kBoxBytes;
   const uint32_t bars = tc::smem_addr(smem + gemv_off_bars(kWide)) + warp * kWarpSlots * 8;
 
@@ -302,13 +304,13 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
     // where the launch is latency-bound: on long slices the prefetch competes
     // with demand loads and was measured slower (35 MB weights, 4% slower
     // even with the first four boxes only).
-    const int nmine_pf = (nboxes - kh + 1) / 2;
+    const int nmine_pf = (nboxes - kp + kP - 1) / kP;
     if (lane == 0 && nmine_pf <= kWarpSlots && row0 + rgp * 16 < N)   // boxes inside the weight
       for (int i = 0; i < nmine_pf; ++i)
-        tma_prefetch_2d(tm_codes, (kb0 + kBoxBlocks * (kh + 2 * i)) * kBlockBytes,
+        tma_prefetch_2d(tm_codes, (kb0 + kBoxBlocks * (kp + kP * i)) * kBlockBytes,
                             static_cast<int32_t>(row0 + rgp * 16));
     const int64_t pr = row0 + rgp * 16 + lane;
-    if (kh == 0 && lane < 16 && pr < N && nb > 0 && nmine_pf <= kWarpSlots) {
+    if (kp == 0 && lane < 16 && pr < N && nb > 0 && nmine_pf <= kWarpSlots) {
       const int64_t ia = pr * p.nblk + kb0;
       if constexpr (kInt8) {
         prefetch_l2(scale + ia);
@@ -373,15 +375,15 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
     }
   }
 
-  // Box i of this warp (the slice's box kh + 2 i) goes into slot i % kWarpSlots, by
+  // Box i of this warp (the slice's box kp + kP i) goes into slot i % kWarpSlots, by
   // TMA; its absmax codes and scales travel alongside: lane e loads those of
   // row pair (e & 7, (e & 7) + 8) of block e >> 3 of the box.
-  const int nmine = (nboxes - kh + 1) / 2;   // boxes of this warp
+  const int nmine = (nboxes - kp + kP - 1) / kP;   // boxes of this warp
   const int64_t ar = row0 + rgp * 16 + (lane & 7);
   const bool ar_ok = ar < N, br_ok = ar + 8 < N;
   auto issue_box = [&](int i) {
     if (lane == 0) {
-      const int b = kh + 2 * i;
+      const int b = kp + kP * i;
       const uint32_t bar = bars + 8u * (i % kWarpSlots);
       tc::mbar_arrive_expect_tx(bar, kBoxBytes);
       tc::tma_load_2d(slots + (i % kWarpSlots) * kBoxBytes, tm_codes,
@@ -392,7 +394,7 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
   // 4-bit: absmax codes qa, qb and scales sa, sb; int8: the block absmax in
   // sa, sb (qa, qb unused)
   auto load_scales = [&](int i, uint32_t& qa, uint32_t& qb, float& sa, float& sb) {
-    const int j = (kh + 2 * i) * kBoxBlocks + (lane >> 3);
+    const int j = (kp + kP * i) * kBoxBlocks + (lane >> 3);
     const bool in = i < nmine && j < nb && (lane >> 3) < kBoxBlocks;
     const int64_t ia = ar * p.nblk + kb0 + j, ib = ia + 8 * p.nblk;
     if constexpr (kInt8) {
@@ -484,7 +486,7 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
     // warp-uniform outcome: the lanes leave together or go on together
     const bool got = tc::mbar_wait(bars + 8u * sl, (i / kWarpSlots) & 1);
     if (!__all_sync(0xffffffffu, got)) return false;
-    const int b = kh + 2 * i;
+    const int b = kp + kP * i;
     const uint8_t* sg = slot_g + sl * kBoxBytes;
 #pragma unroll
     for (int jj = 0; jj < kBoxBlocks; ++jj) {
@@ -579,15 +581,16 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
         tc::mbar_wait(bars + 8u * (i % kWarpSlots), (i / kWarpSlots) & 1);
   }
 
-  // The second K-half of each row group hands its sums to the first.
-  if (kh == 1) {
+  // K-parts 1 .. kP-1 of each row group hand their sums to K-part 0.
+  if (kp > 0) {
+    float* red = red_of(warp);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
       *reinterpret_cast<float4*>(red + (lane * NT + nt) * 4) =
           make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   }
   __syncthreads();
-  // Undo the token scales; the first K-half holds the row group's sums.
+  // Undo the token scales; K-part 0 holds the row group's sums.
   float inv0[NT], inv1[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -595,20 +598,32 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
     inv0[nt] = tk0 < mt ? xinv[tk0] : 0.0f;
     inv1[nt] = tk0 + 1 < mt ? xinv[tk0 + 1] : 0.0f;
   }
-  if (kh == 0) {
+  if (kp == 0) {
+#pragma unroll
+    for (int q = 1; q < kP; ++q) {
+      const float* red = red_of(rgp + kR * q);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float4 o = *reinterpret_cast<const float4*>(red + (lane * NT + nt) * 4);
+        acc[nt][0] += o.x;
+        acc[nt][1] += o.y;
+        acc[nt][2] += o.z;
+        acc[nt][3] += o.w;
+      }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float4 o = *reinterpret_cast<const float4*>(red + (lane * NT + nt) * 4);
-      acc[nt][0] = (acc[nt][0] + o.x) * inv0[nt];
-      acc[nt][1] = (acc[nt][1] + o.y) * inv1[nt];
-      acc[nt][2] = (acc[nt][2] + o.z) * inv0[nt];
-      acc[nt][3] = (acc[nt][3] + o.w) * inv1[nt];
+      acc[nt][0] *= inv0[nt];
+      acc[nt][1] *= inv1[nt];
+      acc[nt][2] *= inv0[nt];
+      acc[nt][3] *= inv1[nt];
     }
   }
   if (p.slices == 1) {
-    // stage [8 NT tokens x 128 rows] over the level table, then float4 stores
+    // stage [8 NT tokens x 16 kR rows] over the level table, then float4 stores
     float* out_s = reinterpret_cast<float*>(tab);
-    if (kh == 0) {
+    constexpr int kOutStride = kRowsCta + 4;   // floats, keeps rows 16-byte aligned
+    if (kp == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int tk0 = nt * 8 + 2 * t, tk1 = tk0 + 1;
@@ -620,8 +635,8 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
       }
     }
     __syncthreads();
-    for (int i = tid; i < 8 * NT * (kGemvRows / 4); i += kGemvThreads) {
-      const int tk = i / (kGemvRows / 4), r4 = (i % (kGemvRows / 4)) * 4;
+    for (int i = tid; i < 8 * NT * (kRowsCta / 4); i += kGemvThreads) {
+      const int tk = i / (kRowsCta / 4), r4 = (i % (kRowsCta / 4)) * 4;
       if (tk < mt && row0 + r4 < N)
         store_out4(Y, (m0 + tk) * N + row0 + r4,
                    *reinterpret_cast<const float4*>(out_s + tk * kOutStride + r4), p.out_bf16,
@@ -632,10 +647,10 @@ gemv_fwd_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ G
     // of the row tile. Every CTA stores its partial of those rows into the
     // owner's inbox slot for its slice, one cluster barrier makes the stores
     // visible, and each owner sums its slots and writes Y once.
-    const int rpc = kGemvRows / p.slices;          // rows owned per CTA (a power of two)
+    const int rpc = kRowsCta / p.slices;           // rows owned per CTA (a power of two)
     const int rpc_shift = 31 - __clz(rpc);
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer has started
-    if (kh == 0) {
+    if (kp == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int tk0 = nt * 8 + 2 * t;
@@ -676,31 +691,37 @@ constexpr size_t kGemvSmemLimit = 220 * 1024;
 // the small-M kernel has a launch shape for every K up to kGemvMaxCols.
 static_assert(gemv_smem_bytes(1, kMaxSliceBlocks, 8, false) <= kGemvSmemLimit, "K limit shape");
 
+// Row groups per CTA the kernel is built for: 8 (128 rows, 2 K-parts) or 2
+// (32 rows, 8 K-parts).
+template <int NT, int kFmt, bool kF16, bool kWide, int kR>
+cudaError_t launch_gemv_kernel(const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
+                               const GemvArgs& a) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(gemv_fwd_kernel<NT, kFmt, kF16, kWide, kR>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kGemvSmemLimit));
+  });
+  return cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<NT, kFmt, kF16, kWide, kR>, tm, a);
+}
+
 template <int NT, int kFmt, bool kF16, bool kWide>
-void set_smem_limit() {
-  cudaFuncSetAttribute(gemv_fwd_kernel<NT, kFmt, kF16, kWide>,
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGemvSmemLimit));
+cudaError_t launch_gemv_r(int r, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
+                          const GemvArgs& a) {
+  return r == 2 ? launch_gemv_kernel<NT, kFmt, kF16, kWide, 2>(cfg, tm, a)
+                : launch_gemv_kernel<NT, kFmt, kF16, kWide, kMaxRowGroups>(cfg, tm, a);
 }
 
 template <int kFmt, bool kF16>
-cudaError_t launch_gemv_as(int nt, bool wide, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
-                           const GemvArgs& a) {
-  static std::once_flag once;
-  std::call_once(once, [] {
-    set_smem_limit<1, kFmt, kF16, false>();
-    set_smem_limit<2, kFmt, kF16, false>();
-    if constexpr (kFmt != kFmtInt8) {
-      set_smem_limit<1, kFmt, kF16, true>();
-      set_smem_limit<2, kFmt, kF16, true>();
-    }
-  });
+cudaError_t launch_gemv_as(int nt, bool wide, int r, const cudaLaunchConfig_t& cfg,
+                           const GemvMaps& tm, const GemvArgs& a) {
   if constexpr (kFmt != kFmtInt8) {
     if (wide)
-      return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1, kFmt, kF16, true>, tm, a)
-                     : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16, true>, tm, a);
+      return nt == 1 ? launch_gemv_r<1, kFmt, kF16, true>(r, cfg, tm, a)
+                     : launch_gemv_r<2, kFmt, kF16, true>(r, cfg, tm, a);
   }
-  return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<1, kFmt, kF16, false>, tm, a)
-                 : cudaLaunchKernelEx(&cfg, gemv_fwd_kernel<2, kFmt, kF16, false>, tm, a);
+  return nt == 1 ? launch_gemv_r<1, kFmt, kF16, false>(r, cfg, tm, a)
+                 : launch_gemv_r<2, kFmt, kF16, false>(r, cfg, tm, a);
 }
 
 cudaError_t launch_gemv_fwd(const MatmulCall& c) { return launch_gemv_group(&c, 1); }
@@ -713,47 +734,69 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
   GemvArgs a = {};
   a.X = static_cast<const uint16_t*>(c.act);
   a.count = count;
-  a.tile0[0] = 0;
   for (int i = 0; i < kGemvGroupMax; ++i) {
     const MatmulCall& ci = cs[i < count ? i : 0];
     a.a8[i] = ci.a8;
     a.scale[i] = ci.scale;
     a.Y[i] = ci.out;
     a.N[i] = ci.N;
-    const int64_t tiles = i < count ? (ci.N + kGemvRows - 1) / kGemvRows : 0;
-    a.tile0[i + 1] = a.tile0[i] + static_cast<int>(tiles);
   }
+  // row tiles of all weights for CTAs of r row groups (16 r rows)
+  auto row_tiles = [&](int r) {
+    int64_t n = 0;
+    for (int i = 0; i < count; ++i) n += (cs[i].N + 16 * r - 1) / (16 * r);
+    return n;
+  };
   a.M = M;
   a.K = K;
   a.nblk = static_cast<int>(K / kBlock);
   a.out_bf16 = c.out_bf16 ? 1 : 0;
   a.accumulate = c.accumulate ? 1 : 0;
   a.status = c.status;
-  // Launch shape: K-slices (cluster size, a power of two <= 8), n-tiles per
-  // CTA and the table layout (the wide one, for 4-bit codes, when its
-  // shared memory fits, else the narrow one). Fewest waves (two CTAs per SM
-  // when they fit in shared memory, else one); among those, the fewest CTAs
-  // that still keep 70% of the SMs busy (bigger CTAs pay the prologue and the
+  // Launch shape: row groups per CTA (8: 128 rows whose 2 K-parts meet in
+  // shared memory; 2: 32 rows, 8 K-parts), K-slices across a cluster (a
+  // power of two <= 8, reducing through distributed shared memory), n-tiles
+  // per CTA and the table layout (the wide one, for 4-bit codes, when its
+  // shared memory fits, else the narrow one). In order: fewest waves (two
+  // CTAs per SM when they fit in shared memory, else one); a code box for
+  // every K-part; a grid that keeps 70% of the SMs busy over one that does
+  // not; the fewest token tiles; the smaller activation slice per CTA, all
+  // up to 16 KB counting alike (it is staged before the first MMA); no
+  // cluster over a cluster (its barrier and remote stores cost about a
+  // microsecond); the fewest CTAs (bigger CTAs pay the prologue and the
   // cluster barrier less often; measured faster than filling every SM with
-  // smaller ones), else the most busy SMs; then two n-tiles over one.
-  const int64_t row_ctas = a.tile0[count];   // row tiles of all weights
+  // smaller ones), else the most busy SMs; two n-tiles over one. (Measured:
+  // one 32-row CTA per SM over the full K is 7-11% faster than 128-row CTAs
+  // in 4-slice clusters for 3584 x 3584 and 4096 x 4096 at one token.)
   const int fmt = c.fmt;
-  struct Shape { int s, nt; bool wide; int64_t ctas, waves, busy; size_t smem; };
-  Shape best{0, 0, false, 0, 0, 0, 0};
+  struct Shape {
+    int s, nt, r;
+    bool wide, parts_busy;
+    int64_t mtiles, x_cost, ctas, waves, busy;
+    size_t smem;
+  };
+  Shape best{0, 0, 0, false, false, 0, 0, 0, 0, 0, 0};
   const int64_t enough = (7 * static_cast<int64_t>(num_sms)) / 10;
   auto better = [&](const Shape& c) {
-    if (best.s == 0 || c.waves != best.waves) return best.s == 0 || c.waves < best.waves;
+    if (best.s == 0) return true;
+    if (c.waves != best.waves) return c.waves < best.waves;
+    if (c.parts_busy != best.parts_busy) return c.parts_busy;
     const bool ce = c.busy >= enough, be = best.busy >= enough;
     if (ce != be) return ce;
+    if (c.mtiles != best.mtiles) return c.mtiles < best.mtiles;
+    if (c.x_cost != best.x_cost) return c.x_cost < best.x_cost;
+    if (ce && (c.s > 1) != (best.s > 1)) return c.s == 1;
     if (ce && c.ctas != best.ctas) return c.ctas < best.ctas;
     if (!ce && c.busy != best.busy) return c.busy > best.busy;
     return c.nt > best.nt;
   };
   auto search = [&](int nt_lo, int nt_hi) {
+   for (int r : {kMaxRowGroups, 2}) {
+    const int64_t row_ctas = row_tiles(r);
     for (int sl = kMaxCluster; sl >= 1; sl /= 2) {
       if (sl > a.nblk) continue;
       const int nb = (a.nblk + sl - 1) / sl;
-      if (nb > kMaxSliceBlocks) continue;
+      if (nb > kMaxSliceBlocks && r == kMaxRowGroups) continue;
       for (int n = nt_hi; n >= nt_lo; --n) {
         // the wide table whenever it fits (two narrow CTAs sharing an SM
         // were measured slower than wide ones one after the other)
@@ -769,9 +812,16 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
           Shape sh;
           sh.s = sl;
           sh.nt = n;
+          sh.r = r;
           sh.wide = wide;
           sh.smem = b;
-          sh.ctas = row_ctas * sl * ((M + 8 * n - 1) / (8 * n));
+          sh.mtiles = (M + 8 * n - 1) / (8 * n);
+          sh.ctas = row_ctas * sl * sh.mtiles;
+          // every K-part has a code box; the activation slice a CTA stages
+          // stays small (it is on the critical path before the first MMA)
+          const int box_blocks = fmt == kFmtInt8 ? 2 : 4;
+          sh.parts_busy = (nb + box_blocks - 1) / box_blocks >= kGemvWarps / r;
+          sh.x_cost = std::max<int64_t>(std::min<int64_t>(M, 8 * n) * nb * 128, 16 * 1024);
           const int64_t cap = (b <= kGemvSmemTwoPerSm ? 2 : 1) * static_cast<int64_t>(num_sms);
           sh.waves = (sh.ctas + cap - 1) / cap;
           sh.busy = std::min(sh.ctas, static_cast<int64_t>(num_sms));
@@ -779,6 +829,7 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
         }
       }
     }
+   }
   };
   // Up to 8 tokens take one n-tile; if no shape fits, two.
   search(1, M <= 8 ? 1 : 2);
@@ -788,6 +839,13 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
   if (best_s == 0) return cudaErrorInvalidValue;
   a.slices = best_s;
   a.max_nb = (a.nblk + best_s - 1) / best_s;
+  a.tile0[0] = 0;
+  for (int i = 0; i < kGemvGroupMax; ++i) {
+    const int64_t rows_cta = 16 * best.r;
+    const int64_t tiles = i < count ? (cs[i].N + rows_cta - 1) / rows_cta : 0;
+    a.tile0[i + 1] = a.tile0[i] + static_cast<int>(tiles);
+  }
+  const int64_t row_ctas = a.tile0[count];   // row tiles of all weights
   const int nt = best_nt;
   const int64_t mtiles = (M + 8 * nt - 1) / (8 * nt);
   // A grid of at most one CTA per SM asks for more shared memory than two
@@ -821,12 +879,12 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   switch (c.fmt * 2 + (c.act_f16 ? 1 : 0)) {
-    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, best.wide, cfg, tm, a);
-    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, best.wide, cfg, tm, a);
-    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, best.wide, cfg, tm, a);
-    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, best.wide, cfg, tm, a);
-    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, best.wide, cfg, tm, a);
-    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, best.wide, cfg, tm, a);
+    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, best.wide, best.r, cfg, tm, a);
+    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, best.wide, best.r, cfg, tm, a);
+    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, best.wide, best.r, cfg, tm, a);
+    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, best.wide, best.r, cfg, tm, a);
+    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, best.wide, best.r, cfg, tm, a);
+    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, best.wide, best.r, cfg, tm, a);
   }
   return cudaErrorInvalidValue;
 }
