@@ -6,12 +6,14 @@
 // activations bf16 or fp16; outputs fp32 or bf16, overwritten or added to.
 //
 // Forward design (HBM-bound: 0.516 B of weight per 2*M flops):
-//  * CTA = 16 warps = 8 row groups of 16 weight rows (128 rows) x 2 halves of
-//    one K-slice. The two warps of a row group reduce through shared memory;
-//    the S K-slices of the same rows form a thread-block cluster and reduce
-//    through distributed shared memory, so every output is written once with
-//    a plain store (no zeroing pass, no atomics). The number of slices keeps
-//    the grid within one wave of two CTAs per SM.
+//  * CTA = 16 warps = R row groups of 16 weight rows x 16 / R parts of one
+//    K-slice (R = 8: 128 rows, 2 K-parts; R = 2: 32 rows, 8 K-parts), the
+//    K-parts taking the slice's code boxes in turn and reducing through
+//    shared memory. When the rows alone give too few CTAs, S K-slices of the
+//    same rows form a thread-block cluster and reduce through distributed
+//    shared memory. Every output is written once with a plain store (no
+//    zeroing pass, no atomics). The launcher picks R, S, the n-tiles and the
+//    table layout (see launch_gemv_group).
 //  * Every warp streams its own codes: lane 0 issues 2-D TMA boxes of 16 rows
 //    x 128 bytes (four 64-weight blocks, 128-byte swizzled) into two private
 //    shared-memory slots with one mbarrier each, so warps never wait for one
