@@ -207,5 +207,4 @@ cudaError_t launch_gemv_fwd(const MatmulCall& c);
 cudaError_t launch_gemv_group(const MatmulCall* cs, int count);
 cudaError_t launch_tc_fwd(const MatmulCall& c);
 cudaError_t launch_tc_dx(const MatmulCall& c);
-cudaError_t launch_simt_dx(const MatmulCall& c);
 }  // namespace nf4

@@ -204,7 +204,7 @@ __host__ __device__ constexpr int slice_begin(int nblk, int slices, int s) {
 // byte permute returns and the window offset folds into the load; the upper
 // 128 bytes of each row stay unused. Then, from the aligned base: code slots
 // (per warp, 1024-byte aligned for the swizzle; after the main loop a
-// second-K-half warp's first slot carries its sums to the first K-half),
+// warp of K-part 1 and up hands its sums to K-part 0 through its first slot),
 // mbarriers, token scales, per-warp max |x|, the cluster reduction inbox and
 // the fp16 activation slice (rows of max_nb * 128 + 8 bytes: the 8 keeps the
 // B fragment loads of 8 token rows on distinct banks).
