@@ -102,26 +102,10 @@ constexpr uint32_t level_to_f16(uint32_t b) {
   return sign | h;
 }
 
-// Level pair table indexed by a code byte, in 32 lane-private copies so that
-// any 32 lookups of a warp hit 32 distinct banks: entry b of copy l is word
-// 32 b + l, whose low half is the fp16 level of the high nibble (the
-// lower-index element of the pair) and whose high half is the level of the
-// low nibble. Each kernel file instantiates its own copy in device memory and
-// brings it into shared memory with one bulk copy per CTA.
-constexpr int kHalfPairTableBytes = 256 * 32 * 4;
-struct HalfPairTable {
-  uint32_t w[256 * 32];
-};
-
-constexpr HalfPairTable make_half_pair_table(int fmt = kFmtNf4) {
-  HalfPairTable t{};
-  const uint32_t (&lv)[16] = level_bits(fmt);
-  for (int i = 0; i < 256 * 32; ++i) {
-    const int b = i >> 5;
-    t.w[i] = level_to_f16(lv[b >> 4]) | (level_to_f16(lv[b & 15]) << 16);
-  }
-  return t;
-}
+// Bytes of a shared-memory level pair table indexed by a code byte: fp16
+// pairs in 32 copies (the GEMV's narrow table) or fp32 pairs in 16 copies
+// (the tensor-core dequant), either way 8 KB per 256 entries x 32 words.
+constexpr int kPairTableBytes = 256 * 32 * 4;
 
 // Device status word values (the library's nf4_status codes).
 constexpr int kStatusTimeout = NF4_ERR_DEVICE_TIMEOUT;

@@ -71,7 +71,7 @@ constexpr int kGemvRows = 16 * kMaxRowGroups;   // most weight rows per CTA
 constexpr int kGemvThreads = 32 * kGemvWarps;
 constexpr int kBoxBytes = 16 * 128;             // 16 rows x 128 bytes
 constexpr int kWarpSlots = 2;                   // code boxes in flight per warp
-constexpr int kTabBytes = kHalfPairTableBytes;
+constexpr int kTabBytes = kPairTableBytes;
 constexpr int kMaxSliceBlocks = 96;
 constexpr int kMaxCluster = 8;
 static_assert(kMaxCluster * kMaxSliceBlocks * kBlock == kGemvMaxCols, "K limit");

@@ -33,10 +33,12 @@
 //
 // Both directions walk the weight along its rows, one thread per (row, 64
 // columns) run, which is one absmax block. A 4-bit code byte gives both
-// levels from one lookup in a 256-entry fp16 level pair table kept in 32
-// lane-private copies (every lookup of a warp hits 32 distinct banks); an
-// int8 byte is converted directly. Either is widened to fp32 and multiplied
-// by the block's dequantized absmax (for int8, absmax / 127), a register.
+// levels from one 8-byte lookup in a 256-entry fp32 level pair table kept
+// in 16 copies (each half-warp's lookups hit 32 distinct banks; measured 1%
+// faster than fp16 pairs in 32 copies, which need widening, and the levels
+// are then exact); an int8 byte is converted directly. Either is multiplied
+// in fp32 by the block's dequantized absmax (for int8, absmax / 127), a
+// register, and rounded to the operand type.
 //
 // Forward: the tile is 128 weight rows, the reduction runs along a row, so a
 // thread's run is K-contiguous and goes straight into tensor memory (one
@@ -126,7 +128,7 @@ struct Cfg {
   // arrivals that free an accumulator buffer: the epilogue warps, or with a
   // single buffer the dequant warps that drain it, of both CTAs of a pair
   static constexpr int kDrainWarps = kAccBufs == 2 ? kEpiWarps : kDqWarps;
-  static constexpr int kLutBytes = kInt8 ? 0 : kHalfPairTableBytes;
+  static constexpr int kLutBytes = kInt8 ? 0 : kPairTableBytes;
   static constexpr int kOffAct = 0;
   static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
   static constexpr int kOffCodes = kOffA + kASlots * kAStageBytes;
@@ -186,9 +188,23 @@ struct Unit {
   int s_begin, nst;        // reduction stages
 };
 
-// Level pair tables of the 4-bit formats (fp16 levels, layout in common.cuh).
-__device__ __align__(128) const HalfPairTable kHalfPairsNf4 = make_half_pair_table(kFmtNf4);
-__device__ __align__(128) const HalfPairTable kHalfPairsFp4 = make_half_pair_table(kFmtFp4);
+// Level pair tables of the 4-bit formats: the fp32 levels of both nibbles
+// of every code byte (the even element's level first), in 16 copies: entry
+// (byte b, copy c) at (16 b + c) * 8 bytes.
+struct FloatPairTable { uint32_t w[256 * 16 * 2]; };
+constexpr FloatPairTable make_float_pair_table(int fmt) {
+  FloatPairTable t{};
+  const uint32_t (&lv)[16] = level_bits(fmt);
+  for (int b = 0; b < 256; ++b)
+    for (int c = 0; c < 16; ++c) {
+      t.w[(b * 16 + c) * 2] = lv[b >> 4];
+      t.w[(b * 16 + c) * 2 + 1] = lv[b & 15];
+    }
+  return t;
+}
+static_assert(sizeof(FloatPairTable) == kPairTableBytes, "table size");
+__device__ __align__(128) const FloatPairTable kPairsNf4 = make_float_pair_table(kFmtNf4);
+__device__ __align__(128) const FloatPairTable kPairsFp4 = make_float_pair_table(kFmtFp4);
 
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
@@ -212,7 +228,8 @@ __device__ __forceinline__ uint32_t pack_operand(float lo, float hi) {
 }
 
 // 16 code bytes of a 4-bit format (32 weights) -> 16 packed operand words.
-// tab is this lane's copy of the level pair table (entries 128 bytes apart).
+// tab is this lane's copy of the level pair table (copy lane % 16; entries
+// 128 bytes apart).
 template <bool kF16>
 __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab, float2 ahat2,
                                                uint32_t (&v)[16]) {
@@ -222,8 +239,7 @@ __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const uint32_t byte = __byte_perm(words[j], 0u, 0x4440u + b);
-      const __half2 h2 = *reinterpret_cast<const __half2*>(tab + (byte << 7));
-      const float2 lv = __fmul2_rn(__half22float2(h2), ahat2);
+      const float2 lv = __fmul2_rn(*reinterpret_cast<const float2*>(tab + (byte << 7)), ahat2);
       v[4 * j + b] = pack_operand<kF16>(lv.x, lv.y);
     }
   }
@@ -342,7 +358,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     *abort_flag = 0;
     tc::fence_barrier_init();
     if constexpr (!kInt8) {
-      const HalfPairTable* lut = p.fmt == kFmtFp4 ? &kHalfPairsFp4 : &kHalfPairsNf4;
+      const FloatPairTable* lut = p.fmt == kFmtFp4 ? &kPairsFp4 : &kPairsNf4;
       tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
       bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), lut, C::kLutBytes, lut_bar);
     }
@@ -584,7 +600,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       else tc::mbar_arrive(dq_bar(a));
     };
     const int grp = (warp - 2) >> 2;        // takes the stages gs % kGroups == grp
-    const uint8_t* tab = smem + C::kOffLut + 4 * lane;
+    const uint8_t* tab = smem + C::kOffLut + 8 * (lane & 15);
     // block scale: 4-bit ahat = fl32(fl32(a8 s2) / 255); int8 absmax / 127
     auto block_scale = [&](uint32_t a8v, float sv) {
       return kInt8 ? div_by_const<127>(sv) : dequant_absmax(a8v, sv);
