@@ -32,13 +32,19 @@
 //     next unit are already under way.
 //
 // Both directions walk the weight along its rows, one thread per (row, 64
-// columns) run, which is one absmax block. A 4-bit code byte gives both
-// levels from one 8-byte lookup in a 256-entry fp32 level pair table kept
-// in 16 copies (each half-warp's lookups hit 32 distinct banks; measured 1%
-// faster than fp16 pairs in 32 copies, which need widening, and the levels
-// are then exact); an int8 byte is converted directly. Either is multiplied
-// in fp32 by the block's dequantized absmax (for int8, absmax / 127), a
-// register, and rounded to the operand type.
+// columns) run, which is one absmax block. Forward: a 4-bit code byte gives
+// both levels from one 8-byte lookup in a 256-entry fp32 level pair table
+// kept in 16 copies (each half-warp's lookups hit 32 distinct banks;
+// measured 1% faster than fp16 pairs in 32 copies, which need widening, and
+// the levels are then exact), multiplied in fp32 by the block's dequantized
+// absmax, a register, and rounded to the operand type. Input gradient: the
+// thread first scales and rounds the 16 levels for its run the same way and
+// keeps them as byte planes in 8 registers, from which byte permutes pick
+// the operands: no shared-memory lookups, whose wavefronts there compete
+// with the A-tile stores and the tensor core's operand reads (7% faster
+// alone, 5% in the decoder layer; the forward, with A in tensor memory,
+// measured 2.5% slower with planes and keeps the table). Both give the same
+// operand bits. An int8 byte is converted directly and scaled by absmax / 127.
 //
 // Forward: the tile is 128 weight rows, the reduction runs along a row, so a
 // thread's run is K-contiguous and goes straight into tensor memory (one
@@ -128,7 +134,10 @@ struct Cfg {
   // arrivals that free an accumulator buffer: the epilogue warps, or with a
   // single buffer the dequant warps that drain it, of both CTAs of a pair
   static constexpr int kDrainWarps = kAccBufs == 2 ? kEpiWarps : kDqWarps;
-  static constexpr int kLutBytes = kInt8 ? 0 : kPairTableBytes;
+  // 4-bit operands from per-run byte planes in registers (the 16 fp32 levels
+  // in shared memory) instead of the pair table: the input gradient only
+  static constexpr bool kPlanes = kDx && !kInt8;
+  static constexpr int kLutBytes = kInt8 ? 0 : kPlanes ? 128 : kPairTableBytes;
   static constexpr int kOffAct = 0;
   static constexpr int kOffA = kOffAct + kStages * kActStageBytes;   // 1 KB aligned
   static constexpr int kOffCodes = kOffA + kASlots * kAStageBytes;
@@ -245,6 +254,53 @@ __device__ __forceinline__ void dequant16_4bit(const uint4 c, const uint8_t* tab
   }
 }
 
+// The 16 levels of a 4-bit format times one block's scale, rounded to the
+// operand type, as byte planes: lo[q] holds the low bytes of levels 4 q ..
+// 4 q + 3 (level 4 q in byte 0), hi[q] their high bytes. The products and
+// roundings are those of the pair-table path, so the operands are the same.
+template <bool kF16>
+__device__ __forceinline__ void level_planes(const float* lev, float ahat, uint32_t (&lo)[4],
+                                             uint32_t (&hi)[4]) {
+  const float4* l4 = reinterpret_cast<const float4*>(lev);
+  const float2 a2 = make_float2(ahat, ahat);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 l = l4[q];
+    const float2 p0 = __fmul2_rn(make_float2(l.x, l.y), a2);
+    const float2 p1 = __fmul2_rn(make_float2(l.z, l.w), a2);
+    const uint32_t w0 = pack_operand<kF16>(p0.x, p0.y), w1 = pack_operand<kF16>(p1.x, p1.y);
+    lo[q] = __byte_perm(w0, w1, 0x6420u);
+    hi[q] = __byte_perm(w0, w1, 0x7531u);
+  }
+}
+
+// 16 code bytes (32 weights) -> 16 packed operand words from the byte planes
+// of one block's scaled levels. Per 16-bit half of a code word (four codes),
+// a byte permute indexed by the codes' low three bits picks among levels 0-7,
+// a second among levels 8-15, and a third between the two by bit 3, for the
+// low and the high bytes alike; two more interleave low and high bytes into
+// operand pairs, the high nibble of a byte (the even element) in the low half.
+template <bool kF16>
+__device__ __forceinline__ void dequant16_4bit_planes(const uint4 c, const uint32_t (&lo)[4],
+                                                      const uint32_t (&hi)[4], uint32_t (&v)[16]) {
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t m = words[j] & 0x77777777u;
+    const uint32_t s = ((words[j] >> 1) & 0x44444444u) | 0x32103210u;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t mh = m >> (16 * hf), sh = s >> (16 * hf);
+      const uint32_t l =
+          __byte_perm(__byte_perm(lo[0], lo[1], mh), __byte_perm(lo[2], lo[3], mh), sh);
+      const uint32_t h =
+          __byte_perm(__byte_perm(hi[0], hi[1], mh), __byte_perm(hi[2], hi[3], mh), sh);
+      v[4 * j + 2 * hf] = __byte_perm(l, h, 0x4051u);
+      v[4 * j + 2 * hf + 1] = __byte_perm(l, h, 0x6273u);
+    }
+  }
+}
+
 // 16 int8 weights -> 8 packed operand words.
 template <bool kF16>
 __device__ __forceinline__ void dequant16_int8(const uint4 c, float2 ahat2, uint32_t* v) {
@@ -357,7 +413,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     tc::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
-    if constexpr (!kInt8) {
+    if constexpr (C::kPlanes) {
+      // level i is the first of the pair of byte 16 i (copy 0)
+      const FloatPairTable* lut = p.fmt == kFmtFp4 ? &kPairsFp4 : &kPairsNf4;
+      float* lev = reinterpret_cast<float*>(smem + C::kOffLut);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lev[i] = __uint_as_float(lut->w[i * 16 * 16 * 2]);
+      tc::mbar_arrive(lut_bar);
+    } else if constexpr (!kInt8) {
       const FloatPairTable* lut = p.fmt == kFmtFp4 ? &kPairsFp4 : &kPairsNf4;
       tc::mbar_arrive_expect_tx(lut_bar, C::kLutBytes);
       bulk_copy_g2s(tc::smem_addr(smem + C::kOffLut), lut, C::kLutBytes, lut_bar);
@@ -699,6 +762,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         const uint32_t ph = (g / kStages) & 1;
         const float ahat = ok ? block_scale(a8v, sv) : 0.0f;
         const float2 ahat2 = make_float2(ahat, ahat);
+        uint32_t plo[4], phi[4];
+        if constexpr (C::kPlanes)
+          level_planes<kF16>(reinterpret_cast<const float*>(smem + C::kOffLut), ahat, plo, phi);
         load_scale(i + kGroups);
         if constexpr (!kDx) {
           // warp-uniform: the stage is done by all lanes or by none (the
@@ -723,8 +789,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
                 dequant16_int8<kF16>(w, ahat2, v + 8 * cc);
               }
             } else {
-              dequant16_4bit<kF16>(
-                  *reinterpret_cast<const uint4*>(cst + tile_row * 32 + 16 * hf), tab, ahat2, v);
+              if constexpr (C::kPlanes)
+                dequant16_4bit_planes<kF16>(
+                    *reinterpret_cast<const uint4*>(cst + tile_row * 32 + 16 * hf), plo, phi, v);
+              else
+                dequant16_4bit<kF16>(
+                    *reinterpret_cast<const uint4*>(cst + tile_row * 32 + 16 * hf), tab, ahat2, v);
             }
             tc::tmem_st16(dst + 16u * hf, v);
           }
@@ -763,9 +833,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
             } else {
               // row rr's chunk 2 h + hf of 64 bytes, 64-byte swizzle
               const int csw = (rr >> 1) & 3;
-              dequant16_4bit<kF16>(
-                  *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw)), tab,
-                  ahat2, v);
+              if constexpr (C::kPlanes)
+                dequant16_4bit_planes<kF16>(
+                    *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw)), plo,
+                    phi, v);
+              else
+                dequant16_4bit<kF16>(
+                    *reinterpret_cast<const uint4*>(cst + rr * 64 + 16 * ((2 * h + hf) ^ csw)), tab,
+                    ahat2, v);
             }
             // columns 32 hf + 8 j .. + 7 form chunk 4 hf + j of the atom row
 #pragma unroll
