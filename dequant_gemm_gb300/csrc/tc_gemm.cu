@@ -537,6 +537,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     // pipeline. The ring runs on across units.
     const uint32_t tx = static_cast<uint32_t>(kActStageBytes + kCodesStageBytes);
     int gs = 0;                    // stages issued (across units)
+    int slot = 0;                  // gs % kStages
+    uint32_t ph = 0;               // (gs / kStages) & 1
     bool stop = false;
     for (int u = cid; u < p.units && !stop; u += ncl) {
       const Unit t = unit_at(u);
@@ -544,8 +546,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       for (int i = 0; i < t.nst; ++i, ++gs) {
         // one vote, so that the lanes leave together
         if (__any_sync(0xffffffffu, *abort_flag != 0)) { stop = true; break; }
-        const int slot = gs % kStages;
-        const uint32_t ph = (gs / kStages) & 1;
         // every lane waits (a wait in lane 0 alone, the others parked at the
         // shuffle, was measured 4% slower on the prefill forward: the warp
         // reconverged late after each stage), then lane 0's outcome decides
@@ -576,6 +576,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
           }
         }
         __syncwarp();
+        if (++slot == kStages) {
+          slot = 0;
+          ph ^= 1u;
+        }
       }
     }
     if (*abort_flag && lane == 0) {  // let copies in flight land before the CTA exits
@@ -601,6 +605,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
       // (2 g + h) KB, i.e. 1 KB apart along M and 2 KB along K
       const uint64_t adesc0 = tc::sw128_mnmajor_desc(tc::smem_addr(smem + C::kOffA), 1024, 2048);
       int gs = 0, k = 0;
+      // ring positions kept as counters, as in the producer: divisions by the
+      // ring depth (12 at 64 tokens) on this warp's per-stage path cost the
+      // forward 1-1.6%
+      int sl = 0, as = 0;      // gs % kStages, gs % kASlots
+      uint32_t aph = 0;        // (gs / kASlots) & 1
       bool stop = false;
       for (int u = cid; u < p.units && !stop; u += ncl, ++k) {
         const Unit t = unit_at(u);
@@ -616,10 +625,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
         tc::fence_after_sync();
         for (int i = 0; i < t.nst; ++i, ++gs) {
-          const int sl = gs % kStages;
-          const int as = gs % kASlots;
-          r = tc::mbar_spin_abortable<kPair>(dq_bar(as), (gs / kASlots) & 1, abort_flag,
-                                             p.mma_wait_limit);
+          r = tc::mbar_spin_abortable<kPair>(dq_bar(as), aph, abort_flag, p.mma_wait_limit);
           r = __shfl_sync(0xffffffffu, r, 0);
           if (r != tc::kWaitDone) {
             if (lane == 0 && r == tc::kWaitTimeout) fail(kRoleMma);
@@ -645,6 +651,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
             if constexpr (kDx) tc::mma_commit<kCg>(afree_bar(as));
           }
           __syncwarp();
+          if (++sl == kStages) sl = 0;
+          if (++as == kASlots) {
+            as = 0;
+            aph ^= 1u;
+          }
         }
         if (stop) break;
         if (tc::elect_one()) tc::mma_commit<kCg>(accf_bar(b));   // the unit's accumulator is done
