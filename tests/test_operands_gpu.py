@@ -1,0 +1,76 @@
+"""The tensor-core kernels feed the MMA exactly the dequantized weight rounded
+to the operand type.
+
+With one-hot activations every output element is one weight times 1.0 plus
+exact zeros, so the fused forward returns the transpose of the operand matrix
+and the input gradient the matrix itself, whatever the reduction order or the
+split of the reduction. The operand matrix is the oracle's fp32 dequantized
+weight rounded to nearest even in bf16 (fp16 with fp16 activations). This
+pins, element by element, the forward's level pair tables, the input
+gradient's byte-plane permutes and the int8 conversion, which the fp64
+tolerance tests can only bound. Weights stay in the normal range of both
+operand types (the smallest nonzero dequantized weight here is ~1e-3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import dequant_gemm_gb300 as nf4
+from dequant_gemm_gb300 import workloads as wl
+from oracle import nf4_oracle as o
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+FORMATS = ("nf4", "fp4", "int8")
+ACTS = (torch.bfloat16, torch.float16)
+
+
+def oracle_operands(W, dtype, act):
+    """fp32 dequantized weight rounded to the operand type, as fp32. 4-bit:
+    the oracle's dequantized weight. int8: the fused kernels scale a block
+    by its step fl32(a / 127), computed once, so the operand is
+    fl32(q * fl32(a / 127)) from the oracle's codes and absmax (the
+    stand-alone dequantize rounds fl32(q * a) / 127 instead; the two differ
+    by at most an fp32 ulp)."""
+    rows, cols = W.shape
+    if dtype == "int8":
+        qv, a = o.int8_quantize_flat(W.reshape(-1))
+        step = (np.asarray(a, dtype=np.float32) / np.float32(127.0)).astype(np.float32)
+        What = (qv.reshape(-1, 64).astype(np.float32) * step[:, None]).astype(np.float32)
+        What = What.reshape(rows, cols)
+    else:
+        lv = o.levels_of(dtype)
+        What = o.dequantize(*o.quantize(W, lv), rows, cols, lv)
+    return torch.from_numpy(np.ascontiguousarray(What, dtype=np.float32)).to(act).float()
+
+
+def one_hot(m, k, act):
+    X = torch.zeros(m, k, dtype=act)
+    X[torch.arange(m), torch.arange(m)] = 1.0
+    return X
+
+
+@pytest.mark.parametrize("act", ACTS, ids=("bf16", "f16"))
+@pytest.mark.parametrize("dtype", FORMATS)
+@pytest.mark.parametrize("N,K", [(384, 256), (256, 640)])
+def test_forward_operands_are_the_rounded_dequantized_weight(dtype, act, N, K):
+    W = wl.weight(N, K, seed=29).numpy()
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
+    X = one_hot(K, K, act).to(DEV)          # K tokens: above the small-M path
+    Y = nf4.nf4_matmul_fwd(X, q).cpu()
+    ref = oracle_operands(W, dtype, act).t()
+    bad = (Y != ref).sum().item()
+    assert bad == 0, f"{bad} of {Y.numel()} operands differ"
+
+
+@pytest.mark.parametrize("act", ACTS, ids=("bf16", "f16"))
+@pytest.mark.parametrize("dtype", FORMATS)
+@pytest.mark.parametrize("N,K", [(384, 256), (640, 512)])
+def test_input_gradient_operands_are_the_rounded_dequantized_weight(dtype, act, N, K):
+    W = wl.weight(N, K, seed=31).numpy()
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
+    dY = one_hot(N, N, act).to(DEV)         # N tokens, one per weight row
+    dX = nf4.nf4_matmul_bwd_dx(dY, q).cpu()
+    ref = oracle_operands(W, dtype, act)
+    bad = (dX != ref).sum().item()
+    assert bad == 0, f"{bad} of {dX.numel()} operands differ"
