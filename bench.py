@@ -744,10 +744,11 @@ def config_record(r):
 def run_naive(args, dev):
     """The fused NF4 forward against the naive path that the pages' speed claim
     compares with: dequantize the whole weight to fp32 in HBM, cast it to bf16,
-    then a cuBLAS bf16 matmul (torch.matmul) widened to fp32. Same inputs, same
-    output shape and dtype. Both timed with CUDA events on the current stream
-    after 3 warm-ups, without an L2 flush (a weight smaller than L2 stays warm
-    for both). One JSON line for the workload."""
+    then a cuBLAS bf16 matmul (torch.matmul) widened to fp32; and against the
+    leaner form that dequantizes straight to bf16 (nf4_dequantize_ex). Same
+    inputs, same output shape and dtype. All timed with CUDA events on the
+    current stream after 3 warm-ups, without an L2 flush (a weight smaller
+    than L2 stays warm for all). One JSON line for the workload."""
     import dequant_gemm_gb300 as nf4
     work = wl.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(dev)
@@ -775,8 +776,12 @@ def run_naive(args, dev):
             t_naive = time_ms(
                 lambda: torch.matmul(X, nf4.nf4_dequantize(q).to(torch.bfloat16).t()).float(),
                 args.steps)
+            t_bf16 = time_ms(
+                lambda: torch.matmul(X, nf4.nf4_dequantize(q, out_dtype=torch.bfloat16).t()).float(),
+                args.steps)
             rows.append({"projection": f"{p.name} {p.rows}x{p.cols}", "M": M,
-                         "fused_ms": t_fused, "naive_ms": t_naive, "speedup": t_naive / t_fused})
+                         "fused_ms": t_fused, "naive_ms": t_naive, "speedup": t_naive / t_fused,
+                         "naive_bf16_ms": t_bf16, "speedup_bf16": t_bf16 / t_fused})
     status = nf4.nf4_poll_device_status(dev)
     if status != 0:
         raise SystemExit(f"device status {status}")

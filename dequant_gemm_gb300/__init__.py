@@ -29,7 +29,7 @@ STATUS = {
 }
 
 # Every symbol the header declares, for load checks.
-EXPORTS = ("nf4_quantize", "nf4_quantize_ex", "nf4_dequantize", "nf4_matmul_fwd",
+EXPORTS = ("nf4_quantize", "nf4_quantize_ex", "nf4_dequantize", "nf4_dequantize_ex", "nf4_matmul_fwd",
            "nf4_matmul_bwd_dx", "nf4_matmul_fwd_ex", "nf4_matmul_bwd_dx_ex", "nf4_matmul_fwd_group",
            "nf4_poll_device_status", "nf4_poll_device_status_site", "nf4_codebook",
            "nf4_codebook_of", "nf4_set_mma_wait_limit", "nf4_last_cuda_error",
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
                 "nf4_quantize": [vp, i64, i64, i32, vp, vp, vp, vp],
                 "nf4_quantize_ex": [vp, i32, i64, i64, i32, i32, vp, vp, vp, vp],
                 "nf4_dequantize": [W, vp, vp],
+                "nf4_dequantize_ex": [W, vp, i32, vp],
                 "nf4_matmul_fwd": [vp, i64, W, vp, vp],
                 "nf4_matmul_bwd_dx": [vp, i64, W, vp, vp],
                 "nf4_matmul_fwd_ex": [vp, i32, i64, W, vp, i32, i32, vp],
@@ -244,18 +245,26 @@ def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None,
     return q
 
 
-def nf4_dequantize(w: NF4Weight, out: torch.Tensor | None = None) -> torch.Tensor:
-    """fp32 [rows, cols] dequantized weight (for checks and export only)."""
+def nf4_dequantize(w: NF4Weight, out: torch.Tensor | None = None,
+                   out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """[rows, cols] dequantized weight in fp32, or rounded to nearest even in
+    bf16 or fp16 (for export and for library GEMMs)."""
+    if out is not None:
+        if not isinstance(out, torch.Tensor):
+            raise ValueError("out must be a tensor")
+        out_dtype = out.dtype
+    if out_dtype not in ELEM:
+        raise ValueError(f"nf4_dequantize: output dtype {out_dtype} is not fp32, bf16 or fp16")
     _check_weight(w, w.device)
     if out is not None:
-        _require(out, "out", torch.float32, shape=(w.rows, w.cols))
+        _require(out, "out", out_dtype, shape=(w.rows, w.cols))
         _same_device(w.device, out=out)
     _require_cuda_device(w.device)
-    y = out if out is not None else torch.empty(w.rows, w.cols, dtype=torch.float32,
-                                                device=w.device)
+    y = out if out is not None else torch.empty(w.rows, w.cols, dtype=out_dtype, device=w.device)
     s = w.c_struct()
     with torch.cuda.device(w.device):
-        _check("nf4_dequantize", lib().nf4_dequantize(ctypes.byref(s), _ptr(y), _stream(w.device)))
+        _check("nf4_dequantize_ex", lib().nf4_dequantize_ex(ctypes.byref(s), _ptr(y), ELEM[out_dtype],
+                                                           _stream(w.device)))
     return y
 
 

@@ -223,8 +223,9 @@ nf4_status nf4_quantize_ex(const void* W, int32_t w_elem, int64_t rows, int64_t 
   return quantize(W, w_elem, rows, cols, blocksize, dtype, codes, absmax_q, absmax_scale, stream);
 }
 
-nf4_status nf4_dequantize(const nf4_weight* w, float* W_out, void* stream) {
+nf4_status nf4_dequantize_ex(const nf4_weight* w, void* W_out, int32_t out_elem, void* stream) {
   if (nf4_status s = check_weight(w)) return s;
+  if (out_elem != NF4_F32 && out_elem != NF4_BF16 && out_elem != NF4_F16) return NF4_ERR_SHAPE;
   if (w->rows == 0 || w->cols == 0) return NF4_OK;
   if (nf4_status s = check_weight_ptrs(w)) return s;
   if (!W_out) return NF4_ERR_NULL;
@@ -232,8 +233,12 @@ nf4_status nf4_dequantize(const nf4_weight* w, float* W_out, void* stream) {
   DeviceInfo* d = nullptr;
   if (nf4_status s = current_device(&d)) return s;
   return launched(nf4::launch_dequantize(w->dtype, w->codes, w->absmax_q, w->absmax_scale,
-                                         w->rows * w->cols, W_out,
+                                         w->rows * w->cols, W_out, out_elem,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+nf4_status nf4_dequantize(const nf4_weight* w, float* W_out, void* stream) {
+  return nf4_dequantize_ex(w, W_out, NF4_F32, stream);
 }
 
 nf4_status nf4_matmul_fwd(const uint16_t* X, int64_t M, const nf4_weight* w, float* Y,

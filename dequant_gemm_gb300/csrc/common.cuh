@@ -182,8 +182,9 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
 // int8 (codes = int8 values, s2 = fp32 absmax per block, a8 unused).
 cudaError_t launch_quantize(const void* W, bool w_bf16, int fmt, int64_t n_elems, uint8_t* codes,
                             uint8_t* a8, float* s2, cudaStream_t st);
+// out: n_elems of out_elem (NF4_F32, NF4_BF16 or NF4_F16).
 cudaError_t launch_dequantize(int fmt, const uint8_t* codes, const uint8_t* a8, const float* s2,
-                              int64_t n_elems, float* out, cudaStream_t st);
+                              int64_t n_elems, void* out, int out_elem, cudaStream_t st);
 cudaError_t launch_gemv_fwd(const MatmulCall& c);
 // One launch for `count` (1 .. kGemvGroupMax) weights that share the
 // activations, K, the data type, the element types, the flags and the

@@ -269,11 +269,34 @@ quantize_int8_kernel(const void* __restrict__ W, int64_t n_blocks, int8_t* __res
   }
 }
 
+// Output element types of the stand-alone dequantize: fp32, or the fp32
+// value rounded to nearest even in bf16 or fp16.
+constexpr int kOutF32 = 0, kOutBf16 = 1, kOutF16 = 2;
+
+// Four dequantized weights to out + 4 e (elements), as fp32 or rounded to
+// 16 bits; streaming stores (the output is not read back here).
+template <int kOut>
+__device__ __forceinline__ void store4(void* out, int64_t e, float4 r) {
+  if constexpr (kOut == kOutF32) {
+    __stcs(reinterpret_cast<float4*>(out) + e, r);
+  } else {
+    uint2 v;
+    if constexpr (kOut == kOutBf16) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(r.x, r.y), b = __floats2bfloat162_rn(r.z, r.w);
+      v = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+      const __half2 a = __floats2half2_rn(r.x, r.y), b = __floats2half2_rn(r.z, r.w);
+      v = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+    __stcs(reinterpret_cast<uint2*>(out) + e, v);
+  }
+}
+
 // Dequantize (4-bit): one thread per 32 weights (16 code bytes, half a block).
-template <int kFmt>
+template <int kFmt, int kOut>
 __global__ void __launch_bounds__(256)
 dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ a8,
-                  const float* __restrict__ s2, int64_t n_chunks, float* __restrict__ out) {
+                  const float* __restrict__ s2, int64_t n_chunks, void* __restrict__ out) {
   __shared__ float s_levels[16];
   if (threadIdx.x < 16)
     s_levels[threadIdx.x] = __uint_as_float(kFmt == kFmtFp4 ? kFp4LevelBitsDev[threadIdx.x]
@@ -285,7 +308,6 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__
   const float ahat = dequant_absmax(a8[blk], s2[blk / kGroup]);
   const uint4 c = __ldg(reinterpret_cast<const uint4*>(codes) + i);
   const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-  float4* o = reinterpret_cast<float4*>(out) + i * 8;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t w = words[j];
@@ -297,21 +319,21 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__
       r.y = __fmul_rn(s_levels[b0 & 15], ahat);
       r.z = __fmul_rn(s_levels[b1 >> 4], ahat);
       r.w = __fmul_rn(s_levels[b1 & 15], ahat);
-      __stcs(o + 2 * j + h, r);
+      store4<kOut>(out, i * 8 + 2 * j + h, r);
     }
   }
 }
 
 // Dequantize (int8): w = fl32(fl32(q * a) / 127); one thread per 16 weights.
+template <int kOut>
 __global__ void __launch_bounds__(256)
 dequantize_int8_kernel(const int8_t* __restrict__ q, const float* __restrict__ absmax,
-                       int64_t n_chunks, float* __restrict__ out) {
+                       int64_t n_chunks, void* __restrict__ out) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n_chunks) return;
   const float a = absmax[i >> 2];
   const uint4 c = __ldg(reinterpret_cast<const uint4*>(q) + i);
   const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-  float4* o = reinterpret_cast<float4*>(out) + i * 4;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float r[4];
@@ -320,8 +342,26 @@ dequantize_int8_kernel(const int8_t* __restrict__ q, const float* __restrict__ a
       const int v = static_cast<int8_t>((words[j] >> (8 * e)) & 0xffu);
       r[e] = div_by_const<127>(__fmul_rn(static_cast<float>(v), a));
     }
-    __stcs(o + j, make_float4(r[0], r[1], r[2], r[3]));
+    store4<kOut>(out, i * 4 + j, make_float4(r[0], r[1], r[2], r[3]));
   }
+}
+
+template <int kOut>
+void launch_dq(int fmt, const uint8_t* codes, const uint8_t* a8, const float* s2, int64_t n_elems,
+               void* out, cudaStream_t st) {
+  if (fmt == kFmtInt8) {
+    const int64_t n_chunks = n_elems / 16;
+    const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
+    dequantize_int8_kernel<kOut><<<grid, 256, 0, st>>>(reinterpret_cast<const int8_t*>(codes), s2,
+                                                       n_chunks, out);
+    return;
+  }
+  const int64_t n_chunks = n_elems / 32;
+  const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
+  if (fmt == kFmtFp4)
+    dequantize_kernel<kFmtFp4, kOut><<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
+  else
+    dequantize_kernel<kFmtNf4, kOut><<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
 }
 
 template <int kFmt, bool kBf16>
@@ -358,18 +398,10 @@ cudaError_t launch_quantize(const void* W, bool w_bf16, int fmt, int64_t n_elems
 }
 
 cudaError_t launch_dequantize(int fmt, const uint8_t* codes, const uint8_t* a8, const float* s2,
-                              int64_t n_elems, float* out, cudaStream_t st) {
-  if (fmt == kFmtInt8) {
-    const int64_t n_chunks = n_elems / 16;
-    const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
-    dequantize_int8_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const int8_t*>(codes), s2,
-                                                 n_chunks, out);
-    return cudaGetLastError();
-  }
-  const int64_t n_chunks = n_elems / 32;
-  const unsigned grid = static_cast<unsigned>((n_chunks + 255) / 256);
-  if (fmt == kFmtFp4) dequantize_kernel<kFmtFp4><<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
-  else dequantize_kernel<kFmtNf4><<<grid, 256, 0, st>>>(codes, a8, s2, n_chunks, out);
+                              int64_t n_elems, void* out, int out_elem, cudaStream_t st) {
+  if (out_elem == NF4_BF16) launch_dq<kOutBf16>(fmt, codes, a8, s2, n_elems, out, st);
+  else if (out_elem == NF4_F16) launch_dq<kOutF16>(fmt, codes, a8, s2, n_elems, out, st);
+  else launch_dq<kOutF32>(fmt, codes, a8, s2, n_elems, out, st);
   return cudaGetLastError();
 }
 

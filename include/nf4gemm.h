@@ -153,6 +153,15 @@ nf4_status nf4_quantize_ex(const void* W, int32_t w_elem, int64_t rows, int64_t 
  * checking and export. */
 nf4_status nf4_dequantize(const nf4_weight* w, float* W_out, void* stream);
 
+/* Dequantize to fp32, fp16 or bf16 ("bitsandbytes", 4-bit paragraph: 4-bit
+ * weights dequantized to float16 or float32; bf16, the tensor-core operand
+ * type of the fused kernels, is this library's addition). W_out: device
+ * [rows, cols] of out_elem NF4_F32, NF4_F16 or NF4_BF16 (output, 16-byte
+ * aligned). A 16-bit output is the fp32 value of nf4_dequantize rounded to
+ * nearest even (fp16 overflows to infinity beyond 65504). NF4_ERR_SHAPE for
+ * another out_elem, before any device access. */
+nf4_status nf4_dequantize_ex(const nf4_weight* w, void* W_out, int32_t out_elem, void* stream);
+
 /* Fused forward Y = X * dequant(W)^T ("Zenbit", zenbit.pallas_nf4 bullet;
  * "bitsandbytes", quantized-GEMM paragraph). The dequantized weight exists
  * only in registers, shared memory and tensor memory.

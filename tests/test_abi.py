@@ -200,3 +200,34 @@ def test_valid_group_call_without_device_reports_device_error():
     ws = (nf4.nf4_weight * 2)(a, a)
     assert nf4.lib().nf4_matmul_fwd_group(P, 1, 4, ws, 2, (ctypes.c_void_p * 2)(P, P), 0, 0,
                                           None) == 5
+
+
+def test_dequantize_ex_validation():
+    L = nf4.lib()
+    w = _weight(codes=P, a8=P, s2=P)
+    g = L.nf4_dequantize_ex
+    assert g(ctypes.byref(w), P, 3, None) == 2           # unknown output type
+    assert g(ctypes.byref(w), P, -1, None) == 2
+    assert g(ctypes.byref(w), None, 1, None) == 1        # no output
+    assert g(ctypes.byref(w), P + 8, 2, None) == 3       # misaligned output
+    empty = nf4.nf4_weight(P, P, P, 0, 64, 64, 256, 0)
+    assert g(ctypes.byref(empty), None, 1, None) == 0    # nothing to write
+    assert g(None, P, 0, None) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_dequantize_ex_without_device_reports_device_error():
+    w = _weight(codes=P, a8=P, s2=P)
+    for elem in (0, 1, 2):
+        assert nf4.lib().nf4_dequantize_ex(ctypes.byref(w), P, elem, None) == 5
+
+
+def test_dequantize_binding_rejects_bad_output_types():
+    w = nf4.NF4Weight(torch.zeros(256, dtype=torch.uint8), torch.zeros(8, dtype=torch.uint8),
+                      torch.zeros(1), 8, 64)
+    with pytest.raises(ValueError):
+        nf4.nf4_dequantize(w, out_dtype=torch.int32)
+    with pytest.raises(ValueError):
+        nf4.nf4_dequantize(w, out=torch.zeros(8, 64, dtype=torch.float64))
+    with pytest.raises(ValueError):
+        nf4.nf4_dequantize(w, out=torch.zeros(8, 32, dtype=torch.bfloat16))

@@ -144,6 +144,31 @@ def test_quantize_bf16_full_size():
     assert_quant_equal(q, o.quantize(W32), "nf4")
 
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16], ids=("bf16", "f16"))
+@pytest.mark.parametrize("dtype", ["nf4", "fp4", "int8"])
+def test_dequantize_to_16_bits_is_the_rounded_fp32_weight(dtype, out_dtype):
+    """nf4_dequantize_ex: the oracle's fp32 dequantized weight rounded to
+    nearest even, bit for bit (special blocks included: fp16 takes 1e30 to
+    infinity and tiny weights to subnormals or zero, like the rounding on
+    the host)."""
+    rng = np.random.default_rng(9)
+    for W in (special_weight(rng), weight_np(3, 192, 4), weight_np(520, 1024, 8, 0.001)):
+        q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
+        Wd = nf4.nf4_dequantize(q, out_dtype=out_dtype).cpu()
+        ref = torch.from_numpy(oracle_dequant(W, dtype)).to(out_dtype)
+        assert Wd.dtype == out_dtype and Wd.shape == ref.shape
+        assert torch.equal(Wd.view(torch.int16), ref.view(torch.int16))
+    assert nf4.nf4_poll_device_status() == 0
+
+
+def test_dequantize_bf16_full_size_matches_fp32_rounded():
+    q = nf4.nf4_quantize(torch.from_numpy(weight_np(11008, 4096, 0)).to(DEV))
+    out = torch.empty(11008, 4096, dtype=torch.bfloat16, device=DEV)
+    Wb = nf4.nf4_dequantize(q, out=out)
+    assert Wb.data_ptr() == out.data_ptr()
+    assert torch.equal(Wb.view(torch.int16), nf4.nf4_dequantize(q).to(torch.bfloat16).view(torch.int16))
+
+
 # ----------------------------------------------------------------- matmuls --
 def run(W, dtype, A, dx, **kw):
     q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
