@@ -1,5 +1,6 @@
 """The tensor-core kernels feed the MMA exactly the dequantized weight rounded
-to the operand type.
+to the operand type, and the small-M kernel scales exactly the fp16 level it
+multiplies.
 
 With one-hot activations every output element is one weight times 1.0 plus
 exact zeros, so the fused forward returns the transpose of the operand matrix
@@ -74,3 +75,42 @@ def test_input_gradient_operands_are_the_rounded_dequantized_weight(dtype, act, 
     ref = oracle_operands(W, dtype, act)
     bad = (dX != ref).sum().item()
     assert bad == 0, f"{bad} of {dX.numel()} operands differ"
+
+
+def small_m_products(W, dtype):
+    """What the small-M kernel computes for one weight and an activation of
+    1: the code's level rounded to fp16 (the operand its MMAs take; int8: the
+    integer, exact) times the block scale after the MMA, in fp32: â from the
+    oracle for 4-bit codes, fl32(a / 127) for int8."""
+    rows, cols = W.shape
+    if dtype == "int8":
+        qv, a = o.int8_quantize_flat(W.reshape(-1))
+        step = (np.asarray(a, dtype=np.float32) / np.float32(127.0)).astype(np.float32)
+        v = qv.reshape(-1, 64).astype(np.float32) * step[:, None]
+    else:
+        lv = o.levels_of(dtype)
+        packed, a8, s2 = o.quantize(W, lv)
+        q = o.unpack_nibbles(packed).reshape(-1, 64)
+        lv16 = lv.astype(np.float16).astype(np.float32)
+        v = lv16[q] * o.dequant_absmax(a8, s2).astype(np.float32)[:, None]
+    return np.ascontiguousarray(v.astype(np.float32).reshape(rows, cols))
+
+
+@pytest.mark.parametrize("act", ACTS, ids=("bf16", "f16"))
+@pytest.mark.parametrize("dtype", FORMATS)
+@pytest.mark.parametrize("N,K,M", [(512, 4096, 1), (4096, 4096, 16), (1040, 18944, 4),
+                                   (136, 45056, 12), (8200, 1024, 1)])
+def test_small_m_forward_is_exact_on_one_hot_tokens(dtype, act, N, K, M):
+    """Token m carries a single 1 at column k_m (spread over the row), so
+    Y[m, n] is that one weight's product: fp32(level16 * scale), bit for bit
+    (the activation's power-of-two rescale into fp16 and back is exact for
+    1; every other block adds exact zeros)."""
+    W = wl.weight(N, K, seed=37).numpy()
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
+    ks = [(m * (K // M) + 37 * m + 5) % K for m in range(M)]
+    X = torch.zeros(M, K, dtype=act)
+    X[torch.arange(M), torch.tensor(ks)] = 1.0
+    Y = nf4.nf4_matmul_fwd(X.to(DEV), q).cpu()
+    ref = torch.from_numpy(small_m_products(W, dtype)[:, ks].T.copy())
+    bad = (Y != ref).sum().item()
+    assert bad == 0, f"{bad} of {Y.numel()} outputs differ"
