@@ -114,3 +114,39 @@ def test_small_m_forward_is_exact_on_one_hot_tokens(dtype, act, N, K, M):
     ref = torch.from_numpy(small_m_products(W, dtype)[:, ks].T.copy())
     bad = (Y != ref).sum().item()
     assert bad == 0, f"{bad} of {Y.numel()} outputs differ"
+
+
+@pytest.mark.parametrize("act", ACTS, ids=("bf16", "f16"))
+@pytest.mark.parametrize("dtype", FORMATS)
+@pytest.mark.parametrize("M", [17, 64, 100, 200])
+def test_tensor_core_forward_tiles_pick_exact_operands(dtype, act, M):
+    """Every token tile width (64, 128, 256) and split: token m's single 1 at
+    column k_m returns column k_m of the operand matrix."""
+    N, K = 640, 1024
+    W = wl.weight(N, K, seed=41).numpy()
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
+    ks = [(13 * m + 7) % K for m in range(M)]
+    X = torch.zeros(M, K, dtype=act)
+    X[torch.arange(M), torch.tensor(ks)] = 1.0
+    Y = nf4.nf4_matmul_fwd(X.to(DEV), q).cpu()
+    ref = oracle_operands(W, dtype, act)[:, ks].t()
+    bad = (Y != ref).sum().item()
+    assert bad == 0, f"{bad} of {Y.numel()} outputs differ"
+
+
+@pytest.mark.parametrize("act", ACTS, ids=("bf16", "f16"))
+@pytest.mark.parametrize("dtype", FORMATS)
+@pytest.mark.parametrize("M", [1, 5, 64, 100, 200])
+def test_tensor_core_input_gradient_tiles_pick_exact_operands(dtype, act, M):
+    """The input gradient at every token tile width: token m's single 1 at
+    weight row n_m returns row n_m of the operand matrix."""
+    N, K = 640, 1024
+    W = wl.weight(N, K, seed=43).numpy()
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype)
+    ns = [(29 * m + 3) % N for m in range(M)]
+    dY = torch.zeros(M, N, dtype=act)
+    dY[torch.arange(M), torch.tensor(ns)] = 1.0
+    dX = nf4.nf4_matmul_bwd_dx(dY.to(DEV), q).cpu()
+    ref = oracle_operands(W, dtype, act)[ns, :]
+    bad = (dX != ref).sum().item()
+    assert bad == 0, f"{bad} of {dX.numel()} outputs differ"
