@@ -150,3 +150,25 @@ def test_tensor_core_input_gradient_tiles_pick_exact_operands(dtype, act, M):
     ref = oracle_operands(W, dtype, act)[ns, :]
     bad = (dX != ref).sum().item()
     assert bad == 0, f"{bad} of {dX.numel()} outputs differ"
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=("f32", "bf16"))
+@pytest.mark.parametrize("M", [1, 16, 64, 200])
+def test_accumulate_adds_the_exact_product(M, out_dtype):
+    """NF4_ACCUMULATE on one-hot tokens: each output becomes its previous
+    contents plus one product, added once in fp32 (and for a bf16 output
+    rounded to nearest even), on both the small-M and the tensor-core paths."""
+    N, K = 384, 1024
+    W = wl.weight(N, K, seed=47).numpy()
+    q = nf4.nf4_quantize(torch.from_numpy(W).to(DEV))
+    ks = [(11 * m + 3) % K for m in range(M)]
+    X = torch.zeros(M, K, dtype=torch.bfloat16)
+    X[torch.arange(M), torch.tensor(ks)] = 1.0
+    prod = (torch.from_numpy(small_m_products(W, "nf4")) if M <= 16
+            else oracle_operands(W, "nf4", torch.bfloat16))[:, ks].t()
+    Y0 = (torch.randn(M, N, generator=torch.Generator().manual_seed(M)) * 0.05).to(out_dtype)
+    Y = Y0.to(DEV)
+    nf4.nf4_matmul_fwd(X.to(DEV), q, out=Y, accumulate=True)
+    ref = (Y0.float() + prod).to(out_dtype)
+    bad = (Y.cpu() != ref).sum().item()
+    assert bad == 0, f"{bad} of {Y.numel()} outputs differ"
