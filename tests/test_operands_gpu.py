@@ -172,3 +172,22 @@ def test_accumulate_adds_the_exact_product(M, out_dtype):
     ref = (Y0.float() + prod).to(out_dtype)
     bad = (Y.cpu() != ref).sum().item()
     assert bad == 0, f"{bad} of {Y.numel()} outputs differ"
+
+
+@pytest.mark.parametrize("dtype", FORMATS)
+@pytest.mark.parametrize("M", [1, 3, 16])
+def test_grouped_forward_is_exact_on_one_hot_tokens(dtype, M):
+    """nf4_matmul_fwd_group: every weight of the group (different row counts,
+    so the row tiles of one launch switch weights mid-grid) gets its own
+    exact products."""
+    K = 2048
+    Ws = [wl.weight(n, K, seed=50 + n % 7).numpy() for n in (1040, 96, 528, 16)]
+    qs = [nf4.nf4_quantize(torch.from_numpy(W).to(DEV), dtype=dtype) for W in Ws]
+    ks = [(97 * m + 11) % K for m in range(M)]
+    X = torch.zeros(M, K, dtype=torch.bfloat16)
+    X[torch.arange(M), torch.tensor(ks)] = 1.0
+    Ys = nf4.nf4_matmul_fwd_group(X.to(DEV), qs)
+    for W, Y in zip(Ws, Ys):
+        ref = torch.from_numpy(small_m_products(W, dtype)[:, ks].T.copy())
+        bad = (Y.cpu() != ref).sum().item()
+        assert bad == 0, f"{bad} of {Y.numel()} outputs differ (rows {W.shape[0]})"
