@@ -17,6 +17,7 @@ struct DeviceInfo {
   bool ok = false;
   int num_sms = 0;
   int* status = nullptr;  // device address of g_device_status
+  int ordinal = -1;
 };
 
 constexpr int kMaxDevices = 64;
@@ -50,6 +51,7 @@ nf4_status current_device(DeviceInfo** out) {
     d.ok = ok;
     d.num_sms = sms;
     d.status = static_cast<int*>(status);
+    d.ordinal = dev;
     d.checked = true;
   }
   if (!d.ok) return NF4_ERR_DEVICE;
@@ -133,6 +135,7 @@ nf4::MatmulCall make_call(const void* act, int32_t act_elem, int64_t M, const nf
   c.num_sms = d->num_sms;
   c.status = d->status;
   c.wait_limit = g_mma_wait_limit.load(std::memory_order_relaxed);
+  c.device = d->ordinal;
   c.st = st;
   return c;
 }

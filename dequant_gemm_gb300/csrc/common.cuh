@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "nf4gemm.h"
 
 namespace nf4 {
@@ -165,8 +167,19 @@ struct MatmulCall {
   int num_sms;
   int* status;
   long long wait_limit;    // cycles before the MMA issuer's stage wait gives up
+  int device;              // the current device's ordinal
   cudaStream_t st;
 };
+
+// Runs f once per device (a kernel's dynamic shared memory limit is an
+// attribute of the function on each device); beyond the first 64 ordinals,
+// on every call.
+constexpr int kOnceDevices = 64;
+template <typename F>
+void once_per_device(std::once_flag (&flags)[kOnceDevices], int device, F&& f) {
+  if (device >= 0 && device < kOnceDevices) std::call_once(flags[device], f);
+  else f();
+}
 
 }  // namespace nf4
 

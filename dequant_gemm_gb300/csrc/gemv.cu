@@ -697,9 +697,9 @@ static_assert(gemv_smem_bytes(1, kMaxSliceBlocks, 8, false) <= kGemvSmemLimit, "
 // (32 rows, 8 K-parts).
 template <int NT, int kFmt, bool kF16, bool kWide, int kR>
 cudaError_t launch_gemv_kernel(const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
-                               const GemvArgs& a) {
-  static std::once_flag once;
-  std::call_once(once, [] {
+                               const GemvArgs& a, int device) {
+  static std::once_flag once[kOnceDevices];
+  once_per_device(once, device, [] {
     cudaFuncSetAttribute(gemv_fwd_kernel<NT, kFmt, kF16, kWide, kR>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(kGemvSmemLimit));
@@ -708,22 +708,22 @@ cudaError_t launch_gemv_kernel(const cudaLaunchConfig_t& cfg, const GemvMaps& tm
 }
 
 template <int NT, int kFmt, bool kF16, bool kWide>
-cudaError_t launch_gemv_r(int r, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
+cudaError_t launch_gemv_r(int r, int device, const cudaLaunchConfig_t& cfg, const GemvMaps& tm,
                           const GemvArgs& a) {
-  return r == 2 ? launch_gemv_kernel<NT, kFmt, kF16, kWide, 2>(cfg, tm, a)
-                : launch_gemv_kernel<NT, kFmt, kF16, kWide, kMaxRowGroups>(cfg, tm, a);
+  return r == 2 ? launch_gemv_kernel<NT, kFmt, kF16, kWide, 2>(cfg, tm, a, device)
+                : launch_gemv_kernel<NT, kFmt, kF16, kWide, kMaxRowGroups>(cfg, tm, a, device);
 }
 
 template <int kFmt, bool kF16>
-cudaError_t launch_gemv_as(int nt, bool wide, int r, const cudaLaunchConfig_t& cfg,
+cudaError_t launch_gemv_as(int nt, bool wide, int r, int device, const cudaLaunchConfig_t& cfg,
                            const GemvMaps& tm, const GemvArgs& a) {
   if constexpr (kFmt != kFmtInt8) {
     if (wide)
-      return nt == 1 ? launch_gemv_r<1, kFmt, kF16, true>(r, cfg, tm, a)
-                     : launch_gemv_r<2, kFmt, kF16, true>(r, cfg, tm, a);
+      return nt == 1 ? launch_gemv_r<1, kFmt, kF16, true>(r, device, cfg, tm, a)
+                     : launch_gemv_r<2, kFmt, kF16, true>(r, device, cfg, tm, a);
   }
-  return nt == 1 ? launch_gemv_r<1, kFmt, kF16, false>(r, cfg, tm, a)
-                 : launch_gemv_r<2, kFmt, kF16, false>(r, cfg, tm, a);
+  return nt == 1 ? launch_gemv_r<1, kFmt, kF16, false>(r, device, cfg, tm, a)
+                 : launch_gemv_r<2, kFmt, kF16, false>(r, device, cfg, tm, a);
 }
 
 cudaError_t launch_gemv_fwd(const MatmulCall& c) { return launch_gemv_group(&c, 1); }
@@ -881,12 +881,12 @@ cudaError_t launch_gemv_group(const MatmulCall* cs, int count) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   switch (c.fmt * 2 + (c.act_f16 ? 1 : 0)) {
-    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, best.wide, best.r, cfg, tm, a);
-    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, best.wide, best.r, cfg, tm, a);
-    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, best.wide, best.r, cfg, tm, a);
-    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, best.wide, best.r, cfg, tm, a);
-    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, best.wide, best.r, cfg, tm, a);
-    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, best.wide, best.r, cfg, tm, a);
+    case kFmtNf4 * 2: return launch_gemv_as<kFmtNf4, false>(nt, best.wide, best.r, c.device, cfg, tm, a);
+    case kFmtNf4 * 2 + 1: return launch_gemv_as<kFmtNf4, true>(nt, best.wide, best.r, c.device, cfg, tm, a);
+    case kFmtFp4 * 2: return launch_gemv_as<kFmtFp4, false>(nt, best.wide, best.r, c.device, cfg, tm, a);
+    case kFmtFp4 * 2 + 1: return launch_gemv_as<kFmtFp4, true>(nt, best.wide, best.r, c.device, cfg, tm, a);
+    case kFmtInt8 * 2: return launch_gemv_as<kFmtInt8, false>(nt, best.wide, best.r, c.device, cfg, tm, a);
+    case kFmtInt8 * 2 + 1: return launch_gemv_as<kFmtInt8, true>(nt, best.wide, best.r, c.device, cfg, tm, a);
   }
   return cudaErrorInvalidValue;
 }

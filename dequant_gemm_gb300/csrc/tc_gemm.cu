@@ -1011,8 +1011,8 @@ cudaError_t launch_tc(const MatmulCall& c) {
                  static_cast<uint64_t>(nd) * out_elem, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
 
-  static std::once_flag once;
-  std::call_once(once, [] {
+  static std::once_flag once[kOnceDevices];
+  once_per_device(once, c.device, [] {
     cudaFuncSetAttribute(tc_gemm_kernel<kDx, kBN, kF16, kInt8>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
